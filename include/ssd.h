@@ -1,0 +1,168 @@
+/*
+ * ssd.h -- C ABI of the GB300 (sm_103a) Mamba-2 chunked SSD forward library.
+ *
+ * The operation (source: "Jane Street ML Engineers Map Mamba-2 Recurrent State
+ * Computation to Tensor Cores with cuTile", paragraphs on the fixed-size
+ * recurrent state, the jump formula and the three-kernel decomposition): for
+ * every batch b and head h, with head h reading group g = h / (nheads/ngroups)
+ * of Bm and Cm and the state h_t a headdim x dstate matrix,
+ *
+ *     h_t = exp(dt_t * A_h) * h_{t-1} + dt_t * x_t b_t^T        (h_{-1} = init_state or 0)
+ *     y_t = h_t c_t + D_h * x_t                                  final_state = h_{L-1}
+ *
+ * computed chunk by chunk (chunk_size tokens) in four kernels: a log-space
+ * cumsum of dt*A per chunk, each chunk's state contribution on the tensor
+ * cores, a sequential pass over chunks that carries the state (the jump
+ * formula with decay), and a fused output kernel (carried-state term, causally
+ * masked decayed interaction matrix, D*x skip).
+ *
+ * Conventions shared by every entry point below:
+ *  - Pointers are caller-owned DEVICE memory (CUDA global memory of the current
+ *    device), row-major and contiguous, never freed or kept by the library.
+ *  - Layouts: x, y [batch][seqlen][nheads][headdim]; dt [batch][seqlen][nheads];
+ *    A, D [nheads]; Bm, Cm [batch][seqlen][ngroups][dstate];
+ *    init_state, final_state [batch][nheads][headdim][dstate].
+ *  - dtype: x, Bm, Cm and y are fp32 (SSD_F32: TF32 tensor-core products with
+ *    fp32 accumulation) or bf16 (SSD_BF16: bf16 products, fp32 accumulation,
+ *    y rounded to nearest even).  dt, A, D, init_state and final_state are
+ *    always fp32.  dt is used as given (post-activation, positive).
+ *  - Work is enqueued on `stream` (0 = legacy default stream) and is
+ *    asynchronous: no call synchronises.  Calls that share a workspace must be
+ *    ordered on one stream.
+ *  - Argument errors are reported before anything is enqueued.  CUDA launch
+ *    errors return SSD_ERR_CUDA.  Waits inside the kernels are bounded; a wait
+ *    that runs out records SSD_ERR_DEVICE_TIMEOUT in the workspace status word,
+ *    which ssd_fwd_check() reads after the caller synchronises.  The library
+ *    never aborts the process.
+ *  - Supported shapes: headdim == 64; dstate in {64, 128, 256};
+ *    chunk_size in {64, 128, 256}; nheads % ngroups == 0 and (nheads/ngroups)
+ *    even; x, Bm, Cm, y and the workspace 16-byte aligned.  Anything else
+ *    returns SSD_ERR_UNSUPPORTED (shape) or SSD_ERR_INVALID_ARG (pointer,
+ *    negative size).  batch == 0 or seqlen == 0 is valid (empty input).
+ */
+#ifndef SSD_GB300_H_
+#define SSD_GB300_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* ssd_stream_t; /* same handle as cudaStream_t */
+
+typedef enum {
+  SSD_OK = 0,
+  SSD_ERR_INVALID_ARG = 1,
+  SSD_ERR_UNSUPPORTED = 2,
+  SSD_ERR_WORKSPACE = 3,
+  SSD_ERR_CUDA = 4,
+  SSD_ERR_DEVICE_TIMEOUT = 5
+} ssd_status;
+
+typedef enum { SSD_F32 = 0, SSD_BF16 = 1 } ssd_dtype;
+
+typedef struct {
+  int64_t batch;      /* B >= 0 */
+  int64_t seqlen;     /* L >= 0; need not be a multiple of chunk_size */
+  int32_t nheads;     /* H */
+  int32_t headdim;    /* P (64) */
+  int32_t ngroups;    /* G, divides H */
+  int32_t dstate;     /* N */
+  int32_t chunk_size; /* Q */
+  int32_t dtype;      /* ssd_dtype of x, Bm, Cm, y */
+} ssd_shape;
+
+/* Byte offsets of the workspace regions (each 1024-byte aligned).  The
+ * workspace is caller-owned scratch; its contents between calls are
+ * intermediate results exposed for testing:
+ *   status      int32 device status word (0 = OK)
+ *   cumsum      fp32 [B][H][nc*Q]  inclusive cumsum of dt*A within each chunk
+ *   dt_t        fp32 [B][H][nc*Q]  dt transposed to head-major order (0 past L)
+ *   states      fp32 [B][nc][H][P][N]  chunk states S_c; after the state pass,
+ *               for SSD_F32 the state entering each chunk (in place)
+ *   states_bf16 bf16 [B][nc][H][P][N]  (SSD_BF16 only) state entering each
+ *               chunk, rounded to bf16 for the output kernel's tensor cores
+ * nc = ceil(seqlen / chunk_size). */
+typedef struct {
+  size_t status;
+  size_t cumsum;
+  size_t dt_t;
+  size_t states;
+  size_t states_bf16;
+  size_t total;
+} ssd_workspace_layout;
+
+/* Human-readable name of a status code (static storage; never NULL). */
+const char* ssd_status_string(ssd_status s);
+
+/* Checks the shape (see "Supported shapes") without touching memory. */
+ssd_status ssd_validate_shape(const ssd_shape* shape);
+
+/* Workspace regions for `shape`; returns SSD_OK or the shape error. */
+ssd_status ssd_fwd_workspace_layout(const ssd_shape* shape, ssd_workspace_layout* out);
+
+/* Bytes of device workspace ssd_fwd needs for `shape` (0 if the shape is
+ * invalid or unsupported). */
+size_t ssd_fwd_workspace_size(const ssd_shape* shape);
+
+/* The whole forward pass: chunk_cumsum, chunk_state, state_passing and
+ * compute_out, enqueued in that order on `stream`.  init_state may be NULL
+ * (zero initial state); final_state may be NULL (not written).  The workspace
+ * must hold ssd_fwd_workspace_size(shape) bytes. */
+ssd_status ssd_fwd(const ssd_shape* shape, const void* x, const float* dt, const float* A,
+                   const void* Bm, const void* Cm, const float* D, const float* init_state, void* y,
+                   float* final_state, void* workspace, size_t workspace_bytes, ssd_stream_t stream);
+
+/* After the caller has synchronised the stream of a call that used
+ * `workspace`: SSD_OK, or SSD_ERR_DEVICE_TIMEOUT if a bounded wait inside a
+ * kernel ran out (its outputs are then invalid).  Blocking 4-byte read. */
+ssd_status ssd_fwd_check(const void* workspace);
+
+/* --- The four steps, callable one by one (ssd_fwd is exactly these four
+ * calls in order).  Each reads and writes the workspace regions named. ---- */
+
+/* Step 1 (page 1, chunk_cumsum): cumsum[b][h][cQ+i] = sum_{k<=i} dt*A over the
+ * chunk, dt_t = dt transposed; tokens past seqlen contribute 0.  Also clears
+ * the status word. */
+ssd_status ssd_chunk_cumsum(const ssd_shape* shape, const float* dt, const float* A, void* workspace,
+                            size_t workspace_bytes, ssd_stream_t stream);
+
+/* Step 2 (page 1, jump formula with decay; fwd_pass_state's per-chunk MMA):
+ * states[b][c][h][p][n] = sum_{j in chunk c} exp(G_last - G_j) dt_j x_j[p] b_j[n]
+ * on the tensor cores (tcgen05, accumulator in tensor memory, operands staged
+ * by TMA).  Needs step 1. */
+ssd_status ssd_chunk_state(const ssd_shape* shape, const void* x, const void* Bm, void* workspace,
+                           size_t workspace_bytes, ssd_stream_t stream);
+
+/* Step 3 (page 1, fwd_pass_state's sequential loop over chunks): with
+ * h = init_state (or 0), for c = 0..nc-1: entering_c = h;
+ * h = exp(G_last_c) h + S_c.  Writes the entering states (see the layout) and
+ * final_state = h (if not NULL).  Needs steps 1-2. */
+ssd_status ssd_state_passing(const ssd_shape* shape, const float* init_state, float* final_state,
+                             void* workspace, size_t workspace_bytes, ssd_stream_t stream);
+
+/* Step 4 (page 1, compute_out): y_i = exp(G_i) C_i h_entering^T
+ *   + sum_{j<=i in chunk} (C_i . B_j) exp(G_i - G_j) dt_j x_j + D_h x_i,
+ * one fused tile kernel on the tensor cores; the causal mask is made in
+ * registers and the chunk_size x chunk_size matrix never reaches global
+ * memory.  Needs steps 1-3. */
+ssd_status ssd_compute_out(const ssd_shape* shape, const void* x, const void* Bm, const void* Cm,
+                           const float* D, void* y, void* workspace, size_t workspace_bytes,
+                           ssd_stream_t stream);
+
+/* Test hook for the failure path: enqueues one block that waits, for at most
+ * `limit_us` microseconds, on a barrier nothing arrives at, then records
+ * SSD_ERR_DEVICE_TIMEOUT in the workspace status word and exits (no trap, no
+ * hang).  The workspace needs at least 4 bytes. */
+ssd_status ssd_debug_timeout_probe(void* workspace, uint32_t limit_us, ssd_stream_t stream);
+
+/* Number of kernels ssd_fwd enqueues for `shape` (0 for an empty input). */
+int ssd_fwd_kernel_count(const ssd_shape* shape);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SSD_GB300_H_ */

@@ -1,0 +1,266 @@
+"""Mamba-2 chunked SSD forward on GB300 (sm_103a): Python binding.
+
+Every step of the forward pass runs in the CUDA library ``libssd_gb300.so``
+(C ABI in ``include/ssd.h``).  This module only marshals arguments: it checks
+tensor dtypes and layouts, allocates outputs and the workspace with PyTorch
+when the caller does not pass them, and calls the C entry points of the same
+names on the current PyTorch CUDA stream.  There is no CPU fallback: importing
+the package fails if the library has not been built.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Dict, Optional, Tuple
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libssd_gb300.so")
+
+SSD_F32, SSD_BF16 = 0, 1
+STATUS = {0: "SSD_OK", 1: "SSD_ERR_INVALID_ARG", 2: "SSD_ERR_UNSUPPORTED", 3: "SSD_ERR_WORKSPACE",
+          4: "SSD_ERR_CUDA", 5: "SSD_ERR_DEVICE_TIMEOUT"}
+
+# Every entry point include/ssd.h declares.
+EXPORTS = ("ssd_status_string", "ssd_validate_shape", "ssd_fwd_workspace_layout", "ssd_fwd_workspace_size",
+           "ssd_fwd", "ssd_fwd_check", "ssd_chunk_cumsum", "ssd_chunk_state", "ssd_state_passing",
+           "ssd_compute_out", "ssd_debug_timeout_probe", "ssd_fwd_kernel_count")
+
+
+class ssd_shape(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int64), ("seqlen", ctypes.c_int64), ("nheads", ctypes.c_int32),
+                ("headdim", ctypes.c_int32), ("ngroups", ctypes.c_int32), ("dstate", ctypes.c_int32),
+                ("chunk_size", ctypes.c_int32), ("dtype", ctypes.c_int32)]
+
+    def __repr__(self):
+        return ("ssd_shape(B=%d, L=%d, H=%d, P=%d, G=%d, N=%d, Q=%d, dtype=%s)" %
+                (self.batch, self.seqlen, self.nheads, self.headdim, self.ngroups, self.dstate,
+                 self.chunk_size, "bf16" if self.dtype == SSD_BF16 else "f32"))
+
+
+class ssd_workspace_layout(ctypes.Structure):
+    _fields_ = [("status", ctypes.c_size_t), ("cumsum", ctypes.c_size_t), ("dt_t", ctypes.c_size_t),
+                ("states", ctypes.c_size_t), ("states_bf16", ctypes.c_size_t), ("total", ctypes.c_size_t)]
+
+
+class SSDError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {STATUS.get(code, code)}")
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"{LIB_PATH} is missing: build it with `python mamba_ssd_forward_chunked_gb300/build_ext.py` "
+            "(there is no CPU fallback)")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, c_int, sz, vp = ctypes.POINTER, ctypes.c_int, ctypes.c_size_t, ctypes.c_void_p
+    sp = P(ssd_shape)
+    lib.ssd_status_string.restype = ctypes.c_char_p
+    lib.ssd_status_string.argtypes = [c_int]
+    lib.ssd_validate_shape.restype = c_int
+    lib.ssd_validate_shape.argtypes = [sp]
+    lib.ssd_fwd_workspace_layout.restype = c_int
+    lib.ssd_fwd_workspace_layout.argtypes = [sp, P(ssd_workspace_layout)]
+    lib.ssd_fwd_workspace_size.restype = sz
+    lib.ssd_fwd_workspace_size.argtypes = [sp]
+    lib.ssd_fwd_kernel_count.restype = c_int
+    lib.ssd_fwd_kernel_count.argtypes = [sp]
+    lib.ssd_fwd.restype = c_int
+    lib.ssd_fwd.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    lib.ssd_fwd_check.restype = c_int
+    lib.ssd_fwd_check.argtypes = [vp]
+    lib.ssd_chunk_cumsum.restype = c_int
+    lib.ssd_chunk_cumsum.argtypes = [sp, vp, vp, vp, sz, vp]
+    lib.ssd_chunk_state.restype = c_int
+    lib.ssd_chunk_state.argtypes = [sp, vp, vp, vp, sz, vp]
+    lib.ssd_state_passing.restype = c_int
+    lib.ssd_state_passing.argtypes = [sp, vp, vp, vp, sz, vp]
+    lib.ssd_compute_out.restype = c_int
+    lib.ssd_compute_out.argtypes = [sp, vp, vp, vp, vp, vp, vp, sz, vp]
+    lib.ssd_debug_timeout_probe.restype = c_int
+    lib.ssd_debug_timeout_probe.argtypes = [vp, ctypes.c_uint32, vp]
+    return lib
+
+
+lib = _load()
+
+
+# ------------------------------------------------------------------ helpers
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _check(code: int, where: str) -> None:
+    if code != 0:
+        raise SSDError(code, where)
+
+
+def make_shape(batch: int, seqlen: int, nheads: int, headdim: int, ngroups: int, dstate: int,
+               chunk_size: int, dtype) -> ssd_shape:
+    """Build an ssd_shape; ``dtype`` is torch.float32 / torch.bfloat16 or SSD_F32 / SSD_BF16."""
+    if isinstance(dtype, torch.dtype):
+        if dtype == torch.float32:
+            dtype = SSD_F32
+        elif dtype == torch.bfloat16:
+            dtype = SSD_BF16
+        else:
+            raise SSDError(2, f"dtype {dtype}")
+    return ssd_shape(batch, seqlen, nheads, headdim, ngroups, dstate, chunk_size, dtype)
+
+
+def shape_of(x: torch.Tensor, Bm: torch.Tensor, chunk_size: int) -> ssd_shape:
+    B, L, H, P = x.shape
+    G, N = Bm.shape[2], Bm.shape[3]
+    return make_shape(B, L, H, P, G, N, chunk_size, x.dtype)
+
+
+def ssd_validate_shape(shape: ssd_shape) -> int:
+    return lib.ssd_validate_shape(ctypes.byref(shape))
+
+
+def ssd_status_string(code: int) -> str:
+    return lib.ssd_status_string(code).decode()
+
+
+def ssd_fwd_workspace_size(shape: ssd_shape) -> int:
+    return lib.ssd_fwd_workspace_size(ctypes.byref(shape))
+
+
+def ssd_fwd_kernel_count(shape: ssd_shape) -> int:
+    return lib.ssd_fwd_kernel_count(ctypes.byref(shape))
+
+
+def ssd_fwd_workspace_layout(shape: ssd_shape) -> Dict[str, int]:
+    L = ssd_workspace_layout()
+    _check(lib.ssd_fwd_workspace_layout(ctypes.byref(shape), ctypes.byref(L)), "ssd_fwd_workspace_layout")
+    return {k: getattr(L, k) for k, _ in ssd_workspace_layout._fields_}
+
+
+def new_workspace(shape: ssd_shape, device="cuda") -> torch.Tensor:
+    n = ssd_fwd_workspace_size(shape)
+    if n == 0:
+        _check(ssd_validate_shape(shape) or 2, "ssd_fwd_workspace_size")
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def workspace_views(shape: ssd_shape, ws: torch.Tensor) -> Dict[str, torch.Tensor]:
+    """Typed views of the workspace regions (intermediate results, for tests)."""
+    L = ssd_fwd_workspace_layout(shape)
+    B, H, P, N, Q = shape.batch, shape.nheads, shape.headdim, shape.dstate, shape.chunk_size
+    nc = -(-shape.seqlen // Q)
+    Lp = nc * Q
+
+    def view(off, count, dt, dims):
+        nbytes = count * torch.tensor([], dtype=dt).element_size()
+        return ws[off:off + nbytes].view(dt).view(*dims)
+    out = {
+        "status": view(L["status"], 1, torch.int32, (1,)),
+        "cumsum": view(L["cumsum"], B * H * Lp, torch.float32, (B, H, Lp)),
+        "dt_t": view(L["dt_t"], B * H * Lp, torch.float32, (B, H, Lp)),
+        "states": view(L["states"], B * nc * H * P * N, torch.float32, (B, nc, H, P, N)),
+    }
+    if shape.dtype == SSD_BF16:
+        out["states_bf16"] = view(L["states_bf16"], B * nc * H * P * N, torch.bfloat16, (B, nc, H, P, N))
+    return out
+
+
+def _check_inputs(x, dt, A, Bm, Cm, D):
+    for name, t in (("x", x), ("dt", dt), ("A", A), ("Bm", Bm), ("Cm", Cm), ("D", D)):
+        if not t.is_cuda or not t.is_contiguous():
+            raise SSDError(1, f"{name} must be a contiguous CUDA tensor")
+    if x.dtype not in (torch.float32, torch.bfloat16) or Bm.dtype != x.dtype or Cm.dtype != x.dtype:
+        raise SSDError(2, "x, Bm and Cm must share dtype float32 or bfloat16")
+    for name, t in (("dt", dt), ("A", A), ("D", D)):
+        if t.dtype != torch.float32:
+            raise SSDError(1, f"{name} must be float32")
+
+
+# ------------------------------------------------------------------ entry points
+
+def ssd_fwd(x: torch.Tensor, dt: torch.Tensor, A: torch.Tensor, Bm: torch.Tensor, Cm: torch.Tensor,
+            D: torch.Tensor, chunk_size: int, init_state: Optional[torch.Tensor] = None,
+            y: Optional[torch.Tensor] = None, final_state: Optional[torch.Tensor] = None,
+            workspace: Optional[torch.Tensor] = None, stream=None,
+            want_final_state: bool = True) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """The whole forward pass (C: ssd_fwd).  Returns (y, final_state)."""
+    _check_inputs(x, dt, A, Bm, Cm, D)
+    shape = shape_of(x, Bm, chunk_size)
+    B, L, H, P = x.shape
+    N = Bm.shape[3]
+    if y is None:
+        y = torch.empty_like(x)
+    if final_state is None and want_final_state:
+        final_state = torch.empty(B, H, P, N, dtype=torch.float32, device=x.device)
+    if init_state is not None and (init_state.dtype != torch.float32 or not init_state.is_contiguous()):
+        raise SSDError(1, "init_state must be contiguous float32")
+    if workspace is None:
+        workspace = new_workspace(shape, x.device)
+    code = lib.ssd_fwd(ctypes.byref(shape), _ptr(x), _ptr(dt), _ptr(A), _ptr(Bm), _ptr(Cm), _ptr(D),
+                       _ptr(init_state), _ptr(y), _ptr(final_state), _ptr(workspace), workspace.numel(),
+                       _stream(stream))
+    _check(code, "ssd_fwd")
+    return y, final_state
+
+
+def ssd_fwd_check(workspace: torch.Tensor) -> int:
+    """Device status word after the caller synchronised (C: ssd_fwd_check)."""
+    return lib.ssd_fwd_check(_ptr(workspace))
+
+
+def ssd_chunk_cumsum(shape: ssd_shape, dt: torch.Tensor, A: torch.Tensor, workspace: torch.Tensor,
+                     stream=None) -> None:
+    _check(lib.ssd_chunk_cumsum(ctypes.byref(shape), _ptr(dt), _ptr(A), _ptr(workspace), workspace.numel(),
+                                _stream(stream)), "ssd_chunk_cumsum")
+
+
+def ssd_chunk_state(shape: ssd_shape, x: torch.Tensor, Bm: torch.Tensor, workspace: torch.Tensor,
+                    stream=None) -> None:
+    _check(lib.ssd_chunk_state(ctypes.byref(shape), _ptr(x), _ptr(Bm), _ptr(workspace), workspace.numel(),
+                               _stream(stream)), "ssd_chunk_state")
+
+
+def ssd_state_passing(shape: ssd_shape, init_state: Optional[torch.Tensor], final_state: Optional[torch.Tensor],
+                      workspace: torch.Tensor, stream=None) -> None:
+    _check(lib.ssd_state_passing(ctypes.byref(shape), _ptr(init_state), _ptr(final_state), _ptr(workspace),
+                                 workspace.numel(), _stream(stream)), "ssd_state_passing")
+
+
+def ssd_compute_out(shape: ssd_shape, x: torch.Tensor, Bm: torch.Tensor, Cm: torch.Tensor, D: torch.Tensor,
+                    y: torch.Tensor, workspace: torch.Tensor, stream=None) -> None:
+    _check(lib.ssd_compute_out(ctypes.byref(shape), _ptr(x), _ptr(Bm), _ptr(Cm), _ptr(D), _ptr(y),
+                               _ptr(workspace), workspace.numel(), _stream(stream)), "ssd_compute_out")
+
+
+def ssd_debug_timeout_probe(workspace: torch.Tensor, limit_us: int, stream=None) -> None:
+    _check(lib.ssd_debug_timeout_probe(_ptr(workspace), int(limit_us), _stream(stream)), "ssd_debug_timeout_probe")
+
+
+def ssd_fwd_host(x, dt, A, Bm, Cm, D, chunk_size: int, init_state=None, device="cuda",
+                 out_y=None, out_final=None, workspace=None, stream=None):
+    """End-to-end call from host memory: copies the inputs to the device,
+    runs ssd_fwd and copies y and the final state back into (pinned) host
+    tensors.  Inputs are CPU tensors (pinned for asynchronous copies).
+    Returns (y_host, final_host); synchronise the stream before reading them."""
+    dev = torch.device(device)
+    st = torch.cuda.current_stream(dev) if stream is None else stream
+    with torch.cuda.stream(st):
+        d = [t.to(dev, non_blocking=True) for t in (x, dt, A, Bm, Cm, D)]
+        h0 = init_state.to(dev, non_blocking=True) if init_state is not None else None
+        y, fin = ssd_fwd(*d, chunk_size, init_state=h0, workspace=workspace, stream=st)
+        if out_y is None:
+            out_y = torch.empty(y.shape, dtype=y.dtype, pin_memory=True)
+        if out_final is None:
+            out_final = torch.empty(fin.shape, dtype=fin.dtype, pin_memory=True)
+        out_y.copy_(y, non_blocking=True)
+        out_final.copy_(fin, non_blocking=True)
+    return out_y, out_final

@@ -1,0 +1,275 @@
+// Step 2 of the SSD forward: each chunk's contribution to the state, on the
+// fifth-generation tensor cores.
+//
+// "Jane Street ML Engineers Map Mamba-2 Recurrent State Computation to Tensor
+// Cores with cuTile", jump-formula paragraph: without decay the state jumps by
+// B X^T over a chunk, one matrix product; with decay the rows are first
+// multiplied by exponentials of log-space sums, which keeps it one product.
+// Per (batch b, chunk c, head h):
+//
+//     S_c[p][n] = sum_j w_j x_j[p] b_j[n],   w_j = exp(G_last - G_j) * dt_j  (<= dt_j)
+//
+// GB300 mapping.  One CTA per (b, c, pair of heads of one group).  The MMA is
+// D[M = 128][N = dstate] = X~^T B: M stacks the two heads' 64 p-rows (x keeps
+// (h, p) contiguous, so one TMA box row covers both), K runs over the chunk's
+// tokens, and the group's B tile is the shared N-side operand.  Both operands
+// come straight from the token-major global layouts, so both are MN-major in
+// shared memory (128-byte swizzle, TMA-written).  The head-dependent token
+// weights w_j are applied in shared memory, in place, between the TMA landing
+// and the MMA -- a row of a 128-byte swizzle atom is one token of one head, so
+// the swizzle never moves data across rows.  The fp32 accumulator lives in
+// tensor memory (dstate columns) and is drained by tcgen05.ld.
+//
+// fp32 inputs run the MMA as TF32, whose shared-memory operands must be
+// K-major: there each 32-token x 32-element TMA box is transposed in place
+// (scaled and rounded to TF32 on the way), so both operands become K-major
+// tiles with the tokens along the 128-byte rows.  bf16 keeps the MN-major
+// tiles and only scales.
+//
+// Warp roles (192 threads): warp 0 issues TMA, warp 1 owns TMEM and issues
+// the MMAs (one thread), warps 2-5 compute the weights, transform each stage
+// and write S_c.  A 4-deep mbarrier ring (full -> scaled -> empty) pipelines
+// the 32-token stages.  All waits are bounded (device-timeout status, no hang).
+#include "ptx.cuh"
+#include "ssd_internal.cuh"
+#include "tile_transpose.cuh"
+
+namespace ssd {
+namespace {
+
+template <typename T>
+struct StateCfg {
+  static constexpr bool kTF32 = sizeof(T) == 4;
+  static constexpr int kAtom = 128 / static_cast<int>(sizeof(T));  // elements per 128-B row
+  static constexpr int kTokens = 32;                                // tokens per stage
+  static constexpr int kKStep = kTF32 ? 8 : 16;                     // K of one MMA
+  static constexpr int kBox = kTokens * 128;                        // one TMA box, bytes
+  static constexpr int kABoxes = 128 / kAtom;                       // boxes spanning M = 128
+  static constexpr int kABytes = kABoxes * kBox;
+  static constexpr int kStages = 4;
+  static constexpr int kThreads = 192;
+};
+
+__host__ __device__ inline uint32_t state_stage_bytes(int N, int atom, int box, int abytes) {
+  return static_cast<uint32_t>(abytes + (N / atom) * box);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(StateCfg<T>::kThreads, 1)
+    chunk_state_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap bmap, Dims d,
+                       const float* __restrict__ cumsum, const float* __restrict__ dt_t,
+                       float* __restrict__ states, int* status, uint64_t spin_ns) {
+  using C = StateCfg<T>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int N = d.N, Q = d.Q;
+  const int h0 = blockIdx.x * 2;
+  const int c = blockIdx.y, b = blockIdx.z;
+  const int g = h0 / (d.H / d.G);
+  const int bBoxes = N / C::kAtom;
+  const uint32_t stage_bytes = state_stage_bytes(N, C::kAtom, C::kBox, C::kABytes);
+  float* w_s = reinterpret_cast<float*>(smem + C::kStages * stage_bytes);  // [2][Q]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(w_s + 2 * Q);
+  uint64_t* full = bars;
+  uint64_t* scaled = bars + C::kStages;
+  uint64_t* empty = bars + 2 * C::kStages;
+  uint64_t* accum = bars + 3 * C::kStages;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(accum + 1);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nstages = Q / C::kTokens;
+  const uint32_t tmem_cols = static_cast<uint32_t>(N);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&scaled[s], 128);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(accum, 1);
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&xmap);
+    tma_prefetch_desc(&bmap);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_holder, tmem_cols);
+    tmem_relinquish();
+  }
+  if (warp >= 2) {
+    // token weights w_j = exp(G_last - G_j) * dt_j for both heads (exponent <= 0)
+    for (int idx = threadIdx.x - 64; idx < 2 * Q; idx += 128) {
+      const int hl = idx / Q, j = idx % Q;
+      const int64_t row = (static_cast<int64_t>(b) * d.H + h0 + hl) * d.Lp + static_cast<int64_t>(c) * Q;
+      w_s[idx] = expf(cumsum[row + Q - 1] - cumsum[row + j]) * dt_t[row + j];
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  bool ok = true;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      for (int it = 0; it < nstages; ++it) {
+        const int s = it % C::kStages, r = it / C::kStages;
+        if (r > 0 && !mbar_wait(&empty[s], (r - 1) & 1, spin_ns)) {
+          ok = false;
+          break;
+        }
+        uint8_t* sa = smem + s * stage_bytes;
+        uint8_t* sb = sa + C::kABytes;
+        mbar_arrive_expect_tx(&full[s], stage_bytes);
+        const int tok = c * Q + it * C::kTokens;
+        for (int k = 0; k < C::kABoxes; ++k)
+          tma_load_3d(sa + k * C::kBox, &xmap, &full[s], h0 * d.P + k * C::kAtom, tok, b);
+        for (int k = 0; k < bBoxes; ++k)
+          tma_load_4d(sb + k * C::kBox, &bmap, &full[s], k * C::kAtom, g, tok, b);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // bf16: both operands MN-major; TF32: both K-major after the transpose
+      const uint32_t mn = C::kTF32 ? 0u : 1u;
+      const uint32_t idesc = idesc_f32acc(C::kTF32 ? 2u : 1u, 128u, static_cast<uint32_t>(N), mn, mn);
+      for (int it = 0; it < nstages; ++it) {
+        const int s = it % C::kStages, r = it / C::kStages;
+        if (!mbar_wait(&scaled[s], r & 1, spin_ns)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t sa = smem_u32(smem + s * stage_bytes);
+        const uint32_t sb = sa + C::kABytes;
+#pragma unroll
+        for (int k = 0; k < C::kTokens / C::kKStep; ++k) {
+          uint64_t ad, bd;
+          if constexpr (C::kTF32) {
+            // K-major, 128-B swizzle: rows of 32 tokens; a K step of 8 tokens
+            // is 32 B along the row; SBO = 1024 B between 8-row groups.
+            ad = sdesc_sw128(sa + k * 32, 16, 1024);
+            bd = sdesc_sw128(sb + k * 32, 16, 1024);
+          } else {
+            // MN-major, 128-B swizzle: LBO = stride between 128-B atom columns
+            // (one TMA box), SBO = stride between 8-row groups along K.
+            ad = sdesc_sw128(sa + k * C::kKStep * 128, C::kBox, 1024);
+            bd = sdesc_sw128(sb + k * C::kKStep * 128, C::kBox, 1024);
+          }
+          mma_ss<C::kTF32>(tmem, ad, bd, idesc, (it | k) != 0 ? 1u : 0u);
+        }
+        mma_commit(&empty[s]);
+      }
+      mma_commit(accum);
+    }
+  } else {
+    const int et = threadIdx.x - 64;
+    for (int it = 0; it < nstages; ++it) {
+      const int s = it % C::kStages, r = it / C::kStages;
+      if (!mbar_wait(&full[s], r & 1, spin_ns)) {
+        ok = false;
+        break;
+      }
+      uint8_t* sa = smem + s * stage_bytes;
+      if constexpr (C::kTF32) {
+        // two boxes per round: the A boxes (x, scaled by w) then the B boxes
+        const int nboxes = C::kABoxes + bBoxes;
+        const int m = et & 63;
+        for (int box0 = 0; box0 < nboxes; box0 += 2) {
+          const int box = box0 + (et >> 6);
+          uint8_t* bp = sa + box * C::kBox;
+          float4 v[4];
+          box_read_4x4(bp, m, v);
+          if (box < C::kABoxes) {
+            const float* w = w_s + (box >> 1) * Q + it * C::kTokens + 4 * (m >> 3);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              v[q].x = round_tf32(v[q].x * w[q]); v[q].y = round_tf32(v[q].y * w[q]);
+              v[q].z = round_tf32(v[q].z * w[q]); v[q].w = round_tf32(v[q].w * w[q]);
+            }
+          } else {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              v[q].x = round_tf32(v[q].x); v[q].y = round_tf32(v[q].y);
+              v[q].z = round_tf32(v[q].z); v[q].w = round_tf32(v[q].w);
+            }
+          }
+          named_bar_sync(1, 128);  // the round's boxes are fully read before any write
+          box_write_4x4_transposed(bp, m, v);
+        }
+      } else {
+        constexpr int kChunks = C::kABytes / 16;
+#pragma unroll 4
+        for (int q = et; q < kChunks; q += 128) {
+          const int box = q / (C::kTokens * 8);
+          const int row = (q >> 3) % C::kTokens;
+          const int hl = box / (C::kABoxes / 2);
+          const float w = w_s[hl * Q + it * C::kTokens + row];
+          uint4* p = reinterpret_cast<uint4*>(sa + q * 16);
+          uint4 v = *p;
+          v.x = pack_bf16x2(bf16_lo(v.x) * w, bf16_hi(v.x) * w);
+          v.y = pack_bf16x2(bf16_lo(v.y) * w, bf16_hi(v.y) * w);
+          v.z = pack_bf16x2(bf16_lo(v.z) * w, bf16_hi(v.z) * w);
+          v.w = pack_bf16x2(bf16_lo(v.w) * w, bf16_hi(v.w) * w);
+          *p = v;
+        }
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(&scaled[s]);
+    }
+    if (ok && !mbar_wait(accum, 0, spin_ns)) ok = false;
+    tc_fence_after();
+    // drain: TMEM lane = 64 * (head within the pair) + p, column = n
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;
+    const int hl = row >> 6, p = row & 63;
+    float* out = states + ((((static_cast<int64_t>(b) * d.nc + c) * d.H + h0 + hl) * d.P + p) * N);
+    for (int n0 = 0; n0 < N; n0 += 32) {
+      uint32_t v[32];
+      tmem_ld32(tmem + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(n0), v);
+      tmem_ld_wait();
+      float4* o = reinterpret_cast<float4*>(out + n0);
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        o[k] = make_float4(__uint_as_float(v[4 * k]), __uint_as_float(v[4 * k + 1]), __uint_as_float(v[4 * k + 2]),
+                           __uint_as_float(v[4 * k + 3]));
+    }
+  }
+  if (!ok) atomicExch(status, static_cast<int>(SSD_ERR_DEVICE_TIMEOUT));
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, tmem_cols);
+  }
+}
+
+template <typename T>
+cudaError_t launch_impl(const Dims& d, const ChunkStateMaps& maps, const Work& w, uint64_t spin_ns,
+                        cudaStream_t stream) {
+  using C = StateCfg<T>;
+  const uint32_t stage_bytes = state_stage_bytes(d.N, C::kAtom, C::kBox, C::kABytes);
+  const size_t smem = 1024 + C::kStages * stage_bytes + 2 * d.Q * sizeof(float) +
+                      (3 * C::kStages + 1) * sizeof(uint64_t) + 16;
+  static size_t configured = 0;
+  if (smem > configured) {
+    cudaError_t e = cudaFuncSetAttribute(chunk_state_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    configured = smem;
+  }
+  const dim3 grid(d.H / 2, d.nc, d.B);
+  chunk_state_kernel<T><<<grid, C::kThreads, smem, stream>>>(maps.x, maps.bm, d, w.cumsum, w.dt_t, w.states,
+                                                             w.status, spin_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_chunk_state(const Dims& d, bool bf16, const ChunkStateMaps& maps, const Work& w,
+                               uint64_t spin_ns, cudaStream_t stream) {
+  return bf16 ? launch_impl<__nv_bfloat16>(d, maps, w, spin_ns, stream)
+              : launch_impl<float>(d, maps, w, spin_ns, stream);
+}
+
+}  // namespace ssd

@@ -1,0 +1,343 @@
+// Host side of the C ABI declared in include/ssd.h: argument checks, workspace
+// carving, TMA tensor-map encoding and the four launches on the caller's
+// stream.  Nothing here allocates device memory or synchronises (except
+// ssd_fwd_check, which reads the 4-byte status word).
+#include <cudaTypedefs.h>
+
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "ssd_internal.cuh"
+
+namespace ssd {
+namespace {
+
+constexpr size_t kAlign = 1024;
+inline size_t align_up(size_t v) { return (v + kAlign - 1) & ~(kAlign - 1); }
+
+uint64_t spin_limit_ns() {
+  static uint64_t v = [] {
+    const char* s = std::getenv("SSD_SPIN_LIMIT_MS");
+    uint64_t ms = 2000;
+    if (s && *s) {
+      char* end = nullptr;
+      unsigned long long x = std::strtoull(s, &end, 10);
+      if (end != s && x > 0) ms = x;
+    }
+    return ms * 1000000ull;
+  }();
+  return v;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// Tiled map with a 128-byte swizzle, zero fill outside the tensor.
+bool encode(CUtensorMap* m, bool bf16, int rank, const void* base, const uint64_t* dims,
+            const uint64_t* strides_bytes, const uint32_t* box) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const uint32_t estr[5] = {1, 1, 1, 1, 1};
+  CUresult r = fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                  static_cast<cuuint32_t>(rank), const_cast<void*>(base), dims, strides_bytes, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+Dims make_dims(const ssd_shape& s) {
+  Dims d{};
+  d.B = static_cast<int>(s.batch);
+  d.L = static_cast<int>(s.seqlen);
+  d.H = s.nheads;
+  d.P = s.headdim;
+  d.G = s.ngroups;
+  d.N = s.dstate;
+  d.Q = s.chunk_size;
+  d.nc = static_cast<int>((s.seqlen + s.chunk_size - 1) / s.chunk_size);
+  d.Lp = d.nc * d.Q;
+  return d;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+bool empty_problem(const ssd_shape& s) { return s.batch == 0 || s.seqlen == 0; }
+
+ssd_status layout_of(const ssd_shape* shape, ssd_workspace_layout* out) {
+  ssd_status st = ssd_validate_shape(shape);
+  if (st != SSD_OK) return st;
+  const ssd_shape& s = *shape;
+  const int64_t nc = (s.seqlen + s.chunk_size - 1) / s.chunk_size;
+  const size_t lp = static_cast<size_t>(nc) * s.chunk_size;
+  const size_t heads = static_cast<size_t>(s.batch) * s.nheads;
+  const size_t nstate = static_cast<size_t>(s.batch) * nc * s.nheads * s.headdim * s.dstate;
+  ssd_workspace_layout L{};
+  size_t off = 0;
+  L.status = off;
+  off = align_up(off + 256);
+  L.cumsum = off;
+  off = align_up(off + heads * lp * sizeof(float));
+  L.dt_t = off;
+  off = align_up(off + heads * lp * sizeof(float));
+  L.states = off;
+  off = align_up(off + nstate * sizeof(float));
+  L.states_bf16 = off;
+  if (s.dtype == SSD_BF16) off = align_up(off + nstate * sizeof(__nv_bfloat16));
+  L.total = off;
+  *out = L;
+  return SSD_OK;
+}
+
+Work carve(void* ws, const ssd_workspace_layout& L, bool bf16) {
+  uint8_t* p = static_cast<uint8_t*>(ws);
+  Work w{};
+  w.status = reinterpret_cast<int*>(p + L.status);
+  w.cumsum = reinterpret_cast<float*>(p + L.cumsum);
+  w.dt_t = reinterpret_cast<float*>(p + L.dt_t);
+  w.states = reinterpret_cast<float*>(p + L.states);
+  w.states_bf16 = bf16 ? reinterpret_cast<__nv_bfloat16*>(p + L.states_bf16) : nullptr;
+  return w;
+}
+
+ssd_status check_workspace(const ssd_shape* shape, void* ws, size_t bytes, ssd_workspace_layout* L) {
+  ssd_status st = layout_of(shape, L);
+  if (st != SSD_OK) return st;
+  if (!ws || !aligned16(ws)) return SSD_ERR_INVALID_ARG;
+  if (bytes < L->total) return SSD_ERR_WORKSPACE;
+  return SSD_OK;
+}
+
+ssd_status from_cuda(cudaError_t e) { return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA; }
+
+size_t esize(const ssd_shape& s) { return s.dtype == SSD_BF16 ? 2 : 4; }
+
+bool build_state_maps(const ssd_shape& s, const void* x, const void* Bm, ChunkStateMaps* m) {
+  const bool bf16 = s.dtype == SSD_BF16;
+  const uint64_t es = esize(s);
+  const uint32_t atom = static_cast<uint32_t>(128 / es);
+  const uint64_t hp = static_cast<uint64_t>(s.nheads) * s.headdim;
+  {
+    const uint64_t dims[3] = {hp, static_cast<uint64_t>(s.seqlen), static_cast<uint64_t>(s.batch)};
+    const uint64_t str[2] = {hp * es, hp * es * s.seqlen};
+    const uint32_t box[3] = {atom, 32, 1};
+    if (!encode(&m->x, bf16, 3, x, dims, str, box)) return false;
+  }
+  {
+    const uint64_t gn = static_cast<uint64_t>(s.ngroups) * s.dstate;
+    const uint64_t dims[4] = {static_cast<uint64_t>(s.dstate), static_cast<uint64_t>(s.ngroups),
+                              static_cast<uint64_t>(s.seqlen), static_cast<uint64_t>(s.batch)};
+    const uint64_t str[3] = {s.dstate * es, gn * es, gn * es * s.seqlen};
+    const uint32_t box[4] = {atom, 1, 32, 1};
+    if (!encode(&m->bm, bf16, 4, Bm, dims, str, box)) return false;
+  }
+  return true;
+}
+
+bool build_out_maps(const ssd_shape& s, const void* x, const void* Bm, const void* Cm, const void* hp_states,
+                    ComputeOutMaps* m) {
+  const bool bf16 = s.dtype == SSD_BF16;
+  const uint64_t es = esize(s);
+  const uint32_t atom = static_cast<uint32_t>(128 / es);
+  const uint64_t gn = static_cast<uint64_t>(s.ngroups) * s.dstate;
+  const uint64_t dims4[4] = {static_cast<uint64_t>(s.dstate), static_cast<uint64_t>(s.ngroups),
+                             static_cast<uint64_t>(s.seqlen), static_cast<uint64_t>(s.batch)};
+  const uint64_t str4[3] = {s.dstate * es, gn * es, gn * es * s.seqlen};
+  const uint32_t box4[4] = {atom, 1, 128, 1};
+  if (!encode(&m->cm, bf16, 4, Cm, dims4, str4, box4)) return false;
+  if (!encode(&m->bm, bf16, 4, Bm, dims4, str4, box4)) return false;
+  const int64_t nc = (s.seqlen + s.chunk_size - 1) / s.chunk_size;
+  {
+    const uint64_t rows = static_cast<uint64_t>(s.batch) * nc * s.nheads * s.headdim;
+    const uint64_t dims[2] = {static_cast<uint64_t>(s.dstate), rows};
+    const uint64_t str[1] = {s.dstate * es};
+    const uint32_t box[2] = {atom, 64};
+    if (!encode(&m->hp, bf16, 2, hp_states, dims, str, box)) return false;
+  }
+  {
+    const uint64_t hp = static_cast<uint64_t>(s.nheads) * s.headdim;
+    const uint64_t dims[3] = {hp, static_cast<uint64_t>(s.seqlen), static_cast<uint64_t>(s.batch)};
+    const uint64_t str[2] = {hp * es, hp * es * s.seqlen};
+    // bf16: one 128-token x 64-p box per block; fp32: 32 x 32 boxes (transposed in shared memory)
+    const uint32_t box[3] = {atom, bf16 ? 128u : 32u, 1};
+    if (!encode(&m->x, bf16, 3, x, dims, str, box)) return false;
+  }
+  return true;
+}
+
+}  // namespace
+}  // namespace ssd
+
+using namespace ssd;
+
+extern "C" {
+
+const char* ssd_status_string(ssd_status s) {
+  switch (s) {
+    case SSD_OK: return "SSD_OK";
+    case SSD_ERR_INVALID_ARG: return "SSD_ERR_INVALID_ARG: null, misaligned or negative argument";
+    case SSD_ERR_UNSUPPORTED: return "SSD_ERR_UNSUPPORTED: shape outside the supported set";
+    case SSD_ERR_WORKSPACE: return "SSD_ERR_WORKSPACE: workspace smaller than ssd_fwd_workspace_size()";
+    case SSD_ERR_CUDA: return "SSD_ERR_CUDA: a CUDA launch or runtime call failed";
+    case SSD_ERR_DEVICE_TIMEOUT: return "SSD_ERR_DEVICE_TIMEOUT: a bounded wait inside a kernel ran out";
+  }
+  return "unknown ssd_status";
+}
+
+ssd_status ssd_validate_shape(const ssd_shape* s) {
+  if (!s) return SSD_ERR_INVALID_ARG;
+  if (s->batch < 0 || s->seqlen < 0 || s->nheads <= 0 || s->headdim <= 0 || s->ngroups <= 0 || s->dstate <= 0 ||
+      s->chunk_size <= 0)
+    return SSD_ERR_INVALID_ARG;
+  if (s->dtype != SSD_F32 && s->dtype != SSD_BF16) return SSD_ERR_UNSUPPORTED;
+  if (s->headdim != 64) return SSD_ERR_UNSUPPORTED;
+  if (s->dstate != 64 && s->dstate != 128 && s->dstate != 256) return SSD_ERR_UNSUPPORTED;
+  if (s->chunk_size != 64 && s->chunk_size != 128 && s->chunk_size != 256) return SSD_ERR_UNSUPPORTED;
+  if (s->nheads % s->ngroups != 0 || (s->nheads / s->ngroups) % 2 != 0) return SSD_ERR_UNSUPPORTED;
+  // every index that reaches a TMA coordinate or a grid dimension fits int32 / grid limits
+  const int64_t nc = (s->seqlen + s->chunk_size - 1) / s->chunk_size;
+  if (s->seqlen > (int64_t(1) << 30) || s->batch > 65535 || nc > 65535) return SSD_ERR_UNSUPPORTED;
+  if (s->batch * nc * s->nheads * int64_t(s->headdim) >= (int64_t(1) << 31)) return SSD_ERR_UNSUPPORTED;
+  if (s->batch * s->seqlen * int64_t(s->nheads) >= (int64_t(1) << 31)) return SSD_ERR_UNSUPPORTED;
+  return SSD_OK;
+}
+
+ssd_status ssd_fwd_workspace_layout(const ssd_shape* shape, ssd_workspace_layout* out) {
+  if (!out) return SSD_ERR_INVALID_ARG;
+  return layout_of(shape, out);
+}
+
+size_t ssd_fwd_workspace_size(const ssd_shape* shape) {
+  ssd_workspace_layout L;
+  return layout_of(shape, &L) == SSD_OK ? L.total : 0;
+}
+
+int ssd_fwd_kernel_count(const ssd_shape* shape) {
+  if (ssd_validate_shape(shape) != SSD_OK || empty_problem(*shape)) return 0;
+  return 4;
+}
+
+ssd_status ssd_chunk_cumsum(const ssd_shape* shape, const float* dt, const float* A, void* workspace,
+                            size_t workspace_bytes, ssd_stream_t stream) {
+  ssd_workspace_layout L;
+  ssd_status st = check_workspace(shape, workspace, workspace_bytes, &L);
+  if (st != SSD_OK) return st;
+  if (empty_problem(*shape)) return SSD_OK;
+  if (!dt || !A || !aligned4(dt) || !aligned4(A)) return SSD_ERR_INVALID_ARG;
+  Work w = carve(workspace, L, shape->dtype == SSD_BF16);
+  return from_cuda(launch_chunk_cumsum(make_dims(*shape), dt, A, w, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+ssd_status ssd_chunk_state(const ssd_shape* shape, const void* x, const void* Bm, void* workspace,
+                           size_t workspace_bytes, ssd_stream_t stream) {
+  ssd_workspace_layout L;
+  ssd_status st = check_workspace(shape, workspace, workspace_bytes, &L);
+  if (st != SSD_OK) return st;
+  if (empty_problem(*shape)) return SSD_OK;
+  if (!x || !Bm || !aligned16(x) || !aligned16(Bm)) return SSD_ERR_INVALID_ARG;
+  const bool bf16 = shape->dtype == SSD_BF16;
+  ChunkStateMaps maps;
+  if (!build_state_maps(*shape, x, Bm, &maps)) return SSD_ERR_CUDA;
+  Work w = carve(workspace, L, bf16);
+  return from_cuda(
+      launch_chunk_state(make_dims(*shape), bf16, maps, w, spin_limit_ns(), reinterpret_cast<cudaStream_t>(stream)));
+}
+
+ssd_status ssd_state_passing(const ssd_shape* shape, const float* init_state, float* final_state,
+                             void* workspace, size_t workspace_bytes, ssd_stream_t stream) {
+  ssd_workspace_layout L;
+  ssd_status st = check_workspace(shape, workspace, workspace_bytes, &L);
+  if (st != SSD_OK) return st;
+  if ((init_state && !aligned16(init_state)) || (final_state && !aligned16(final_state)))
+    return SSD_ERR_INVALID_ARG;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  if (empty_problem(*shape)) {
+    // no tokens: the final state is the initial one (or zero)
+    if (!final_state || shape->batch == 0) return SSD_OK;
+    const size_t bytes = static_cast<size_t>(shape->batch) * shape->nheads * shape->headdim * shape->dstate * 4;
+    return from_cuda(init_state ? cudaMemcpyAsync(final_state, init_state, bytes, cudaMemcpyDeviceToDevice, cs)
+                                : cudaMemsetAsync(final_state, 0, bytes, cs));
+  }
+  const bool bf16 = shape->dtype == SSD_BF16;
+  Work w = carve(workspace, L, bf16);
+  return from_cuda(launch_state_passing(make_dims(*shape), bf16, init_state, final_state, w, cs));
+}
+
+ssd_status ssd_compute_out(const ssd_shape* shape, const void* x, const void* Bm, const void* Cm, const float* D,
+                           void* y, void* workspace, size_t workspace_bytes, ssd_stream_t stream) {
+  ssd_workspace_layout L;
+  ssd_status st = check_workspace(shape, workspace, workspace_bytes, &L);
+  if (st != SSD_OK) return st;
+  if (empty_problem(*shape)) return SSD_OK;
+  if (!x || !Bm || !Cm || !D || !y || !aligned16(x) || !aligned16(Bm) || !aligned16(Cm) || !aligned16(y) ||
+      !aligned4(D))
+    return SSD_ERR_INVALID_ARG;
+  const bool bf16 = shape->dtype == SSD_BF16;
+  Work w = carve(workspace, L, bf16);
+  ComputeOutMaps maps;
+  const void* hp = bf16 ? static_cast<const void*>(w.states_bf16) : static_cast<const void*>(w.states);
+  if (!build_out_maps(*shape, x, Bm, Cm, hp, &maps)) return SSD_ERR_CUDA;
+  return from_cuda(launch_compute_out(make_dims(*shape), bf16, maps, D, y, w, spin_limit_ns(),
+                                      reinterpret_cast<cudaStream_t>(stream)));
+}
+
+ssd_status ssd_fwd(const ssd_shape* shape, const void* x, const float* dt, const float* A, const void* Bm,
+                   const void* Cm, const float* D, const float* init_state, void* y, float* final_state,
+                   void* workspace, size_t workspace_bytes, ssd_stream_t stream) {
+  ssd_workspace_layout L;
+  ssd_status st = check_workspace(shape, workspace, workspace_bytes, &L);
+  if (st != SSD_OK) return st;
+  if (!empty_problem(*shape)) {
+    if (!x || !dt || !A || !Bm || !Cm || !D || !y) return SSD_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(Bm) || !aligned16(Cm) || !aligned16(y) || !aligned4(dt) || !aligned4(A) ||
+        !aligned4(D))
+      return SSD_ERR_INVALID_ARG;
+  }
+  if ((init_state && !aligned16(init_state)) || (final_state && !aligned16(final_state)))
+    return SSD_ERR_INVALID_ARG;
+  if (empty_problem(*shape)) return ssd_state_passing(shape, init_state, final_state, workspace, workspace_bytes, stream);
+  // build every tensor map before the first launch, so an encoding failure enqueues nothing
+  const bool bf16 = shape->dtype == SSD_BF16;
+  Work w = carve(workspace, L, bf16);
+  ChunkStateMaps smaps;
+  ComputeOutMaps omaps;
+  const void* hp = bf16 ? static_cast<const void*>(w.states_bf16) : static_cast<const void*>(w.states);
+  if (!build_state_maps(*shape, x, Bm, &smaps) || !build_out_maps(*shape, x, Bm, Cm, hp, &omaps))
+    return SSD_ERR_CUDA;
+  const Dims d = make_dims(*shape);
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  const uint64_t spin = spin_limit_ns();
+  cudaError_t e = launch_chunk_cumsum(d, dt, A, w, cs);
+  if (e == cudaSuccess) e = launch_chunk_state(d, bf16, smaps, w, spin, cs);
+  if (e == cudaSuccess) e = launch_state_passing(d, bf16, init_state, final_state, w, cs);
+  if (e == cudaSuccess) e = launch_compute_out(d, bf16, omaps, D, y, w, spin, cs);
+  return from_cuda(e);
+}
+
+ssd_status ssd_fwd_check(const void* workspace) {
+  if (!workspace) return SSD_ERR_INVALID_ARG;
+  int v = 0;
+  if (cudaMemcpy(&v, workspace, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return SSD_ERR_CUDA;
+  return v == 0 ? SSD_OK : static_cast<ssd_status>(v);
+}
+
+ssd_status ssd_debug_timeout_probe(void* workspace, uint32_t limit_us, ssd_stream_t stream) {
+  if (!workspace || !aligned4(workspace) || limit_us == 0 || limit_us > 10u * 1000u * 1000u)
+    return SSD_ERR_INVALID_ARG;
+  return from_cuda(launch_timeout_probe(static_cast<int*>(workspace), static_cast<uint64_t>(limit_us) * 1000ull,
+                                        reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,52 @@
+// Shapes, workspace pointers and kernel launchers shared by the SSD forward
+// translation units (host side of the library only).
+#pragma once
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "ssd.h"
+
+namespace ssd {
+
+// Problem sizes with everything the kernels derive from them.
+struct Dims {
+  int B, L, H, P, G, N, Q;
+  int nc;  // chunks per sequence, ceil(L / Q)
+  int Lp;  // padded length nc * Q (row length of the head-major workspace arrays)
+};
+
+// Workspace regions, as device pointers.
+struct Work {
+  int* status;
+  float* cumsum;               // [B][H][Lp]
+  float* dt_t;                 // [B][H][Lp]
+  float* states;               // [B][nc][H][P][N]
+  __nv_bfloat16* states_bf16;  // [B][nc][H][P][N] or null (fp32 problems)
+};
+
+// Tensor maps built on the host for one call.
+struct ChunkStateMaps {
+  CUtensorMap x;   // x viewed as [B][L][H*P], box {128 B of (h,p), 32 tokens, 1}
+  CUtensorMap bm;  // Bm [B][L][G][N], box {128 B of n, 1, 32 tokens, 1}
+};
+struct ComputeOutMaps {
+  CUtensorMap cm;  // Cm [B][L][G][N], box {128 B of n, 1, 128 tokens, 1}
+  CUtensorMap bm;  // Bm, same box
+  CUtensorMap hp;  // entering states [(B*nc*H*P)][N], box {128 B of n, 64 rows}
+  CUtensorMap x;   // x [B][L][H*P], box {128 B of p, 128 (bf16) or 32 (fp32) tokens, 1}
+};
+
+cudaError_t launch_chunk_cumsum(const Dims& d, const float* dt, const float* A, const Work& w,
+                                cudaStream_t stream);
+cudaError_t launch_chunk_state(const Dims& d, bool bf16, const ChunkStateMaps& maps, const Work& w,
+                               uint64_t spin_ns, cudaStream_t stream);
+cudaError_t launch_state_passing(const Dims& d, bool bf16, const float* init, float* final_state,
+                                 const Work& w, cudaStream_t stream);
+cudaError_t launch_compute_out(const Dims& d, bool bf16, const ComputeOutMaps& maps, const float* D,
+                               void* y, const Work& w, uint64_t spin_ns, cudaStream_t stream);
+cudaError_t launch_timeout_probe(int* status, uint64_t limit_ns, cudaStream_t stream);
+
+}  // namespace ssd

@@ -1,0 +1,112 @@
+"""C ABI checks that need no GPU: the library builds and loads, exports every
+entry point include/ssd.h declares, and its host-side argument logic (shape
+validation, workspace sizing and layout, argument errors) behaves as the header
+documents.  No call here reaches a CUDA kernel."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ssd.h")
+
+
+@pytest.fixture(scope="module")
+def ext():
+    import __graft_entry__
+    __graft_entry__.build()
+    import mamba_ssd_forward_chunked_gb300 as m
+    return m
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(ssd_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_expected_entry_points():
+    names = declared_functions()
+    for n in ("ssd_fwd", "ssd_fwd_workspace_size", "ssd_fwd_check", "ssd_status_string", "ssd_chunk_cumsum",
+              "ssd_chunk_state", "ssd_state_passing", "ssd_compute_out"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(ext):
+    lib = ctypes.CDLL(ext.LIB_PATH)
+    for n in declared_functions():
+        assert hasattr(lib, n), f"{n} declared in include/ssd.h but not exported"
+    assert set(declared_functions()) == set(ext.EXPORTS)
+
+
+def test_status_strings(ext):
+    for code in range(6):
+        assert ext.ssd_status_string(code).startswith(ext.STATUS[code])
+
+
+def shape(ext, **kw):
+    base = dict(batch=2, seqlen=2048, nheads=32, headdim=64, ngroups=1, dstate=128, chunk_size=256, dtype=ext.SSD_F32)
+    base.update(kw)
+    return ext.make_shape(**base)
+
+
+def test_validate_shape(ext):
+    assert ext.ssd_validate_shape(shape(ext)) == 0
+    assert ext.ssd_validate_shape(shape(ext, dtype=ext.SSD_BF16, nheads=80)) == 0
+    for bad in (dict(headdim=32), dict(dstate=96), dict(chunk_size=100), dict(chunk_size=512),
+                dict(nheads=3, ngroups=1), dict(nheads=8, ngroups=3), dict(dtype=7)):
+        assert ext.ssd_validate_shape(shape(ext, **bad)) == 2, bad
+    for bad in (dict(batch=-1), dict(seqlen=-5), dict(nheads=0), dict(chunk_size=0)):
+        assert ext.ssd_validate_shape(shape(ext, **bad)) == 1, bad
+    assert ext.ssd_validate_shape(shape(ext, batch=0)) == 0
+    assert ext.ssd_validate_shape(shape(ext, seqlen=0)) == 0
+
+
+def test_workspace_layout(ext):
+    for dt in (ext.SSD_F32, ext.SSD_BF16):
+        for L in (1, 255, 256, 2048, 2049):
+            s = shape(ext, seqlen=L, dtype=dt)
+            lay = ext.ssd_fwd_workspace_layout(s)
+            nc = -(-L // 256)
+            Lp = nc * 256
+            assert all(v % 1024 == 0 for v in lay.values())
+            assert lay["dt_t"] - lay["cumsum"] >= 2 * 32 * Lp * 4
+            assert lay["states_bf16"] - lay["states"] >= 2 * nc * 32 * 64 * 128 * 4
+            extra = 2 * nc * 32 * 64 * 128 * 2 if dt == ext.SSD_BF16 else 0
+            assert lay["total"] >= lay["states_bf16"] + extra
+            assert ext.ssd_fwd_workspace_size(s) == lay["total"]
+    assert ext.ssd_fwd_workspace_size(shape(ext, dstate=100)) == 0
+
+
+def test_argument_errors_before_any_launch(ext):
+    s = shape(ext)
+    need = ext.ssd_fwd_workspace_size(s)
+    fake = ctypes.c_void_p(1 << 20)  # never dereferenced: every case fails its checks first
+    lib = ext.lib
+    by = ctypes.byref
+    # workspace too small
+    assert lib.ssd_fwd(by(s), fake, fake, fake, fake, fake, fake, None, fake, None, fake, need - 1, None) == 3
+    # null input
+    assert lib.ssd_fwd(by(s), None, fake, fake, fake, fake, fake, None, fake, None, fake, need, None) == 1
+    # misaligned x
+    odd = ctypes.c_void_p((1 << 20) + 4)
+    assert lib.ssd_fwd(by(s), odd, fake, fake, fake, fake, fake, None, fake, None, fake, need, None) == 1
+    # null / misaligned workspace
+    assert lib.ssd_fwd(by(s), fake, fake, fake, fake, fake, fake, None, fake, None, None, need, None) == 1
+    assert lib.ssd_fwd(by(s), fake, fake, fake, fake, fake, fake, None, fake, None, odd, need, None) == 1
+    # unsupported shape
+    bad = shape(ext, dstate=96)
+    assert lib.ssd_fwd(by(bad), fake, fake, fake, fake, fake, fake, None, fake, None, fake, need, None) == 2
+    assert lib.ssd_fwd_check(None) == 1
+    assert lib.ssd_debug_timeout_probe(None, 10, None) == 1
+    assert lib.ssd_debug_timeout_probe(fake, 0, None) == 1
+
+
+def test_empty_batch_needs_no_device(ext):
+    s = shape(ext, batch=0)
+    ws = ctypes.c_void_p(1 << 20)
+    n = ext.ssd_fwd_workspace_size(s)
+    assert ext.lib.ssd_fwd(ctypes.byref(s), None, None, None, None, None, None, None, None, None, ws, n, None) == 0
+    assert ext.ssd_fwd_kernel_count(s) == 0
+    assert ext.ssd_fwd_kernel_count(shape(ext)) == 4
