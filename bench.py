@@ -1,0 +1,441 @@
+#!/usr/bin/env python3
+"""Throughput of the Mamba-2 chunked SSD forward pass on GB300.
+
+One step = one ssd_fwd call (chunk_cumsum -> chunk_state -> state_passing ->
+compute_out) over one batch of seeded synthetic inputs already resident in HBM.
+Prints ONE JSON line (rank 0).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+N > 1 runs under torchrun, one rank per GPU: every rank solves its own
+independent problem of the same size (weak scaling; no collective on the data
+path) and the value is all ranks' tokens over the slowest rank's time.
+
+--impl reference times the fp64 CPU oracle (the recurrence) on the host cores
+on a bounded sample of the same workload, reported in the same metric.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import ssd_synth  # noqa: E402
+
+METRIC = "SSD forward tokens/s and % of roofline (TF32 / bf16), 1xGB300"
+DEFAULT_WORKLOAD = "mamba2-370m"
+L2_FLUSH_BYTES = 256 << 20
+NOMINAL_TF32_OVER_BF16 = 1.1 / 2.25  # dense tensor-core rate ratio (nominal)
+KERNELS = ("chunk_cumsum", "chunk_state", "state_passing", "compute_out")
+
+
+# ------------------------------------------------------------------ model of the work
+
+def algorithmic(w: ssd_synth.Workload):
+    """Algorithmic flops and compulsory bytes of one forward pass.
+
+    Flops per (batch, chunk, head): 4*Q*N*P (chunk state and carried-state
+    term) + P*Q*(Q+1) (causal intra-chunk product); per (batch, chunk, group):
+    N*Q*(Q+1) (causal C B^T, once per group).  Bytes: x read, y write, Bm and
+    Cm read, dt read, A and D read, final state write (+ initial state read).
+    """
+    B, L, H, P, N, G, Q = w.batch, w.seqlen, w.nheads, w.headdim, w.dstate, w.ngroups, w.chunk_size
+    nc = -(-L // Q)
+    es = 2 if w.dtype == "bf16" else 4
+    flops = B * nc * H * (4 * Q * N * P + P * Q * (Q + 1)) + B * nc * G * N * Q * (Q + 1)
+    x = B * L * H * P * es
+    st = B * H * P * N * 4
+    by = {"x": x, "y": x, "BmCm": 2 * B * L * G * N * es, "dt": B * L * H * 4, "AD": 2 * H * 4,
+          "final": st, "init": st if w.init_state else 0}
+    return flops, by
+
+
+def kernel_model(w: ssd_synth.Workload):
+    """Per-kernel algorithmic work: the user-visible bytes each kernel must
+    touch and its share of the algorithmic flops (intermediate workspace
+    traffic is overhead and not counted)."""
+    flops, by = algorithmic(w)
+    B, L, H, P, N, Q = w.batch, w.seqlen, w.nheads, w.headdim, w.dstate, w.chunk_size
+    nc = -(-L // Q)
+    f_state = B * nc * H * 2 * Q * N * P
+    return {
+        "chunk_cumsum": {"bytes": by["dt"] + by["AD"] // 2, "flops": 0},
+        "chunk_state": {"bytes": by["x"] + by["BmCm"] // 2, "flops": f_state},
+        "state_passing": {"bytes": by["final"] + by["init"], "flops": 0},
+        "compute_out": {"bytes": by["x"] + by["y"] + by["BmCm"] + by["AD"] // 2, "flops": flops - f_state},
+    }
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def tensor_peak(pk, dtype):
+    base = pk["bf16_tflops"]
+    return base * NOMINAL_TF32_OVER_BF16 if dtype == "f32" else base
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockMonitor:
+    """nvidia-smi samples during the timed region (SM clock, throttle reasons)."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in self.lines:
+            f = [t.strip() for t in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        med = statistics.median(sm) if sm else None
+        return {"sm_mhz": med, "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ GPU arm
+
+def _profile_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current source of that kernel (else None)."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    src = os.path.join(ROOT, "mamba_ssd_forward_chunked_gb300", "csrc", kernel + ".cu")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+        e = rec[workload][kernel]
+        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        if e.get("source_sha256_16") != digest:
+            return None
+        return float(e["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+def run_gpu(args, w: ssd_synth.Workload, rank: int, world: int, local_rank: int):
+    import torch
+    import torch.distributed as dist
+
+    import mamba_ssd_forward_chunked_gb300 as ssd
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    inp = ssd_synth.make_inputs(w, seed=w.seed + rank)
+    tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    host = {k: torch.from_numpy(v) for k, v in inp.items()}
+    for k in ("x", "Bm", "Cm"):
+        host[k] = host[k].to(tdt)
+    host = {k: v.pin_memory() for k, v in host.items()}
+    d = {k: v.to(dev) for k, v in host.items()}
+    init = d.get("init")
+    shape = ssd.shape_of(d["x"], d["Bm"], w.chunk_size)
+    ws = ssd.new_workspace(shape, dev)
+    y = torch.empty_like(d["x"])
+    fin = torch.empty(w.batch, w.nheads, w.headdim, w.dstate, dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def fwd():
+        ssd.ssd_fwd(d["x"], d["dt"], d["A"], d["Bm"], d["Cm"], d["D"], w.chunk_size, init_state=init, y=y,
+                    final_state=fin, workspace=ws, stream=stream)
+
+    def staged(ev):
+        # the same four launches ssd_fwd makes, in its order, with events between them
+        ev[0].record(stream)
+        ssd.ssd_chunk_cumsum(shape, d["dt"], d["A"], ws, stream)
+        ev[1].record(stream)
+        ssd.ssd_chunk_state(shape, d["x"], d["Bm"], ws, stream)
+        ev[2].record(stream)
+        ssd.ssd_state_passing(shape, init, fin, ws, stream)
+        ev[3].record(stream)
+        ssd.ssd_compute_out(shape, d["x"], d["Bm"], d["Cm"], d["D"], y, ws, stream)
+        ev[4].record(stream)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        fwd()
+    torch.cuda.synchronize(dev)
+    if ssd.ssd_fwd_check(ws) != 0:
+        raise RuntimeError("device status after warm-up: " + ssd.ssd_status_string(ssd.ssd_fwd_check(ws)))
+
+    with ClockMonitor(local_rank) as clocks:
+        # timed region 1: the public call, L2 flushed before every step (outside the events)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        barrier()
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        for a, b in evs:
+            flush.zero_()
+            a.record(stream)
+            fwd()
+            b.record(stream)
+        torch.cuda.synchronize(dev)
+        wall = time.perf_counter() - t0
+        barrier()
+        step_ms = [a.elapsed_time(b) for a, b in evs]
+
+        # timed region 2: the same launches with an event between kernels
+        kev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+        barrier()
+        torch.cuda.synchronize(dev)
+        for ev in kev:
+            flush.zero_()
+            staged(ev)
+        torch.cuda.synchronize(dev)
+        barrier()
+        per_kernel = {n: statistics.mean(ev[i].elapsed_time(ev[i + 1]) for ev in kev) for i, n in enumerate(KERNELS)}
+
+        # timed region 3: end to end from pinned host memory (copies inside the events)
+        out_y = torch.empty(y.shape, dtype=y.dtype, pin_memory=True)
+        out_f = torch.empty(fin.shape, dtype=fin.dtype, pin_memory=True)
+        e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(args.steps)]
+        barrier()
+        torch.cuda.synchronize(dev)
+        for a, b in e2e_ev:
+            flush.zero_()
+            a.record(stream)
+            ssd.ssd_fwd_host(host["x"], host["dt"], host["A"], host["Bm"], host["Cm"], host["D"], w.chunk_size,
+                             init_state=host.get("init"), device=dev, out_y=out_y, out_final=out_f, workspace=ws,
+                             stream=stream)
+            b.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier()
+        e2e_ms = [a.elapsed_time(b) for a, b in e2e_ev]
+    status = ssd.ssd_fwd_check(ws)
+    if status != 0:
+        raise RuntimeError("device status after timing: " + ssd.ssd_status_string(status))
+
+    ms = statistics.mean(step_ms)
+    ms_e2e = statistics.mean(e2e_ms)
+    if world > 1:
+        t = torch.tensor([ms, ms_e2e], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms, ms_e2e = float(t[0]), float(t[1])
+    if rank != 0:
+        return None
+
+    flops, by = algorithmic(w)
+    total_bytes = sum(by.values())
+    pk = peaks()
+    tpeak = tensor_peak(pk, w.dtype)
+    t_roof_us = max(flops / (tpeak * 1e12), total_bytes / (pk["hbm_gbs"] * 1e9)) * 1e6
+    tokens = w.tokens * world
+    km = kernel_model(w)
+    dom = max(per_kernel, key=per_kernel.get)
+    dk = km[dom]
+    t_dom = per_kernel[dom] * 1e-3
+    t_mem = dk["bytes"] / (pk["hbm_gbs"] * 1e9)
+    t_tc = dk["flops"] / (tpeak * 1e12)
+    if t_tc > t_mem:
+        roof = {"bound": "tensor", "achieved": dk["flops"] / t_dom / 1e12, "peak": tpeak, "unit": "TFLOP/s"}
+    else:
+        roof = {"bound": "hbm", "achieved": dk["bytes"] / t_dom / 1e9, "peak": pk["hbm_gbs"], "unit": "GB/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    traffic = _profile_traffic(dom, w.name)
+    roof.update({
+        "traffic": traffic,
+        "kernel": dom,
+        "algorithmic_per_launch": dk["flops"] if roof["bound"] == "tensor" else dk["bytes"],
+        "peak_source": pk["source"] + (" bf16 x nominal tf32/bf16 ratio" if roof["bound"] == "tensor"
+                                       and w.dtype == "f32" else ""),
+    })
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_y.numel() * out_y.element_size() + out_f.numel() * out_f.element_size()
+    line = {
+        "metric": METRIC,
+        "value": tokens / (ms * 1e-3),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "tf32" if w.dtype == "f32" else "bf16",
+        "data": "synthetic (seeded SplitMix64 inputs with the Mamba-2 layer value recipe)",
+        "config": {"workload": w.name, "batch": w.batch, "seqlen": w.seqlen, "nheads": w.nheads,
+                   "headdim": w.headdim, "dstate": w.dstate, "ngroups": w.ngroups, "chunk_size": w.chunk_size,
+                   "init_state": w.init_state, "input_dtype": w.dtype, "tokens_per_step_per_gpu": w.tokens,
+                   "l2": f"flushed before every timed step ({L2_FLUSH_BYTES >> 20} MB write, outside the events)"},
+        "tflops": flops * world / (ms * 1e-3) / 1e12,
+        "step_roofline": {"t_roof_us": t_roof_us, "t_us": ms * 1e3, "frac": t_roof_us / (ms * 1e3),
+                          "flops": flops, "bytes": total_bytes, "tensor_peak_tflops": tpeak,
+                          "hbm_peak_gbs": pk["hbm_gbs"], "peak_source": pk["source"]},
+        "roofline": roof,
+        "kernels_ms": per_kernel,
+        "gpu_launches": 4 * args.steps,
+        "e2e": {"value": tokens / (ms_e2e * 1e-3), "unit": "tokens/s", "ms_per_step": ms_e2e,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "wall_s_timed_region_1": wall,
+        "clocks": clocks.summary(),
+    }
+    if not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds, inp=inp)
+    return line
+
+
+# ------------------------------------------------------------------ CPU oracle arm
+
+def _oracle_sample(w: ssd_synth.Workload, seconds: float):
+    """(b, h) pairs for a bounded run of the oracle (about `seconds` of CPU work)."""
+    import oracle
+    threads = oracle.threads_available()
+    per_pair = 2.0 * w.seqlen * w.headdim * w.dstate / 1.0e9  # ~1 G multiply-adds / s per thread
+    total = w.batch * w.nheads
+    k = min(total, max(threads, int(seconds * threads / max(per_pair, 1e-9))))
+    rng = np.random.default_rng(0)
+    idx = np.sort(rng.choice(total, size=k, replace=False))
+    return np.stack([idx // w.nheads, idx % w.nheads], axis=1).astype(np.int64), threads
+
+
+def cpu_baseline(w: ssd_synth.Workload, seconds: float, inp=None, reps: int = 3):
+    import oracle
+    inp = ssd_synth.make_inputs(w) if inp is None else inp
+    pairs, threads = _oracle_sample(w, seconds / reps)
+    times, used = [], threads
+    for _ in range(reps):
+        t0 = time.perf_counter()
+        _, _, used = oracle.recurrence(inp, pairs=pairs)
+        times.append(time.perf_counter() - t0)
+    t = statistics.median(times)
+    frac = len(pairs) / (w.batch * w.nheads)
+    return {"value": w.tokens * frac / t, "unit": "tokens/s", "cores": used, "kind": "oracle",
+            "sample": f"fp64 recurrence (C, OpenMP) on {len(pairs)} of {w.batch * w.nheads} (batch, head) pairs "
+                      f"of the same workload, median of {reps}; tokens/s scaled by that fraction",
+            "seconds_per_run": t}
+
+
+def run_reference(args, w: ssd_synth.Workload):
+    import oracle
+    inp = ssd_synth.make_inputs(w)
+    pairs, threads = _oracle_sample(w, args.cpu_seconds / max(1, args.steps))
+    frac = len(pairs) / (w.batch * w.nheads)
+    for _ in range(args.warmup):
+        oracle.recurrence(inp, pairs=pairs[: max(1, len(pairs) // 8)])
+    times, used = [], threads
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        _, _, used = oracle.recurrence(inp, pairs=pairs)
+        times.append(time.perf_counter() - t0)
+    t = statistics.mean(times)
+    value = w.tokens * frac / t
+    sample = (f"fp64 recurrence (C, OpenMP) on {len(pairs)} of {w.batch * w.nheads} (batch, head) pairs per step; "
+              f"tokens/s scaled by that fraction")
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded SplitMix64 inputs with the Mamba-2 layer value recipe)",
+        "config": {"workload": w.name, "batch": w.batch, "seqlen": w.seqlen, "nheads": w.nheads, "headdim": w.headdim,
+                   "dstate": w.dstate, "ngroups": w.ngroups, "chunk_size": w.chunk_size, "input_dtype": w.dtype},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": used, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+# ------------------------------------------------------------------ main
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(ssd_synth.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=15.0, help="CPU work budget of the oracle leg")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    w = ssd_synth.WORKLOADS[args.workload]
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if world == 1 and args.gpus > 1:
+        ap.error("--gpus N > 1 must be launched with torchrun (one rank per GPU)")
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args, w)), flush=True)
+        return 0
+
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    try:
+        line = run_gpu(args, w, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())
