@@ -161,6 +161,37 @@ ssd_status ssd_debug_timeout_probe(void* workspace, uint32_t limit_us, ssd_strea
 /* Number of kernels ssd_fwd enqueues for `shape` (0 for an empty input). */
 int ssd_fwd_kernel_count(const ssd_shape* shape);
 
+/* Bytes of the device array that ssd_fwd_static_scratch uses as its workspace. */
+#define SSD_STATIC_SCRATCH_BYTES ((size_t)32 << 20)
+
+/* ssd_fwd for callers that may not allocate device memory.  The paper has no
+ * counterpart: this is a service of the library, not a step of the method.
+ *
+ * Who needs it: code that runs inside a host which owns all device memory
+ * (a plugin of another runtime with its own pool), serving processes that
+ * allow no allocation after start-up, and any caller for whom a cudaMalloc
+ * on the hot path is not allowed or too risky (it can stall the device and
+ * can fail under memory pressure).  Such a caller passes only the inputs and
+ * outputs of ssd_fwd; the workspace is a fixed array of
+ * SSD_STATIC_SCRATCH_BYTES in the library's own device data, which every GPU
+ * that loads the library holds until the process exits.  Nothing is
+ * allocated by this call.
+ *
+ * Arguments, layouts, dtypes and supported shapes are those of ssd_fwd.
+ * Returns SSD_ERR_WORKSPACE, before enqueuing anything, when
+ * ssd_fwd_workspace_size(shape) is larger than SSD_STATIC_SCRATCH_BYTES.
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) for that device, so make that first call before any
+ * stream capture.  Each call clears the status word and then overwrites the
+ * rest of the array; the array keeps the last call's intermediate results.
+ * All calls share the one array: calls whose GPU work can overlap in time
+ * (different streams, or threads without ordering between them) race and
+ * give wrong results.  A device-timeout status (see ssd_fwd_check) is left in
+ * the array and cannot be read through this entry point. */
+ssd_status ssd_fwd_static_scratch(const ssd_shape* shape, const void* x, const float* dt, const float* A,
+                                  const void* Bm, const void* Cm, const float* D, const float* init_state,
+                                  void* y, float* final_state, ssd_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

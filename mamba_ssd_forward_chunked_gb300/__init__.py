@@ -25,7 +25,10 @@ STATUS = {0: "SSD_OK", 1: "SSD_ERR_INVALID_ARG", 2: "SSD_ERR_UNSUPPORTED", 3: "S
 # Every entry point include/ssd.h declares.
 EXPORTS = ("ssd_status_string", "ssd_validate_shape", "ssd_fwd_workspace_layout", "ssd_fwd_workspace_size",
            "ssd_fwd", "ssd_fwd_check", "ssd_chunk_cumsum", "ssd_chunk_state", "ssd_state_passing",
-           "ssd_compute_out", "ssd_debug_timeout_probe", "ssd_fwd_kernel_count")
+           "ssd_compute_out", "ssd_debug_timeout_probe", "ssd_fwd_kernel_count", "ssd_fwd_static_scratch")
+
+# Size of the library's own workspace array used by ssd_fwd_static_scratch.
+SSD_STATIC_SCRATCH_BYTES = 32 << 20
 
 
 class ssd_shape(ctypes.Structure):
@@ -82,6 +85,8 @@ def _load() -> ctypes.CDLL:
     lib.ssd_compute_out.argtypes = [sp, vp, vp, vp, vp, vp, vp, sz, vp]
     lib.ssd_debug_timeout_probe.restype = c_int
     lib.ssd_debug_timeout_probe.argtypes = [vp, ctypes.c_uint32, vp]
+    lib.ssd_fwd_static_scratch.restype = c_int
+    lib.ssd_fwd_static_scratch.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
     return lib
 
 
@@ -264,3 +269,21 @@ def ssd_fwd_host(x, dt, A, Bm, Cm, D, chunk_size: int, init_state=None, device="
         out_y.copy_(y, non_blocking=True)
         out_final.copy_(fin, non_blocking=True)
     return out_y, out_final
+
+
+def ssd_fwd_static_scratch(x: torch.Tensor, dt: torch.Tensor, A: torch.Tensor, Bm: torch.Tensor,
+                           Cm: torch.Tensor, D: torch.Tensor, chunk_size: int, y: torch.Tensor,
+                           final_state: Optional[torch.Tensor] = None,
+                           init_state: Optional[torch.Tensor] = None, stream=None) -> None:
+    """The forward pass without a workspace argument (C: ssd_fwd_static_scratch).
+
+    For callers that may not allocate device memory: the caller provides the
+    inputs and the outputs ``y`` / ``final_state``; the workspace is the
+    library's fixed SSD_STATIC_SCRATCH_BYTES device array, shared by every
+    call (calls whose GPU work overlaps race).  Nothing is allocated here.
+    """
+    _check_inputs(x, dt, A, Bm, Cm, D)
+    shape = shape_of(x, Bm, chunk_size)
+    code = lib.ssd_fwd_static_scratch(ctypes.byref(shape), _ptr(x), _ptr(dt), _ptr(A), _ptr(Bm), _ptr(Cm),
+                                      _ptr(D), _ptr(init_state), _ptr(y), _ptr(final_state), _stream(stream))
+    _check(code, "ssd_fwd_static_scratch")

@@ -1,0 +1,65 @@
+"""The entry point for callers that cannot allocate device memory.
+
+ssd_fwd_static_scratch runs the same forward pass as ssd_fwd but keeps its
+workspace in a fixed array inside the library, for hosts that own all device
+memory or forbid allocation on the hot path.  These tests call it through the
+C ABI and compare it with ssd_fwd (which uses a caller-allocated workspace)
+within the tolerance of the other parity tests, on two calls in a row: the
+array keeps the first call's contents, so the second call must not depend on
+them.  This file is named so that pytest collects it last.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import ssd_synth
+from gpu_util import TOL, rel_err, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+def _static_call(ssd, d, Q, y, fin, init):
+    shape = ssd.shape_of(d["x"], d["Bm"], Q)
+    p = lambda t: None if t is None else t.data_ptr()  # noqa: E731
+    return ssd.lib.ssd_fwd_static_scratch(ctypes.byref(shape), p(d["x"]), p(d["dt"]), p(d["A"]), p(d["Bm"]),
+                                          p(d["Cm"]), p(d["D"]), p(init), p(y), p(fin),
+                                          torch.cuda.current_stream().cuda_stream)
+
+
+@pytest.mark.parametrize("over", [
+    dict(seqlen=300, nheads=4, dstate=128, chunk_size=128, dtype="f32", init_state=True),
+    dict(batch=2, seqlen=640, nheads=8, ngroups=2, dstate=64, chunk_size=256, dtype="bf16"),
+], ids=["f32", "bf16"])
+def test_static_scratch_matches_ssd_fwd_twice(over):
+    import mamba_ssd_forward_chunked_gb300 as ssd
+    results = []
+    for seed in (1, 2):  # two calls in a row on different inputs
+        w = ssd_synth.custom("noalloc", seed=seed, **over)
+        inp = ssd_synth.make_inputs(w)
+        d = to_device(inp, w.dtype)
+        init = d.get("init")
+        y_ref, f_ref = ssd.ssd_fwd(d["x"], d["dt"], d["A"], d["Bm"], d["Cm"], d["D"], w.chunk_size,
+                                   init_state=init)
+        y = torch.full_like(d["x"], float("nan"))
+        fin = torch.full_like(f_ref, float("nan"))
+        assert _static_call(ssd, d, w.chunk_size, y, fin, init) == 0
+        torch.cuda.synchronize()
+        ey = rel_err(y.float().cpu().numpy(), y_ref.float().cpu().numpy())
+        ef = rel_err(fin.cpu().numpy(), f_ref.cpu().numpy())
+        assert np.isfinite(y.float().cpu().numpy()).all()
+        assert ey <= TOL[w.dtype] and ef <= TOL[w.dtype], (seed, ey, ef)
+        results.append(y.clone())
+    assert not torch.equal(results[0], results[1])
+
+
+def test_static_scratch_rejects_problems_beyond_its_size():
+    import mamba_ssd_forward_chunked_gb300 as ssd
+    w = ssd_synth.WORKLOADS["long-16k-n256"]  # needs ~140 MB of workspace
+    shape = ssd.make_shape(w.batch, w.seqlen, w.nheads, w.headdim, w.ngroups, w.dstate, w.chunk_size, ssd.SSD_F32)
+    assert ssd.ssd_fwd_workspace_size(shape) > ssd.SSD_STATIC_SCRATCH_BYTES
+    fake = ctypes.c_void_p(1 << 20)  # never dereferenced: the size check comes first
+    code = ssd.lib.ssd_fwd_static_scratch(ctypes.byref(shape), fake, fake, fake, fake, fake, fake, None, fake, None,
+                                          None)
+    assert code == 3  # SSD_ERR_WORKSPACE
