@@ -7,77 +7,82 @@
 // strided [batch, token, head] layout to [batch, head, token] so that the
 // consumers read contiguous rows with TMA or vector loads.
 //
-// One block per (chunk, batch, 32-head slice).  dt arrives as [B][L][H]: a
-// block reads its Q x 32 slice row by row (128 contiguous bytes per token),
-// transposes it through shared memory, scans each head's Q values with one
-// warp (serial runs per lane + a warp-shuffle scan of the run totals) and
-// writes cumsum and dt as contiguous [B][H][Lp] rows.  Tokens past L read as
-// dt = 0, so the cumsum stays flat in a ragged last chunk.
+// One block per (chunk, batch, 8-head slice): the work is a few MB in total, so
+// the grid is made wide (many small blocks) and every load of a block is issued
+// before any is used.  A block reads its Q x 8 slice of dt ([B][L][H]: 32
+// contiguous bytes per token), transposes it through shared memory, scans each
+// head's Q values with one warp (serial runs per lane + a warp-shuffle scan of
+// the run totals) and writes cumsum and dt as contiguous [B][H][Lp] rows.
+// Tokens past L read as dt = 0, so the cumsum stays flat in a ragged last chunk.
 #include "ssd_internal.cuh"
 
 namespace ssd {
 namespace {
 
-constexpr int kHeadsPerBlock = 32;
+constexpr int kHeadsPerBlock = 8;
 constexpr int kThreads = 256;
 
 __global__ void __launch_bounds__(kThreads) chunk_cumsum_kernel(Dims d, const float* __restrict__ dt,
                                                                  const float* __restrict__ A,
                                                                  float* __restrict__ cumsum,
                                                                  float* __restrict__ dt_t, int* status) {
-  extern __shared__ float sm[];
+  __shared__ float s_dt[kHeadsPerBlock * 257];
+  __shared__ float s_g[kHeadsPerBlock * 257];
   const int Q = d.Q;
   const int ld = Q + 1;  // odd row stride: the transposing writes hit distinct banks
-  float* s_dt = sm;
-  float* s_g = sm + kHeadsPerBlock * ld;
   const int c = blockIdx.x;
   const int h0 = blockIdx.y * kHeadsPerBlock;
   const int b = blockIdx.z;
   if (c == 0 && blockIdx.y == 0 && b == 0 && threadIdx.x == 0) *status = 0;
 
-  for (int idx = threadIdx.x; idx < Q * kHeadsPerBlock; idx += kThreads) {
+  // all of the block's loads first (Q * 8 / 256 <= 8 per thread), then the stores to shared memory
+  float v[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const int idx = threadIdx.x + k * kThreads;
     const int t = idx / kHeadsPerBlock, hh = idx % kHeadsPerBlock;
     const int tok = c * Q + t, h = h0 + hh;
-    float v = 0.f;
-    if (tok < d.L && h < d.H) v = dt[(static_cast<int64_t>(b) * d.L + tok) * d.H + h];
-    s_dt[hh * ld + t] = v;
+    v[k] = (t < Q && tok < d.L && h < d.H) ? dt[(static_cast<int64_t>(b) * d.L + tok) * d.H + h] : 0.f;
+  }
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const int idx = threadIdx.x + k * kThreads;
+    const int t = idx / kHeadsPerBlock, hh = idx % kHeadsPerBlock;
+    if (t < Q) s_dt[hh * ld + t] = v[k];
   }
   __syncthreads();
 
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31, hh = threadIdx.x >> 5;  // one warp per head
+  const int h = h0 + hh;
+  const float a_h = h < d.H ? A[h] : 0.f;
   const int per = Q / 32;  // 2, 4 or 8 tokens per lane
-  for (int hh = warp; hh < kHeadsPerBlock; hh += kThreads / 32) {
-    const int h = h0 + hh;
-    const float a_h = h < d.H ? A[h] : 0.f;
-    float run[8];
-    float acc = 0.f;
+  float run[8];
+  float acc = 0.f;
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      if (k < per) {
-        acc += s_dt[hh * ld + lane * per + k] * a_h;
-        run[k] = acc;
-      }
+  for (int k = 0; k < 8; ++k) {
+    if (k < per) {
+      acc += s_dt[hh * ld + lane * per + k] * a_h;
+      run[k] = acc;
     }
-    float incl = acc;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const float v = __shfl_up_sync(0xffffffffu, incl, off);
-      if (lane >= off) incl += v;
-    }
-    const float excl = incl - acc;
-#pragma unroll
-    for (int k = 0; k < 8; ++k)
-      if (k < per) s_g[hh * ld + lane * per + k] = run[k] + excl;
   }
+  float incl = acc;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const float u = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += u;
+  }
+  const float excl = incl - acc;
+#pragma unroll
+  for (int k = 0; k < 8; ++k)
+    if (k < per) s_g[hh * ld + lane * per + k] = run[k] + excl;
   __syncthreads();
 
   for (int idx = threadIdx.x; idx < kHeadsPerBlock * Q; idx += kThreads) {
-    const int hh = idx / Q, t = idx % Q;
-    const int h = h0 + hh;
-    if (h < d.H) {
-      const int64_t o = (static_cast<int64_t>(b) * d.H + h) * d.Lp + static_cast<int64_t>(c) * Q + t;
-      cumsum[o] = s_g[hh * ld + t];
-      dt_t[o] = s_dt[hh * ld + t];
+    const int hq = idx / Q, t = idx % Q;
+    if (h0 + hq < d.H) {
+      const int64_t o = (static_cast<int64_t>(b) * d.H + h0 + hq) * d.Lp + static_cast<int64_t>(c) * Q + t;
+      cumsum[o] = s_g[hq * ld + t];
+      dt_t[o] = s_dt[hq * ld + t];
     }
   }
 }
@@ -87,15 +92,7 @@ __global__ void __launch_bounds__(kThreads) chunk_cumsum_kernel(Dims d, const fl
 cudaError_t launch_chunk_cumsum(const Dims& d, const float* dt, const float* A, const Work& w,
                                 cudaStream_t stream) {
   const dim3 grid(d.nc, (d.H + kHeadsPerBlock - 1) / kHeadsPerBlock, d.B);
-  const size_t smem = 2u * kHeadsPerBlock * (d.Q + 1) * sizeof(float);
-  static size_t configured = 0;
-  if (smem > configured) {  // above 48 KB (chunk_size 256) the opt-in limit must be raised
-    cudaError_t e = cudaFuncSetAttribute(chunk_cumsum_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    configured = smem;
-  }
-  chunk_cumsum_kernel<<<grid, kThreads, smem, stream>>>(d, dt, A, w.cumsum, w.dt_t, w.status);
+  chunk_cumsum_kernel<<<grid, kThreads, 0, stream>>>(d, dt, A, w.cumsum, w.dt_t, w.status);
   return cudaGetLastError();
 }
 

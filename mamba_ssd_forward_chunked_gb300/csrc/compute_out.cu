@@ -10,33 +10,44 @@
 // operand may live in tensor memory while B must come from shared memory, so
 // the register-computed (fused) operand is routed to the A side.
 //
-// Per (batch b, chunk c, head h, 128-row tile t of the chunk), rows i in the
-// tile, columns j in 128-wide blocks jb <= t:
+// Work unit ("tile"): batch b, chunk c, 128-row block t of the chunk (rows i),
+// and a PAIR of heads (h0, h1) of one group.  Both heads read the same C and B,
+// so C B^T is computed once per tile and shared.  Columns j run over 128-wide
+// blocks jb <= t.  Per head h:
 //
-//     Y_off   = C_t hprev^T                          (K = dstate)
-//     CB_jb   = C_t B_jb^T                           (K = dstate)
-//     M_jb    = CB_jb o [j <= i] exp(G_i - G_j) dt_j (registers, -> TMEM)
-//     Y_intra = sum_jb M_jb X_jb                     (A = M from TMEM, K = 128)
-//     y_i     = exp(G_i) Y_off_i + Y_intra_i + D_h x_i
+//     Y_h   = C_t hprev_h^T                                  (K = dstate)
+//     Y_h  *= exp(G_i)            (row scale, in tensor memory)
+//     CB    = C_t B_jb^T                                     (K = dstate, shared)
+//     M_h   = CB o [j <= i] exp(G_i - G_j) dt_j              (registers -> TMEM)
+//     Y_h  += M_h X_h,jb                                     (A = M_h from TMEM)
+//     y_i   = Y_h[i] + D_h x_i
 //
-// Tensor memory (256 columns): [0,64) Y_off, [64,128) Y_intra, [128,256) CB,
-// overwritten in place by M (packed bf16 pairs in the bf16 path).  The
-// exponentials are factored so that every factor is <= 1: for a 32-column
-// strip entirely left of row i, exp(G_i - G_j) = exp(G_i - G_e) exp(G_e - G_j)
-// with e the strip's last column (one exp per row and strip plus a per-column
-// table); only the 32 x 32 blocks on the diagonal take one exp per element,
+// Tensor memory (512 columns): [0,128) CB (fp32), [128,256) M_h0, [256,384)
+// M_h1 (TF32: 128 columns; bf16: packed pairs in the first 64), [384,448)
+// Y_h0, [448,512) Y_h1.  The exponentials are factored so that every factor
+// is <= 1: for a 32-column strip entirely left of row i,
+// exp(G_i - G_j) = exp(G_i - G_e) exp(G_e - G_j) with e the strip's last
+// column; only the 32 x 32 blocks on the diagonal take one exp per element,
 // behind the causal select.
 //
-// TF32 (fp32 inputs) needs K-major shared-memory operands.  The C, B and state
-// tiles already have dstate (the K of their products) along the rows; the X
-// tiles of the intra-chunk product (K = tokens) arrive as 32 x 32 boxes that
-// the epilogue warps transpose in place before the first use.  bf16 reads X
-// MN-major directly.
-//
-// Warp roles (192 threads): warp 0 TMA, warp 1 TMEM owner + MMA issuer,
-// warps 2-5 mask pass and epilogue (TMEM lane quadrant = warp % 4).  C, B and
-// the entering state stream through a 2-slot ring in 128-byte K-slices; the
-// X tiles the intra-chunk product needs are loaded once.  Bounded waits.
+// GB300 mapping: a persistent grid (one CTA per SM, the CTA's tensor memory is
+// the whole 512 columns) walks the tiles with the head pair fastest, so the
+// CTAs running at one time share C and B tiles in L2.  Warp 0 issues TMA into
+// a 4-stage ring of 48 KB stages, in the order the MMA warp consumes them:
+// per column block, dstate slices of {C, B, the two entering states} then the
+// two heads' X blocks, so the next tile's loads stream in while this one
+// computes.  Warp 1 owns tensor memory and issues every MMA from one thread.
+// Warps 2-5 and 6-9 are two warpgroups, one per head of the pair: each scales
+// its carried-state accumulator, builds its masked matrix from the shared CB,
+// and writes its head's output rows, so the two heads' elementwise work runs
+// side by side.  A warpgroup loads the next tile's per-column data into
+// registers one tile ahead, keeps its row of x (for D*x) from the X block in
+// shared memory, and takes exponentials as 2^x of the cumsum scaled by
+// log2(e), so no global load sits on its critical path.  TF32 operands must be K-major in shared memory (an MN-major
+// TF32 operand read back as zeros in a layout probe on this part), so in the
+// fp32 path each warpgroup first transposes its X block (eight 32 x 32 boxes)
+// in place; bf16 reads X MN-major.  Every wait is bounded; on expiry the CTA
+// records SSD_ERR_DEVICE_TIMEOUT, stops, frees its tensor memory and exits.
 #include "ptx.cuh"
 #include "ssd_internal.cuh"
 #include "tile_transpose.cuh"
@@ -48,35 +59,46 @@ template <typename T>
 struct OutCfg {
   static constexpr bool kTF32 = sizeof(T) == 4;
   static constexpr int kAtom = 128 / static_cast<int>(sizeof(T));  // elements per 128-B row
-  static constexpr int kRows = 128;                                 // tile rows / block columns
-  static constexpr int kCBox = kRows * 128;                         // 128 rows x 128 B
-  static constexpr int kHBox = 64 * 128;                            // 64 state rows x 128 B
-  static constexpr int kSlot = 2 * kCBox + kHBox;
-  static constexpr int kXBoxes = 64 / kAtom;                        // x tile: 64 p = 1 or 2 atoms
-  static constexpr int kXTile = kXBoxes * kCBox;                    // 128 tokens x 64 p
-  static constexpr int kKStepMN = kTF32 ? 8 : 16;                  // tokens per MMA (intra product)
-  static constexpr int kStages = 2;
-  static constexpr int kThreads = 192;
-  static constexpr uint32_t kColYoff = 0, kColYint = 64, kColCB = 128, kTmemCols = 256;
+  static constexpr int kStages = 4;
+  static constexpr int kStageBytes = 48 * 1024;
+  static constexpr int kOffC = 0, kOffB = 16384, kOffH0 = 32768, kOffH1 = 40960;  // K-slice stage
+  static constexpr int kXBytes = kTF32 ? 32768 : 16384;                            // X stage: 128 tokens x 64 p
+  static constexpr int kKStepX = kTF32 ? 8 : 16;                                   // tokens per intra MMA
+  static constexpr int kThreads = 320;
+  static constexpr uint32_t kColCB = 0, kColM0 = 128, kColY0 = 384, kTmemCols = 512;
+  static constexpr int kWgFloats = 3 * 256;  // per warpgroup: cumsum, dt, strip factors for 256 columns
 };
 
 struct OutSmem {
-  uint32_t slots, xt, gs, dts, vref, bars, holder, total;
+  uint32_t ring, wg, bars, holder, total;
 };
 
 template <typename T>
-__host__ __device__ inline OutSmem out_smem_layout(int ntile) {
+__host__ __device__ constexpr OutSmem out_smem_layout() {
   using C = OutCfg<T>;
   OutSmem s{};
-  s.slots = 0;
-  s.xt = s.slots + C::kStages * C::kSlot;
-  s.gs = s.xt + ntile * C::kXTile;
-  s.dts = s.gs + ntile * 128 * 4;
-  s.vref = s.dts + ntile * 128 * 4;
-  s.bars = s.vref + ntile * 128 * 4;
-  s.holder = s.bars + (2 * C::kStages + 6) * 8;
+  s.ring = 0;
+  s.wg = C::kStages * C::kStageBytes;
+  s.bars = s.wg + 2 * C::kWgFloats * 4;
+  s.holder = s.bars + 32 * 8;
   s.total = s.holder + 16;
   return s;
+}
+
+struct TileId {
+  int b, c, t, h0;
+};
+
+__device__ __forceinline__ TileId decode_tile(int tile, const Dims& d, int ntile) {
+  const int hp = d.H / 2;
+  TileId id;
+  id.h0 = 2 * (tile % hp);
+  int rest = tile / hp;
+  id.t = rest % ntile;
+  rest /= ntile;
+  id.c = rest % d.nc;
+  id.b = rest / d.nc;
+  return id;
 }
 
 template <typename T>
@@ -88,27 +110,19 @@ __global__ void __launch_bounds__(OutCfg<T>::kThreads, 1)
   using C = OutCfg<T>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  constexpr OutSmem L = out_smem_layout<T>();
   const int Q = d.Q;
   const int ntile = Q >= 128 ? Q / 128 : 1;
-  const int t = blockIdx.x % ntile;
-  const int h = blockIdx.x / ntile;
-  const int c = blockIdx.y, b = blockIdx.z;
-  const int g = h / (d.H / d.G);
-  const int i0 = t * 128;
-  const int njb = t + 1;
+  const int ntiles = d.B * d.nc * ntile * (d.H / 2);
   const int NB = d.N / C::kAtom;
-  const OutSmem L = out_smem_layout<T>(ntile);
-  float* gs = reinterpret_cast<float*>(smem + L.gs);
-  float* dts = reinterpret_cast<float*>(smem + L.dts);
-  float* vref = reinterpret_cast<float*>(smem + L.vref);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
-  uint64_t* full = bars;
-  uint64_t* empty = bars + C::kStages;
-  uint64_t* xfull = bars + 2 * C::kStages;
-  uint64_t* cbfull = xfull + 1;
-  uint64_t* mready = xfull + 2;
-  uint64_t* mfree = xfull + 3;
-  uint64_t* yfull = xfull + 4;
+  uint64_t* full = bars;                  // [kStages]
+  uint64_t* empty = bars + C::kStages;    // [kStages]
+  uint64_t* cbfull = bars + 2 * C::kStages;
+  uint64_t* mready = cbfull + 1;          // [2]
+  uint64_t* mfree = cbfull + 3;           // [2]
+  uint64_t* yfull = cbfull + 5;
+  uint64_t* yfree = cbfull + 6;           // [2]
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L.holder);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -117,11 +131,14 @@ __global__ void __launch_bounds__(OutCfg<T>::kThreads, 1)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    mbar_init(xfull, 1);
     mbar_init(cbfull, 1);
-    mbar_init(mready, 128);
-    mbar_init(mfree, 1);
+    mbar_init(&mready[0], 128);
+    mbar_init(&mready[1], 128);
+    mbar_init(&mfree[0], 1);
+    mbar_init(&mfree[1], 1);
     mbar_init(yfull, 1);
+    mbar_init(&yfree[0], 128);
+    mbar_init(&yfree[1], 128);
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
@@ -141,234 +158,307 @@ __global__ void __launch_bounds__(OutCfg<T>::kThreads, 1)
   bool ok = true;
 
   if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      uint8_t* xt = smem + L.xt;
-      mbar_arrive_expect_tx(xfull, static_cast<uint32_t>(njb * C::kXTile));
-      for (int jb = 0; jb < njb; ++jb) {
-        if constexpr (C::kTF32) {
-          // 32-token x 32-p boxes; box (s, half) at s * 8 KB + half * 4 KB so that,
-          // once transposed, each 32-token K block is one 64-row K-major tile
-          for (int sb = 0; sb < 4; ++sb)
-            for (int hf = 0; hf < 2; ++hf)
-              tma_load_3d(xt + jb * C::kXTile + sb * 8192 + hf * 4096, &xmap, xfull, h * d.P + hf * 32,
-                          c * Q + jb * 128 + sb * 32, b);
-        } else {
-          tma_load_3d(xt + jb * C::kXTile, &xmap, xfull, h * d.P, c * Q + jb * 128, b);
-        }
-      }
-      const int hrow = ((b * d.nc + c) * d.H + h) * d.P;
       int it = 0;
-      for (int jb = 0; jb < njb && ok; ++jb) {
-        for (int nb = 0; nb < NB; ++nb, ++it) {
-          const int s = it % C::kStages, r = it / C::kStages;
-          if (r > 0 && !mbar_wait(&empty[s], (r - 1) & 1, spin_ns)) {
-            ok = false;
-            break;
+      for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+        const TileId id = decode_tile(tile, d, ntile);
+        const int g = id.h0 / (d.H / d.G);
+        const int hrow0 = ((id.b * d.nc + id.c) * d.H + id.h0) * d.P;
+        for (int jb = 0; jb <= id.t && ok; ++jb) {
+          for (int nb = 0; nb < NB + 2; ++nb, ++it) {
+            const int s = it % C::kStages, r = it / C::kStages;
+            if (r > 0 && !mbar_wait(&empty[s], (r - 1) & 1, spin_ns)) {
+              ok = false;
+              break;
+            }
+            uint8_t* st = smem + L.ring + s * C::kStageBytes;
+            if (nb < NB) {  // dstate slice: C, B (and the entering states at jb = 0)
+              mbar_arrive_expect_tx(&full[s], 32768u + (jb == 0 ? 16384u : 0u));
+              tma_load_4d(st + C::kOffC, &cmap, &full[s], nb * C::kAtom, g, id.c * Q + id.t * 128, id.b);
+              tma_load_4d(st + C::kOffB, &bmap, &full[s], nb * C::kAtom, g, id.c * Q + jb * 128, id.b);
+              if (jb == 0) {
+                tma_load_2d(st + C::kOffH0, &hmap, &full[s], nb * C::kAtom, hrow0);
+                tma_load_2d(st + C::kOffH1, &hmap, &full[s], nb * C::kAtom, hrow0 + d.P);
+              }
+            } else {  // X block of one head: 128 tokens x 64 p
+              const int h = id.h0 + (nb - NB);
+              mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(C::kXBytes));
+              if constexpr (C::kTF32) {
+                // 32 x 32 boxes at s * 8 KB + half * 4 KB: once transposed, each
+                // 32-token K block is one 64-row K-major tile
+                for (int sb = 0; sb < 4; ++sb)
+                  for (int hf = 0; hf < 2; ++hf)
+                    tma_load_3d(st + sb * 8192 + hf * 4096, &xmap, &full[s], h * d.P + hf * 32,
+                                id.c * Q + jb * 128 + sb * 32, id.b);
+              } else {
+                tma_load_3d(st, &xmap, &full[s], h * d.P, id.c * Q + jb * 128, id.b);
+              }
+            }
           }
-          uint8_t* slot = smem + L.slots + s * C::kSlot;
-          mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(2 * C::kCBox + (jb == 0 ? C::kHBox : 0)));
-          tma_load_4d(slot, &cmap, &full[s], nb * C::kAtom, g, c * Q + i0, b);
-          tma_load_4d(slot + C::kCBox, &bmap, &full[s], nb * C::kAtom, g, c * Q + jb * 128, b);
-          if (jb == 0) tma_load_2d(slot + 2 * C::kCBox, &hmap, &full[s], nb * C::kAtom, hrow);
         }
       }
     }
   } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       const uint32_t fmt = C::kTF32 ? 2u : 1u;
       const uint32_t id_yoff = idesc_f32acc(fmt, 128, 64, 0, 0);
       const uint32_t id_cb = idesc_f32acc(fmt, 128, 128, 0, 0);
       const uint32_t id_yint = idesc_f32acc(fmt, 128, 64, 0, C::kTF32 ? 0u : 1u);
-      const uint32_t xt = smem_u32(smem + L.xt);
-      int it = 0;
-      for (int jb = 0; jb < njb && ok; ++jb) {
-        if (jb > 0 && !mbar_wait(mfree, (jb - 1) & 1, spin_ns)) {
-          ok = false;
-          break;
-        }
-        for (int nb = 0; nb < NB; ++nb, ++it) {
-          const int s = it % C::kStages, r = it / C::kStages;
-          if (!mbar_wait(&full[s], r & 1, spin_ns)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t slot = smem_u32(smem + L.slots + s * C::kSlot);
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            // K-major, 128-B swizzle: K advances 32 B inside the atom row;
-            // SBO = 1024 B between 8-row groups; LBO unused.
-            const uint64_t ad = sdesc_sw128(slot + k * 32, 16, 1024);
-            const uint64_t bd = sdesc_sw128(slot + C::kCBox + k * 32, 16, 1024);
-            const uint32_t acc = (nb | k) != 0 ? 1u : 0u;
-            if (jb == 0) {
-              const uint64_t hd = sdesc_sw128(slot + 2 * C::kCBox + k * 32, 16, 1024);
-              mma_ss<C::kTF32>(tmem + C::kColYoff, ad, hd, id_yoff, acc);
+      int it = 0, ntd = 0, nm = 0;
+      for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x, ++ntd) {
+        const TileId id = decode_tile(tile, d, ntile);
+        for (int jb = 0; jb <= id.t && ok; ++jb) {
+          if (jb == 0 && ntd > 0) {  // both heads drained Y of the previous tile
+            if (!mbar_wait(&yfree[0], (ntd - 1) & 1, spin_ns) || !mbar_wait(&yfree[1], (ntd - 1) & 1, spin_ns)) {
+              ok = false;
+              break;
             }
-            mma_ss<C::kTF32>(tmem + C::kColCB, ad, bd, id_cb, acc);
           }
-          mma_commit(&empty[s]);
-        }
-        if (!ok) break;
-        mma_commit(cbfull);
-        if (!mbar_wait(mready, jb & 1, spin_ns)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        if (jb == 0 && !mbar_wait(xfull, 0, spin_ns)) {
-          ok = false;
-          break;
-        }
-        const uint32_t xb = xt + jb * C::kXTile;
+          for (int nb = 0; nb < NB; ++nb, ++it) {
+            const int s = it % C::kStages, r = it / C::kStages;
+            if (!mbar_wait(&full[s], r & 1, spin_ns)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t st = smem_u32(smem + L.ring + s * C::kStageBytes);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              // K-major, 128-B swizzle: a K step is 32 B along the row; SBO = 1024 B
+              const uint64_t ad = sdesc_sw128(st + C::kOffC + k * 32, 16, 1024);
+              const uint32_t acc = (nb | k) != 0 ? 1u : 0u;
+              if (jb == 0) {
+                mma_ss<C::kTF32>(tmem + C::kColY0, ad, sdesc_sw128(st + C::kOffH0 + k * 32, 16, 1024), id_yoff, acc);
+                mma_ss<C::kTF32>(tmem + C::kColY0 + 64, ad, sdesc_sw128(st + C::kOffH1 + k * 32, 16, 1024), id_yoff,
+                                 acc);
+              }
+              mma_ss<C::kTF32>(tmem + C::kColCB, ad, sdesc_sw128(st + C::kOffB + k * 32, 16, 1024), id_cb, acc);
+            }
+            mma_commit(&empty[s]);
+          }
+          if (!ok) break;
+          mma_commit(cbfull);
+          for (int hh = 0; hh < 2; ++hh, ++it) {
+            const int s = it % C::kStages, r = it / C::kStages;
+            if (!mbar_wait(&full[s], r & 1, spin_ns) || !mbar_wait(&mready[hh], nm & 1, spin_ns)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t xb = smem_u32(smem + L.ring + s * C::kStageBytes);
 #pragma unroll 4
-        for (int k = 0; k < 128 / C::kKStepMN; ++k) {
-          uint64_t xd;
-          if constexpr (C::kTF32) {
-            // B = X^T block, K-major: 64 p-rows of 32 tokens per 8 KB block;
-            // a K step of 8 tokens is 32 B along the row.
-            xd = sdesc_sw128(xb + (k >> 2) * 8192 + (k & 3) * 32, 16, 1024);
-          } else {
-            // B = X block, MN-major (p contiguous, one 128-B atom = 64 p):
-            // SBO = 1024 B between 8-token groups.
-            xd = sdesc_sw128(xb + k * C::kKStepMN * 128, C::kCBox, 1024);
+            for (int k = 0; k < 128 / C::kKStepX; ++k) {
+              uint64_t xd;
+              if constexpr (C::kTF32) {
+                xd = sdesc_sw128(xb + (k >> 2) * 8192 + (k & 3) * 32, 16, 1024);  // X^T, K-major
+              } else {
+                xd = sdesc_sw128(xb + k * C::kKStepX * 128, 16384, 1024);  // X, MN-major (one 64-p atom)
+              }
+              mma_ts<C::kTF32>(tmem + C::kColY0 + 64 * hh, tmem + C::kColM0 + 128 * hh + k * 8, xd, id_yint, 1u);
+            }
+            mma_commit(&empty[s]);
+            mma_commit(&mfree[hh]);
           }
-          mma_ts<C::kTF32>(tmem + C::kColYint, tmem + C::kColCB + k * 8, xd, id_yint, (jb | k) != 0 ? 1u : 0u);
+          ++nm;
         }
-        mma_commit(mfree);
+        if (ok) mma_commit(yfull);
       }
-      mma_commit(yfull);
     }
   } else {
-    const int et = threadIdx.x - 64;
-    const int64_t grow = (static_cast<int64_t>(b) * d.H + h) * d.Lp + static_cast<int64_t>(c) * Q;
-    const int ncol = 128 * ntile;
-    for (int j = et; j < ncol; j += 128) {
-      const bool in = j < Q;
-      gs[j] = cumsum[grow + (in ? j : Q - 1)];
-      dts[j] = in ? dt_t[grow + j] : 0.f;
-    }
-    named_bar_sync(1, 128);
-    for (int j = et; j < ncol; j += 128) vref[j] = expf(gs[j | 31] - gs[j]) * dts[j];
-    named_bar_sync(1, 128);
-    if constexpr (C::kTF32) {
-      // flip the X boxes to K-major before the first intra-chunk product
-      if (!mbar_wait(xfull, 0, spin_ns)) ok = false;
-      uint8_t* xt = smem + L.xt;
-      const int m = et & 63;
-      for (int box0 = 0; box0 < njb * 8; box0 += 2) {
-        uint8_t* bp = xt + (box0 + (et >> 6)) * 4096;
-        float4 v[4];
-        box_read_4x4(bp, m, v);
-        named_bar_sync(1, 128);
-        box_write_4x4_transposed(bp, m, v);
-      }
-      fence_proxy_async_smem();
-      named_bar_sync(1, 128);  // the D*x epilogue below reads other threads' writes
-    }
-
+    // ------------------------------------------------------------ one warpgroup per head
+    const int hh = (warp - 2) >> 2;
+    const int et = threadIdx.x - 64 - 128 * hh;  // 0..127
+    const uint32_t bar_id = 1 + hh;
+    float* gs = reinterpret_cast<float*>(smem + L.wg) + hh * C::kWgFloats;  // cumsum in log2 units
+    float* dts = gs + 256;
+    float* vref = gs + 512;
     const int quad = warp & 3;
-    const int r = quad * 32 + lane;  // TMEM lane = tile row
-    const int i = i0 + r;            // row within the chunk
-    const float Gi = gs[i];
+    const int r = quad * 32 + lane;  // TMEM lane = row of the tile
     const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+    const uint32_t colM = C::kColM0 + 128 * hh, colY = C::kColY0 + 64 * hh;
+    constexpr int kXRegs = C::kTF32 ? 64 : 32;  // x row of this thread (fp32, or packed bf16 pairs)
+    uint32_t xrow[kXRegs];
+    // per-tile column data (columns et and et + 128) and D_h, loaded one tile ahead
+    float pg[2], pd[2], pD = 0.f;
+    auto prefetch = [&](int tile) {
+      const TileId id = decode_tile(tile, d, ntile);
+      const int h = id.h0 + hh;
+      const int64_t grow = (static_cast<int64_t>(id.b) * d.H + h) * d.Lp + static_cast<int64_t>(id.c) * Q;
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const int j = et + 128 * k;
+        pg[k] = cumsum[grow + (j < Q ? j : Q - 1)];
+        pd[k] = j < Q ? dt_t[grow + j] : 0.f;
+      }
+      pD = Dvec[h];
+    };
+    if (static_cast<int>(blockIdx.x) < ntiles) prefetch(blockIdx.x);
+    int it = 0, ncb = 0, nm = 0, ntd = 0;
+    for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x, ++ntd) {
+      const TileId id = decode_tile(tile, d, ntile);
+      const int h = id.h0 + hh;
+      const int i = id.t * 128 + r;  // row within the chunk
+      const int ncol = 128 * (id.t + 1);
+      named_bar_sync(bar_id, 128);  // the previous tile's readers of gs / dts / vref are done
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const int j = et + 128 * k;
+        if (j < ncol) {
+          gs[j] = pg[k] * kLog2e;
+          dts[j] = pd[k];
+        }
+      }
+      const float Dh = pD;
+      if (tile + static_cast<int>(gridDim.x) < ntiles) prefetch(tile + gridDim.x);  // in flight during this tile
+      named_bar_sync(bar_id, 128);
+      for (int j = et; j < ncol; j += 128) vref[j] = fast_exp2(gs[j | 31] - gs[j]) * dts[j];
+      named_bar_sync(bar_id, 128);
+      const float Gi = gs[i];
 
-    for (int jb = 0; jb < njb; ++jb) {
-      if (!mbar_wait(cbfull, jb & 1, spin_ns)) {
+      for (int jb = 0; jb <= id.t; ++jb) {
+        if (!mbar_wait(cbfull, ncb & 1, spin_ns)) {
+          ok = false;
+          break;
+        }
+        ++ncb;
+        tc_fence_after();
+        it += NB;
+        const int xs = it + hh;  // ring stage holding this head's X block
+        it += 2;
+        uint8_t* xb = smem + L.ring + (xs % C::kStages) * C::kStageBytes;
+        if (jb == 0) {  // carried-state term: scale row i by exp(G_i)
+          const float eGi = fast_exp2(Gi);
+#pragma unroll 1
+          for (int half = 0; half < 2; ++half) {
+            uint32_t v[32];
+            tmem_ld32(tmem + lane_base + colY + half * 32, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int q = 0; q < 32; ++q) v[q] = __float_as_uint(__uint_as_float(v[q]) * eGi);
+            tmem_st32(tmem + lane_base + colY + half * 32, v);
+          }
+        }
+        if (nm > 0 && !mbar_wait(&mfree[hh], (nm - 1) & 1, spin_ns)) {  // M_h no longer read
+          ok = false;
+          break;
+        }
+        if (!mbar_wait(&full[xs % C::kStages], (xs / C::kStages) & 1, spin_ns)) {  // X block landed
+          ok = false;
+          break;
+        }
+        if constexpr (C::kTF32) {
+          // flip this head's X block to K-major (eight boxes, two per round)
+          const int m = et & 63;
+#pragma unroll 1
+          for (int box0 = 0; box0 < 8; box0 += 2) {
+            uint8_t* bp = xb + (box0 + (et >> 6)) * 4096;
+            float4 v[4];
+            box_read_4x4(bp, m, v);
+            named_bar_sync(bar_id, 128);
+            box_write_4x4_transposed(bp, m, v);
+          }
+          fence_proxy_async_smem();
+        }
+#pragma unroll 1
+        for (int cc = 0; cc < 4; ++cc) {
+          const int j0 = jb * 128 + cc * 32;
+          uint32_t v[32];
+          tmem_ld32(tmem + lane_base + C::kColCB + cc * 32, v);
+          tmem_ld_wait();
+          float m[32];
+          if (j0 + 31 < i) {  // strip strictly left of the diagonal (warp-uniform)
+            const float u = fast_exp2(Gi - gs[j0 + 31]);
+#pragma unroll
+            for (int q = 0; q < 32; ++q) m[q] = __uint_as_float(v[q]) * u * vref[j0 + q];
+          } else if (j0 > i) {  // strip strictly right of the diagonal (warp-uniform)
+#pragma unroll
+            for (int q = 0; q < 32; ++q) m[q] = 0.f;
+          } else {  // the 32 x 32 block on the diagonal: select, then exp (exponent <= 0)
+#pragma unroll
+            for (int q = 0; q < 32; ++q) {
+              const int j = j0 + q;
+              m[q] = j <= i ? __uint_as_float(v[q]) * fast_exp2(Gi - gs[j]) * dts[j] : 0.f;
+            }
+          }
+          if constexpr (C::kTF32) {
+            uint32_t o[32];
+#pragma unroll
+            for (int q = 0; q < 32; ++q) o[q] = __float_as_uint(round_tf32(m[q]));
+            tmem_st32(tmem + lane_base + colM + cc * 32, o);
+          } else {
+            uint32_t o[16];
+#pragma unroll
+            for (int q = 0; q < 16; ++q) o[q] = pack_bf16x2(m[2 * q], m[2 * q + 1]);
+            tmem_st16(tmem + lane_base + colM + cc * 16, o);
+          }
+        }
+        if (jb == id.t) {
+          // keep this row's x for the D*x term before the X block is released
+          if constexpr (C::kTF32) {
+            const uint8_t* bx = xb + (r >> 5) * 8192;
+#pragma unroll
+            for (int q = 0; q < 64; ++q)
+              xrow[q] = *reinterpret_cast<const uint32_t*>(bx + (q >> 5) * 4096 + box_t_offset(r & 31, q & 31));
+          } else {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              const uint4 v = *reinterpret_cast<const uint4*>(xb + r * 128 + ((k ^ (r & 7)) << 4));
+              xrow[4 * k] = v.x; xrow[4 * k + 1] = v.y; xrow[4 * k + 2] = v.z; xrow[4 * k + 3] = v.w;
+            }
+          }
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&mready[hh]);
+        ++nm;
+      }
+      if (!ok) break;
+
+      // epilogue: y_i = Y_h[i] + D_h x_i
+      if (!mbar_wait(yfull, ntd & 1, spin_ns)) {
         ok = false;
         break;
       }
       tc_fence_after();
-#pragma unroll 1
-      for (int cc = 0; cc < 4; ++cc) {
-        const int j0 = jb * 128 + cc * 32;
-        uint32_t v[32];
-        tmem_ld32(tmem + lane_base + C::kColCB + cc * 32, v);
+      const bool valid = (i < Q) && (id.c * Q + i < d.L);
+      const int64_t row = ((static_cast<int64_t>(id.b) * d.L + static_cast<int64_t>(id.c) * Q + i) * d.H + h) * d.P;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t yv[32];
+        tmem_ld32(tmem + lane_base + colY + half * 32, yv);
         tmem_ld_wait();
-        float m[32];
-        if (j0 + 31 < i) {  // strip strictly left of the diagonal (warp-uniform)
-          const float u = expf(Gi - gs[j0 + 31]);
+        if (valid) {
+          if constexpr (C::kTF32) {
+            float4* yr = reinterpret_cast<float4*>(y + row + half * 32);
 #pragma unroll
-          for (int q = 0; q < 32; ++q) m[q] = __uint_as_float(v[q]) * u * vref[j0 + q];
-        } else if (j0 > i) {  // strip strictly right of the diagonal (warp-uniform)
+            for (int k = 0; k < 8; ++k) {
+              const int q = 4 * k;
+              yr[k] = make_float4(fmaf(Dh, __uint_as_float(xrow[half * 32 + q]), __uint_as_float(yv[q])),
+                                  fmaf(Dh, __uint_as_float(xrow[half * 32 + q + 1]), __uint_as_float(yv[q + 1])),
+                                  fmaf(Dh, __uint_as_float(xrow[half * 32 + q + 2]), __uint_as_float(yv[q + 2])),
+                                  fmaf(Dh, __uint_as_float(xrow[half * 32 + q + 3]), __uint_as_float(yv[q + 3])));
+            }
+          } else {
+            uint4* yr = reinterpret_cast<uint4*>(y + row + half * 32);
 #pragma unroll
-          for (int q = 0; q < 32; ++q) m[q] = 0.f;
-        } else {  // the 32 x 32 block on the diagonal: select, then exp (exponent <= 0)
+            for (int k = 0; k < 4; ++k) {
+              uint32_t o[4];
 #pragma unroll
-          for (int q = 0; q < 32; ++q) {
-            const int j = j0 + q;
-            m[q] = j <= i ? __uint_as_float(v[q]) * expf(Gi - gs[j]) * dts[j] : 0.f;
+              for (int e = 0; e < 4; ++e) {
+                const uint32_t xw = xrow[half * 16 + 4 * k + e];
+                const int q = 8 * k + 2 * e;
+                o[e] = pack_bf16x2(fmaf(Dh, bf16_lo(xw), __uint_as_float(yv[q])),
+                                   fmaf(Dh, bf16_hi(xw), __uint_as_float(yv[q + 1])));
+              }
+              yr[k] = make_uint4(o[0], o[1], o[2], o[3]);
+            }
           }
         }
-        if constexpr (C::kTF32) {
-          uint32_t o[32];
-#pragma unroll
-          for (int q = 0; q < 32; ++q) o[q] = __float_as_uint(round_tf32(m[q]));
-          tmem_st32(tmem + lane_base + C::kColCB + cc * 32, o);
-        } else {
-          uint32_t o[16];
-#pragma unroll
-          for (int q = 0; q < 16; ++q) o[q] = pack_bf16x2(m[2 * q], m[2 * q + 1]);
-          tmem_st16(tmem + lane_base + C::kColCB + cc * 16, o);
-        }
       }
-      tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(mready);
-    }
-
-    if (ok && !mbar_wait(yfull, 0, spin_ns)) ok = false;
-    tc_fence_after();
-    const bool valid = (i < Q) && (c * Q + i < d.L);
-    const float eGi = expf(Gi);
-    const float Dh = Dvec[h];
-    const uint8_t* xrow_base = smem + L.xt + t * C::kXTile;
-    T* yrow = y + ((static_cast<int64_t>(b) * d.L + static_cast<int64_t>(c) * Q + i) * d.H + h) * d.P;
-#pragma unroll 1
-    for (int half = 0; half < 2; ++half) {
-      uint32_t yo[32], yi[32];
-      tmem_ld32(tmem + lane_base + C::kColYoff + half * 32, yo);
-      tmem_ld32(tmem + lane_base + C::kColYint + half * 32, yi);
-      tmem_ld_wait();
-      float out[32];
-      // x_i[p] for p = 32*half .. +31 from the x tile of this row block
-      if constexpr (C::kTF32) {
-        // transposed boxes: token r lives in K block r / 32, p in box half p / 32
-        const uint8_t* bx = xrow_base + (r >> 5) * 8192 + half * 4096;
-#pragma unroll
-        for (int q = 0; q < 32; ++q) {
-          const float xf = *reinterpret_cast<const float*>(bx + box_t_offset(r & 31, q));
-          out[q] = fmaf(eGi, __uint_as_float(yo[q]), __uint_as_float(yi[q])) + Dh * xf;
-        }
-      } else {
-        // MN-major rows: token r is row r, p in 16-B chunks of 8
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int chunk = half * 4 + k;
-          const uint4 xv = *reinterpret_cast<const uint4*>(xrow_base + r * 128 + ((chunk ^ (r & 7)) << 4));
-          const float xf[8] = {bf16_lo(xv.x), bf16_hi(xv.x), bf16_lo(xv.y), bf16_hi(xv.y),
-                               bf16_lo(xv.z), bf16_hi(xv.z), bf16_lo(xv.w), bf16_hi(xv.w)};
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int q = k * 8 + e;
-            out[q] = fmaf(eGi, __uint_as_float(yo[q]), __uint_as_float(yi[q])) + Dh * xf[e];
-          }
-        }
-      }
-      if (valid) {
-        if constexpr (C::kTF32) {
-          float4* o4 = reinterpret_cast<float4*>(yrow + half * 32);
-#pragma unroll
-          for (int k = 0; k < 8; ++k) o4[k] = make_float4(out[4 * k], out[4 * k + 1], out[4 * k + 2], out[4 * k + 3]);
-        } else {
-          uint4* o4 = reinterpret_cast<uint4*>(yrow + half * 32);
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            o4[k] = make_uint4(pack_bf16x2(out[8 * k], out[8 * k + 1]), pack_bf16x2(out[8 * k + 2], out[8 * k + 3]),
-                               pack_bf16x2(out[8 * k + 4], out[8 * k + 5]),
-                               pack_bf16x2(out[8 * k + 6], out[8 * k + 7]));
-        }
-      }
+      mbar_arrive(&yfree[hh]);
     }
   }
   if (!ok) atomicExch(status, static_cast<int>(SSD_ERR_DEVICE_TIMEOUT));
@@ -380,31 +470,44 @@ __global__ void __launch_bounds__(OutCfg<T>::kThreads, 1)
   }
 }
 
+int sm_count() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 148;
+  }
+  return n;
+}
+
 template <typename T>
-cudaError_t launch_impl(const Dims& d, const ComputeOutMaps& maps, const float* D, void* y, const Work& w,
-                        uint64_t spin_ns, cudaStream_t stream) {
+cudaError_t launch_impl(const Dims& d, const ComputeOutMaps& maps, const float* D, const void* x, void* y,
+                        const Work& w, uint64_t spin_ns, cudaStream_t stream) {
   using C = OutCfg<T>;
-  const int ntile = d.Q >= 128 ? d.Q / 128 : 1;
-  const size_t smem = 1024 + out_smem_layout<T>(ntile).total;
-  static size_t configured = 0;
-  if (smem > configured) {
+  const size_t smem = 1024 + out_smem_layout<T>().total;
+  static bool configured = false;
+  if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(compute_out_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    configured = smem;
+    configured = true;
   }
-  const dim3 grid(ntile * d.H, d.nc, d.B);
-  compute_out_kernel<T><<<grid, C::kThreads, smem, stream>>>(maps.cm, maps.bm, maps.hp, maps.x, d, w.cumsum,
-                                                             w.dt_t, D, static_cast<T*>(y), w.status, spin_ns);
+  const int ntile = d.Q >= 128 ? d.Q / 128 : 1;
+  const long long ntiles = static_cast<long long>(d.B) * d.nc * ntile * (d.H / 2);
+  const int grid = static_cast<int>(ntiles < sm_count() ? ntiles : sm_count());
+  (void)x;  // the D*x term reads x from the X blocks already in shared memory
+  compute_out_kernel<T><<<grid, C::kThreads, smem, stream>>>(maps.cm, maps.bm, maps.hp, maps.x, d, w.cumsum, w.dt_t,
+                                                             D, static_cast<T*>(y), w.status, spin_ns);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_compute_out(const Dims& d, bool bf16, const ComputeOutMaps& maps, const float* D, void* y,
-                               const Work& w, uint64_t spin_ns, cudaStream_t stream) {
-  return bf16 ? launch_impl<__nv_bfloat16>(d, maps, D, y, w, spin_ns, stream)
-              : launch_impl<float>(d, maps, D, y, w, spin_ns, stream);
+cudaError_t launch_compute_out(const Dims& d, bool bf16, const ComputeOutMaps& maps, const float* D, const void* x,
+                               void* y, const Work& w, uint64_t spin_ns, cudaStream_t stream) {
+  return bf16 ? launch_impl<__nv_bfloat16>(d, maps, D, x, y, w, spin_ns, stream)
+              : launch_impl<float>(d, maps, D, x, y, w, spin_ns, stream);
 }
 
 }  // namespace ssd

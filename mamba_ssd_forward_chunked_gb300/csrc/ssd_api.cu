@@ -289,7 +289,7 @@ ssd_status ssd_compute_out(const ssd_shape* shape, const void* x, const void* Bm
   ComputeOutMaps maps;
   const void* hp = bf16 ? static_cast<const void*>(w.states_bf16) : static_cast<const void*>(w.states);
   if (!build_out_maps(*shape, x, Bm, Cm, hp, &maps)) return SSD_ERR_CUDA;
-  return from_cuda(launch_compute_out(make_dims(*shape), bf16, maps, D, y, w, spin_limit_ns(),
+  return from_cuda(launch_compute_out(make_dims(*shape), bf16, maps, D, x, y, w, spin_limit_ns(),
                                       reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -322,7 +322,7 @@ ssd_status ssd_fwd(const ssd_shape* shape, const void* x, const float* dt, const
   cudaError_t e = launch_chunk_cumsum(d, dt, A, w, cs);
   if (e == cudaSuccess) e = launch_chunk_state(d, bf16, smaps, w, spin, cs);
   if (e == cudaSuccess) e = launch_state_passing(d, bf16, init_state, final_state, w, cs);
-  if (e == cudaSuccess) e = launch_compute_out(d, bf16, omaps, D, y, w, spin, cs);
+  if (e == cudaSuccess) e = launch_compute_out(d, bf16, omaps, D, x, y, w, spin, cs);
   return from_cuda(e);
 }
 

@@ -46,7 +46,7 @@ cudaError_t launch_chunk_state(const Dims& d, bool bf16, const ChunkStateMaps& m
 cudaError_t launch_state_passing(const Dims& d, bool bf16, const float* init, float* final_state,
                                  const Work& w, cudaStream_t stream);
 cudaError_t launch_compute_out(const Dims& d, bool bf16, const ComputeOutMaps& maps, const float* D,
-                               void* y, const Work& w, uint64_t spin_ns, cudaStream_t stream);
+                               const void* x, void* y, const Work& w, uint64_t spin_ns, cudaStream_t stream);
 cudaError_t launch_timeout_probe(int* status, uint64_t limit_ns, cudaStream_t stream);
 
 }  // namespace ssd

@@ -9,11 +9,11 @@
 // reads S_c once and writes the state entering chunk c once.
 //
 // Memory-bound by construction (no reuse): 16-byte vector loads and stores,
-// consecutive threads on consecutive n, and eight chunks of loads in flight
-// per thread before their (in-place) stores.  fp32 problems overwrite S_c
-// with the entering state; bf16 problems write it, rounded to bf16, to a
-// separate array (the compute_out tensor cores read bf16 operands) and leave
-// S_c in place.
+// consecutive threads on consecutive n, and a software pipeline that keeps the
+// next eight chunks' loads in flight while the current eight are stored.
+// fp32 problems overwrite S_c with the entering state; bf16 problems write it,
+// rounded to bf16, to a separate array (the compute_out tensor cores read bf16
+// operands) and leave S_c in place.
 #include "ssd_internal.cuh"
 
 namespace ssd {
@@ -43,16 +43,22 @@ __global__ void __launch_bounds__(kThreads) state_passing_kernel(Dims d, const f
   const int64_t base = (b * d.nc * d.H + h) * pn4 + e4;     // chunk 0
   float4* s4 = reinterpret_cast<float4*>(states);
 
-  for (int c0 = 0; c0 < d.nc; c0 += kPrefetch) {
-    float4 v[kPrefetch];
-    float decay[kPrefetch];
+  // rounds of kPrefetch chunks; the loads of round r+1 are issued before the
+  // stores of round r, so each thread always has a round of loads in flight
+  float4 cur[kPrefetch], nxt[kPrefetch];
+  float dcur[kPrefetch], dnxt[kPrefetch];
+  auto load_round = [&](int c0, float4 (&v)[kPrefetch], float (&dk)[kPrefetch]) {
 #pragma unroll
     for (int k = 0; k < kPrefetch; ++k) {
       if (c0 + k < d.nc) {
         v[k] = __ldcs(s4 + base + (c0 + k) * cstride);
-        decay[k] = expf(g_last[static_cast<int64_t>(c0 + k) * d.Q]);
+        dk[k] = g_last[static_cast<int64_t>(c0 + k) * d.Q];
       }
     }
+  };
+  load_round(0, cur, dcur);
+  for (int c0 = 0; c0 < d.nc; c0 += kPrefetch) {
+    if (c0 + kPrefetch < d.nc) load_round(c0 + kPrefetch, nxt, dnxt);
 #pragma unroll
     for (int k = 0; k < kPrefetch; ++k) {
       if (c0 + k < d.nc) {
@@ -67,12 +73,17 @@ __global__ void __launch_bounds__(kThreads) state_passing_kernel(Dims d, const f
         } else {
           s4[o] = st;
         }
-        const float dk = decay[k];
-        st.x = fmaf(dk, st.x, v[k].x);
-        st.y = fmaf(dk, st.y, v[k].y);
-        st.z = fmaf(dk, st.z, v[k].z);
-        st.w = fmaf(dk, st.w, v[k].w);
+        const float dk = expf(dcur[k]);
+        st.x = fmaf(dk, st.x, cur[k].x);
+        st.y = fmaf(dk, st.y, cur[k].y);
+        st.z = fmaf(dk, st.z, cur[k].z);
+        st.w = fmaf(dk, st.w, cur[k].w);
       }
+    }
+#pragma unroll
+    for (int k = 0; k < kPrefetch; ++k) {
+      cur[k] = nxt[k];
+      dcur[k] = dnxt[k];
     }
   }
   if (final_state) reinterpret_cast<float4*>(final_state)[bh * pn4 + e4] = st;
