@@ -33,17 +33,19 @@
 // GB300 mapping: a persistent grid (one CTA per SM, the CTA's tensor memory is
 // the whole 512 columns) walks the tiles with the head pair fastest, so the
 // CTAs running at one time share C and B tiles in L2.  Warp 0 issues TMA into
-// a 4-stage ring of 48 KB stages, in the order the MMA warp consumes them:
-// per column block, dstate slices of {C, B, the two entering states} then the
-// two heads' X blocks, so the next tile's loads stream in while this one
-// computes.  Warp 1 owns tensor memory and issues every MMA from one thread.
+// two rings, in the order the MMA warp consumes them: per column block, the
+// dstate slices of {C, B, the two entering states} (48 KB stages) and the two
+// heads' X blocks (a ring of its own, so X blocks are fetched up to two column
+// blocks ahead); the next tile's loads stream in while this one computes.  Warp 1 owns tensor memory and issues every MMA from one thread.
 // Warps 2-5 and 6-9 are two warpgroups, one per head of the pair: each scales
 // its carried-state accumulator, builds its masked matrix from the shared CB,
 // and writes its head's output rows, so the two heads' elementwise work runs
 // side by side.  A warpgroup loads the next tile's per-column data into
-// registers one tile ahead, keeps its row of x (for D*x) from the X block in
-// shared memory, and takes exponentials as 2^x of the cumsum scaled by
-// log2(e), so no global load sits on its critical path.  TF32 operands must be K-major in shared memory (an MN-major
+// registers one tile ahead, takes exponentials as 2^x of the cumsum scaled by
+// log2(e), and keeps the last X block of its head until the epilogue: it reads
+// x_i (for D*x) from it, overwrites it with y in the same swizzled layout and
+// writes y out with TMA tensor stores, so no global load or scattered store
+// sits on its critical path.  TF32 operands must be K-major in shared memory (an MN-major
 // TF32 operand read back as zeros in a layout probe on this part), so in the
 // fp32 path each warpgroup first transposes its X block (eight 32 x 32 boxes)
 // in place; bf16 reads X MN-major.  Every wait is bounded; on expiry the CTA
@@ -59,10 +61,11 @@ template <typename T>
 struct OutCfg {
   static constexpr bool kTF32 = sizeof(T) == 4;
   static constexpr int kAtom = 128 / static_cast<int>(sizeof(T));  // elements per 128-B row
-  static constexpr int kStages = 4;
+  static constexpr int kStages = 3;                                                // dstate-slice ring
   static constexpr int kStageBytes = 48 * 1024;
   static constexpr int kOffC = 0, kOffB = 16384, kOffH0 = 32768, kOffH1 = 40960;  // K-slice stage
   static constexpr int kXBytes = kTF32 ? 32768 : 16384;                            // X stage: 128 tokens x 64 p
+  static constexpr int kXStages = kTF32 ? 2 : 4;                                   // X ring
   static constexpr int kKStepX = kTF32 ? 8 : 16;                                   // tokens per intra MMA
   static constexpr int kThreads = 320;
   static constexpr uint32_t kColCB = 0, kColM0 = 128, kColY0 = 384, kTmemCols = 512;
@@ -70,7 +73,7 @@ struct OutCfg {
 };
 
 struct OutSmem {
-  uint32_t ring, wg, bars, holder, total;
+  uint32_t ring, xring, wg, bars, holder, total;
 };
 
 template <typename T>
@@ -78,7 +81,8 @@ __host__ __device__ constexpr OutSmem out_smem_layout() {
   using C = OutCfg<T>;
   OutSmem s{};
   s.ring = 0;
-  s.wg = C::kStages * C::kStageBytes;
+  s.xring = C::kStages * C::kStageBytes;
+  s.wg = s.xring + C::kXStages * C::kXBytes;
   s.bars = s.wg + 2 * C::kWgFloats * 4;
   s.holder = s.bars + 32 * 8;
   s.total = s.holder + 16;
@@ -101,12 +105,47 @@ __device__ __forceinline__ TileId decode_tile(int tile, const Dims& d, int ntile
   return id;
 }
 
+// One 32-column strip of the masked, decayed matrix for row i, in place:
+// v holds C_i . B_j for j = j0 .. j0 + 31 on entry and is written to the
+// tensor-memory A operand at `dst` (TF32: one column per element; bf16: packed
+// pairs).  gs is the cumsum in log2 units, vref[j] = 2^(gs[e] - gs[j]) dt_j
+// for e the last column of j's strip.
+template <bool kTF32>
+__device__ __forceinline__ void mask_strip(uint32_t (&v)[32], int j0, int i, float Gi, const float* gs,
+                                           const float* dts, const float* vref, uint32_t dst) {
+  if (j0 + 31 < i) {  // strip strictly left of the diagonal (warp-uniform)
+    const float u = fast_exp2(Gi - gs[j0 + 31]);
+#pragma unroll
+    for (int q = 0; q < 32; ++q) v[q] = __float_as_uint(__uint_as_float(v[q]) * u * vref[j0 + q]);
+  } else if (j0 > i) {  // strip strictly right of the diagonal (warp-uniform)
+#pragma unroll
+    for (int q = 0; q < 32; ++q) v[q] = 0u;
+  } else {  // the 32 x 32 block on the diagonal: select, then exp (exponent <= 0)
+#pragma unroll
+    for (int q = 0; q < 32; ++q) {
+      const int j = j0 + q;
+      v[q] = j <= i ? __float_as_uint(__uint_as_float(v[q]) * fast_exp2(Gi - gs[j]) * dts[j]) : 0u;
+    }
+  }
+  if constexpr (kTF32) {
+#pragma unroll
+    for (int q = 0; q < 32; ++q) v[q] = __float_as_uint(round_tf32(__uint_as_float(v[q])));
+    tmem_st32(dst, v);
+  } else {
+    uint32_t o[16];
+#pragma unroll
+    for (int q = 0; q < 16; ++q) o[q] = pack_bf16x2(__uint_as_float(v[2 * q]), __uint_as_float(v[2 * q + 1]));
+    tmem_st16(dst, o);
+  }
+}
+
 template <typename T>
 __global__ void __launch_bounds__(OutCfg<T>::kThreads, 1)
     compute_out_kernel(const __grid_constant__ CUtensorMap cmap, const __grid_constant__ CUtensorMap bmap,
-                       const __grid_constant__ CUtensorMap hmap, const __grid_constant__ CUtensorMap xmap, Dims d,
+                       const __grid_constant__ CUtensorMap hmap, const __grid_constant__ CUtensorMap xmap,
+                       const __grid_constant__ CUtensorMap ymap, Dims d,
                        const float* __restrict__ cumsum, const float* __restrict__ dt_t,
-                       const float* __restrict__ Dvec, T* __restrict__ y, int* status, uint64_t spin_ns) {
+                       const float* __restrict__ Dvec, int* status, uint64_t spin_ns) {
   using C = OutCfg<T>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -118,7 +157,9 @@ __global__ void __launch_bounds__(OutCfg<T>::kThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
   uint64_t* full = bars;                  // [kStages]
   uint64_t* empty = bars + C::kStages;    // [kStages]
-  uint64_t* cbfull = bars + 2 * C::kStages;
+  uint64_t* xfullb = bars + 2 * C::kStages;    // [kXStages]
+  uint64_t* xempty = xfullb + C::kXStages;      // [kXStages]
+  uint64_t* cbfull = xempty + C::kXStages;
   uint64_t* mready = cbfull + 1;          // [2]
   uint64_t* mfree = cbfull + 3;           // [2]
   uint64_t* yfull = cbfull + 5;
@@ -130,6 +171,10 @@ __global__ void __launch_bounds__(OutCfg<T>::kThreads, 1)
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
+    }
+    for (int s = 0; s < C::kXStages; ++s) {
+      mbar_init(&xfullb[s], 1);
+      mbar_init(&xempty[s], 1 + 128);  // the MMA commit and the head's warpgroup
     }
     mbar_init(cbfull, 1);
     mbar_init(&mready[0], 128);
@@ -146,6 +191,7 @@ __global__ void __launch_bounds__(OutCfg<T>::kThreads, 1)
     tma_prefetch_desc(&bmap);
     tma_prefetch_desc(&hmap);
     tma_prefetch_desc(&xmap);
+    tma_prefetch_desc(&ymap);
   }
   if (warp == 1) {
     tmem_alloc(tmem_holder, C::kTmemCols);
@@ -160,20 +206,24 @@ __global__ void __launch_bounds__(OutCfg<T>::kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      int it = 0;
+      int it = 0, xit = 0;
       for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
         const TileId id = decode_tile(tile, d, ntile);
         const int g = id.h0 / (d.H / d.G);
         const int hrow0 = ((id.b * d.nc + id.c) * d.H + id.h0) * d.P;
         for (int jb = 0; jb <= id.t && ok; ++jb) {
-          for (int nb = 0; nb < NB + 2; ++nb, ++it) {
-            const int s = it % C::kStages, r = it / C::kStages;
-            if (r > 0 && !mbar_wait(&empty[s], (r - 1) & 1, spin_ns)) {
+          for (int nb = 0; nb < NB + 2; ++nb) {
+            const bool kslice = nb < NB;
+            const int ring_n = kslice ? C::kStages : C::kXStages;
+            const int cnt = kslice ? it++ : xit++;
+            const int s = cnt % ring_n, r = cnt / ring_n;
+            uint64_t* emp = kslice ? &empty[s] : &xempty[s];
+            if (r > 0 && !mbar_wait(emp, (r - 1) & 1, spin_ns)) {
               ok = false;
               break;
             }
-            uint8_t* st = smem + L.ring + s * C::kStageBytes;
-            if (nb < NB) {  // dstate slice: C, B (and the entering states at jb = 0)
+            uint8_t* st = kslice ? smem + L.ring + s * C::kStageBytes : smem + L.xring + s * C::kXBytes;
+            if (kslice) {  // dstate slice: C, B (and the entering states at jb = 0)
               mbar_arrive_expect_tx(&full[s], 32768u + (jb == 0 ? 16384u : 0u));
               tma_load_4d(st + C::kOffC, &cmap, &full[s], nb * C::kAtom, g, id.c * Q + id.t * 128, id.b);
               tma_load_4d(st + C::kOffB, &bmap, &full[s], nb * C::kAtom, g, id.c * Q + jb * 128, id.b);
@@ -183,16 +233,16 @@ __global__ void __launch_bounds__(OutCfg<T>::kThreads, 1)
               }
             } else {  // X block of one head: 128 tokens x 64 p
               const int h = id.h0 + (nb - NB);
-              mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(C::kXBytes));
+              mbar_arrive_expect_tx(&xfullb[s], static_cast<uint32_t>(C::kXBytes));
               if constexpr (C::kTF32) {
                 // 32 x 32 boxes at s * 8 KB + half * 4 KB: once transposed, each
                 // 32-token K block is one 64-row K-major tile
                 for (int sb = 0; sb < 4; ++sb)
                   for (int hf = 0; hf < 2; ++hf)
-                    tma_load_3d(st + sb * 8192 + hf * 4096, &xmap, &full[s], h * d.P + hf * 32,
+                    tma_load_3d(st + sb * 8192 + hf * 4096, &xmap, &xfullb[s], h * d.P + hf * 32,
                                 id.c * Q + jb * 128 + sb * 32, id.b);
               } else {
-                tma_load_3d(st, &xmap, &full[s], h * d.P, id.c * Q + jb * 128, id.b);
+                tma_load_3d(st, &xmap, &xfullb[s], h * d.P, id.c * Q + jb * 128, id.b);
               }
             }
           }
@@ -206,7 +256,7 @@ __global__ void __launch_bounds__(OutCfg<T>::kThreads, 1)
       const uint32_t id_yoff = idesc_f32acc(fmt, 128, 64, 0, 0);
       const uint32_t id_cb = idesc_f32acc(fmt, 128, 128, 0, 0);
       const uint32_t id_yint = idesc_f32acc(fmt, 128, 64, 0, C::kTF32 ? 0u : 1u);
-      int it = 0, ntd = 0, nm = 0;
+      int it = 0, xit = 0, ntd = 0, nm = 0;
       for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x, ++ntd) {
         const TileId id = decode_tile(tile, d, ntile);
         for (int jb = 0; jb <= id.t && ok; ++jb) {
@@ -240,14 +290,14 @@ __global__ void __launch_bounds__(OutCfg<T>::kThreads, 1)
           }
           if (!ok) break;
           mma_commit(cbfull);
-          for (int hh = 0; hh < 2; ++hh, ++it) {
-            const int s = it % C::kStages, r = it / C::kStages;
-            if (!mbar_wait(&full[s], r & 1, spin_ns) || !mbar_wait(&mready[hh], nm & 1, spin_ns)) {
+          for (int hh = 0; hh < 2; ++hh, ++xit) {
+            const int s = xit % C::kXStages, r = xit / C::kXStages;
+            if (!mbar_wait(&xfullb[s], r & 1, spin_ns) || !mbar_wait(&mready[hh], nm & 1, spin_ns)) {
               ok = false;
               break;
             }
             tc_fence_after();
-            const uint32_t xb = smem_u32(smem + L.ring + s * C::kStageBytes);
+            const uint32_t xb = smem_u32(smem + L.xring + s * C::kXBytes);
 #pragma unroll 4
             for (int k = 0; k < 128 / C::kKStepX; ++k) {
               uint64_t xd;
@@ -258,7 +308,7 @@ __global__ void __launch_bounds__(OutCfg<T>::kThreads, 1)
               }
               mma_ts<C::kTF32>(tmem + C::kColY0 + 64 * hh, tmem + C::kColM0 + 128 * hh + k * 8, xd, id_yint, 1u);
             }
-            mma_commit(&empty[s]);
+            mma_commit(&xempty[s]);
             mma_commit(&mfree[hh]);
           }
           ++nm;
@@ -278,8 +328,6 @@ __global__ void __launch_bounds__(OutCfg<T>::kThreads, 1)
     const int r = quad * 32 + lane;  // TMEM lane = row of the tile
     const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
     const uint32_t colM = C::kColM0 + 128 * hh, colY = C::kColY0 + 64 * hh;
-    constexpr int kXRegs = C::kTF32 ? 64 : 32;  // x row of this thread (fp32, or packed bf16 pairs)
-    uint32_t xrow[kXRegs];
     // per-tile column data (columns et and et + 128) and D_h, loaded one tile ahead
     float pg[2], pd[2], pD = 0.f;
     auto prefetch = [&](int tile) {
@@ -295,7 +343,9 @@ __global__ void __launch_bounds__(OutCfg<T>::kThreads, 1)
       pD = Dvec[h];
     };
     if (static_cast<int>(blockIdx.x) < ntiles) prefetch(blockIdx.x);
-    int it = 0, ncb = 0, nm = 0, ntd = 0;
+    int xit = 0, ncb = 0, nm = 0, ntd = 0;
+    const uint8_t* xlast = nullptr;  // X block (this head, last column block) read by the epilogue
+    int xs_last = 0;
     for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x, ++ntd) {
       const TileId id = decode_tile(tile, d, ntile);
       const int h = id.h0 + hh;
@@ -324,27 +374,29 @@ __global__ void __launch_bounds__(OutCfg<T>::kThreads, 1)
         }
         ++ncb;
         tc_fence_after();
-        it += NB;
-        const int xs = it + hh;  // ring stage holding this head's X block
-        it += 2;
-        uint8_t* xb = smem + L.ring + (xs % C::kStages) * C::kStageBytes;
+        const int xs = xit + hh;  // X-ring stage holding this head's X block
+        xit += 2;
+        uint8_t* xb = smem + L.xring + (xs % C::kXStages) * C::kXBytes;
         if (jb == 0) {  // carried-state term: scale row i by exp(G_i)
           const float eGi = fast_exp2(Gi);
-#pragma unroll 1
-          for (int half = 0; half < 2; ++half) {
-            uint32_t v[32];
-            tmem_ld32(tmem + lane_base + colY + half * 32, v);
-            tmem_ld_wait();
+          uint32_t v0[32], v1[32];
+          tmem_ld32(tmem + lane_base + colY, v0);
+          tmem_ld32(tmem + lane_base + colY + 32, v1);
+          tmem_ld_wait();
 #pragma unroll
-            for (int q = 0; q < 32; ++q) v[q] = __float_as_uint(__uint_as_float(v[q]) * eGi);
-            tmem_st32(tmem + lane_base + colY + half * 32, v);
+          for (int q = 0; q < 32; ++q) {
+            v0[q] = __float_as_uint(__uint_as_float(v0[q]) * eGi);
+            v1[q] = __float_as_uint(__uint_as_float(v1[q]) * eGi);
           }
+          tmem_st32(tmem + lane_base + colY, v0);
+          tmem_st32(tmem + lane_base + colY + 32, v1);
         }
         if (nm > 0 && !mbar_wait(&mfree[hh], (nm - 1) & 1, spin_ns)) {  // M_h no longer read
           ok = false;
           break;
         }
-        if (!mbar_wait(&full[xs % C::kStages], (xs / C::kStages) & 1, spin_ns)) {  // X block landed
+        // X block landed (TF32 transposes it before its first use)
+        if (C::kTF32 && !mbar_wait(&xfullb[xs % C::kXStages], (xs / C::kXStages) & 1, spin_ns)) {
           ok = false;
           break;
         }
@@ -361,107 +413,111 @@ __global__ void __launch_bounds__(OutCfg<T>::kThreads, 1)
           }
           fence_proxy_async_smem();
         }
-#pragma unroll 1
-        for (int cc = 0; cc < 4; ++cc) {
-          const int j0 = jb * 128 + cc * 32;
-          uint32_t v[32];
-          tmem_ld32(tmem + lane_base + C::kColCB + cc * 32, v);
+        // masked matrix, four 32-column strips; two TMEM loads in flight so the
+        // next strip's load overlaps this strip's arithmetic
+        {
+          uint32_t va[32], vb[32];
+          tmem_ld32(tmem + lane_base + C::kColCB, va);
+          tmem_ld32(tmem + lane_base + C::kColCB + 32, vb);
           tmem_ld_wait();
-          float m[32];
-          if (j0 + 31 < i) {  // strip strictly left of the diagonal (warp-uniform)
-            const float u = fast_exp2(Gi - gs[j0 + 31]);
-#pragma unroll
-            for (int q = 0; q < 32; ++q) m[q] = __uint_as_float(v[q]) * u * vref[j0 + q];
-          } else if (j0 > i) {  // strip strictly right of the diagonal (warp-uniform)
-#pragma unroll
-            for (int q = 0; q < 32; ++q) m[q] = 0.f;
-          } else {  // the 32 x 32 block on the diagonal: select, then exp (exponent <= 0)
-#pragma unroll
-            for (int q = 0; q < 32; ++q) {
-              const int j = j0 + q;
-              m[q] = j <= i ? __uint_as_float(v[q]) * fast_exp2(Gi - gs[j]) * dts[j] : 0.f;
-            }
-          }
-          if constexpr (C::kTF32) {
-            uint32_t o[32];
-#pragma unroll
-            for (int q = 0; q < 32; ++q) o[q] = __float_as_uint(round_tf32(m[q]));
-            tmem_st32(tmem + lane_base + colM + cc * 32, o);
-          } else {
-            uint32_t o[16];
-#pragma unroll
-            for (int q = 0; q < 16; ++q) o[q] = pack_bf16x2(m[2 * q], m[2 * q + 1]);
-            tmem_st16(tmem + lane_base + colM + cc * 16, o);
-          }
-        }
-        if (jb == id.t) {
-          // keep this row's x for the D*x term before the X block is released
-          if constexpr (C::kTF32) {
-            const uint8_t* bx = xb + (r >> 5) * 8192;
-#pragma unroll
-            for (int q = 0; q < 64; ++q)
-              xrow[q] = *reinterpret_cast<const uint32_t*>(bx + (q >> 5) * 4096 + box_t_offset(r & 31, q & 31));
-          } else {
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-              const uint4 v = *reinterpret_cast<const uint4*>(xb + r * 128 + ((k ^ (r & 7)) << 4));
-              xrow[4 * k] = v.x; xrow[4 * k + 1] = v.y; xrow[4 * k + 2] = v.z; xrow[4 * k + 3] = v.w;
-            }
-          }
+          mask_strip<C::kTF32>(va, jb * 128, i, Gi, gs, dts, vref, tmem + lane_base + colM);
+          tmem_ld32(tmem + lane_base + C::kColCB + 64, va);
+          mask_strip<C::kTF32>(vb, jb * 128 + 32, i, Gi, gs, dts, vref, tmem + lane_base + colM + (C::kTF32 ? 32 : 16));
+          tmem_ld_wait();
+          tmem_ld32(tmem + lane_base + C::kColCB + 96, vb);
+          mask_strip<C::kTF32>(va, jb * 128 + 64, i, Gi, gs, dts, vref, tmem + lane_base + colM + (C::kTF32 ? 64 : 32));
+          tmem_ld_wait();
+          mask_strip<C::kTF32>(vb, jb * 128 + 96, i, Gi, gs, dts, vref, tmem + lane_base + colM + (C::kTF32 ? 96 : 48));
         }
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&mready[hh]);
         ++nm;
+        // this warpgroup's share of releasing the X block; the last one is kept for D*x
+        if (!C::kTF32 && !mbar_wait(&xfullb[xs % C::kXStages], (xs / C::kXStages) & 1, spin_ns)) {
+          ok = false;
+          break;
+        }
+        if (jb < id.t) {
+          mbar_arrive(&xempty[xs % C::kXStages]);
+        } else {
+          xlast = xb;
+          xs_last = xs % C::kXStages;
+        }
       }
       if (!ok) break;
 
-      // epilogue: y_i = Y_h[i] + D_h x_i
+      // epilogue: y_i = Y_h[i] + D_h x_i, written over x in the X block and
+      // stored with TMA (rows past Q are not stored; TMA clips rows past L)
       if (!mbar_wait(yfull, ntd & 1, spin_ns)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const bool valid = (i < Q) && (id.c * Q + i < d.L);
-      const int64_t row = ((static_cast<int64_t>(id.b) * d.L + static_cast<int64_t>(id.c) * Q + i) * d.H + h) * d.P;
+      uint32_t yall[2][32];
+      tmem_ld32(tmem + lane_base + colY, yall[0]);
+      tmem_ld32(tmem + lane_base + colY + 32, yall[1]);
+      tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(&yfree[hh]);  // Y_h may be overwritten by the next tile's MMAs
+      uint8_t* xy = const_cast<uint8_t*>(xlast);
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
-        uint32_t yv[32];
-        tmem_ld32(tmem + lane_base + colY + half * 32, yv);
-        tmem_ld_wait();
-        if (valid) {
-          if constexpr (C::kTF32) {
-            float4* yr = reinterpret_cast<float4*>(y + row + half * 32);
+        const uint32_t (&yv)[32] = yall[half];
+        if constexpr (C::kTF32) {
+          // box (r / 32, half) holds x transposed (row = p); y goes back untransposed
+          // (row = token).  The box belongs to this warp alone, so a warp sync
+          // separates its reads from its writes.
+          uint8_t* bx = xy + (r >> 5) * 8192 + half * 4096;
+          float out[32];
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-              const int q = 4 * k;
-              yr[k] = make_float4(fmaf(Dh, __uint_as_float(xrow[half * 32 + q]), __uint_as_float(yv[q])),
-                                  fmaf(Dh, __uint_as_float(xrow[half * 32 + q + 1]), __uint_as_float(yv[q + 1])),
-                                  fmaf(Dh, __uint_as_float(xrow[half * 32 + q + 2]), __uint_as_float(yv[q + 2])),
-                                  fmaf(Dh, __uint_as_float(xrow[half * 32 + q + 3]), __uint_as_float(yv[q + 3])));
+          for (int q = 0; q < 32; ++q)
+            out[q] = fmaf(Dh, *reinterpret_cast<const float*>(bx + box_t_offset(r & 31, q)), __uint_as_float(yv[q]));
+          __syncwarp();
+          const int rr = r & 31;
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            *reinterpret_cast<float4*>(bx + rr * 128 + ((k ^ (rr & 7)) << 4)) =
+                make_float4(out[4 * k], out[4 * k + 1], out[4 * k + 2], out[4 * k + 3]);
+        } else {
+          // MN-major rows: token r is row r, p in 16-B chunks of 8 (in place)
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            uint4* px = reinterpret_cast<uint4*>(xy + r * 128 + (((half * 4 + k) ^ (r & 7)) << 4));
+            const uint4 xv = *px;
+            const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+            uint32_t o[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int q = 8 * k + 2 * e;
+              o[e] = pack_bf16x2(fmaf(Dh, bf16_lo(xw[e]), __uint_as_float(yv[q])),
+                                 fmaf(Dh, bf16_hi(xw[e]), __uint_as_float(yv[q + 1])));
             }
-          } else {
-            uint4* yr = reinterpret_cast<uint4*>(y + row + half * 32);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              uint32_t o[4];
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const uint32_t xw = xrow[half * 16 + 4 * k + e];
-                const int q = 8 * k + 2 * e;
-                o[e] = pack_bf16x2(fmaf(Dh, bf16_lo(xw), __uint_as_float(yv[q])),
-                                   fmaf(Dh, bf16_hi(xw), __uint_as_float(yv[q + 1])));
-              }
-              yr[k] = make_uint4(o[0], o[1], o[2], o[3]);
-            }
+            *px = make_uint4(o[0], o[1], o[2], o[3]);
           }
         }
       }
-      tc_fence_before();
-      mbar_arrive(&yfree[hh]);
+      fence_proxy_async_smem();
+      named_bar_sync(bar_id, 128);
+      if (et == 0) {
+        const int nbox = Q >= 128 ? 4 : Q / 32;  // 32-token boxes of valid rows
+        const int tok0 = id.c * Q + id.t * 128;
+        for (int sb = 0; sb < nbox; ++sb) {
+          if constexpr (C::kTF32) {
+            tma_store_3d(&ymap, xy + sb * 8192, h * d.P, tok0 + 32 * sb, id.b);
+            tma_store_3d(&ymap, xy + sb * 8192 + 4096, h * d.P + 32, tok0 + 32 * sb, id.b);
+          } else {
+            tma_store_3d(&ymap, xy + sb * 4096, h * d.P, tok0 + 32 * sb, id.b);
+          }
+        }
+        tma_store_commit();
+        tma_store_wait_read();  // the X block may be refilled once the stores have read it
+      }
+      mbar_arrive(&xempty[xs_last]);
     }
   }
   if (!ok) atomicExch(status, static_cast<int>(SSD_ERR_DEVICE_TIMEOUT));
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");  // this thread's TMA stores are complete
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -497,8 +553,9 @@ cudaError_t launch_impl(const Dims& d, const ComputeOutMaps& maps, const float* 
   const long long ntiles = static_cast<long long>(d.B) * d.nc * ntile * (d.H / 2);
   const int grid = static_cast<int>(ntiles < sm_count() ? ntiles : sm_count());
   (void)x;  // the D*x term reads x from the X blocks already in shared memory
-  compute_out_kernel<T><<<grid, C::kThreads, smem, stream>>>(maps.cm, maps.bm, maps.hp, maps.x, d, w.cumsum, w.dt_t,
-                                                             D, static_cast<T*>(y), w.status, spin_ns);
+  (void)y;  // written through maps.y
+  compute_out_kernel<T><<<grid, C::kThreads, smem, stream>>>(maps.cm, maps.bm, maps.hp, maps.x, maps.y, d, w.cumsum,
+                                                             w.dt_t, D, w.status, spin_ns);
   return cudaGetLastError();
 }
 

@@ -147,7 +147,7 @@ bool build_state_maps(const ssd_shape& s, const void* x, const void* Bm, ChunkSt
 }
 
 bool build_out_maps(const ssd_shape& s, const void* x, const void* Bm, const void* Cm, const void* hp_states,
-                    ComputeOutMaps* m) {
+                    const void* y, ComputeOutMaps* m) {
   const bool bf16 = s.dtype == SSD_BF16;
   const uint64_t es = esize(s);
   const uint32_t atom = static_cast<uint32_t>(128 / es);
@@ -173,6 +173,8 @@ bool build_out_maps(const ssd_shape& s, const void* x, const void* Bm, const voi
     // bf16: one 128-token x 64-p box per block; fp32: 32 x 32 boxes (transposed in shared memory)
     const uint32_t box[3] = {atom, bf16 ? 128u : 32u, 1};
     if (!encode(&m->x, bf16, 3, x, dims, str, box)) return false;
+    const uint32_t ybox[3] = {atom, 32u, 1};
+    if (!encode(&m->y, bf16, 3, y, dims, str, ybox)) return false;
   }
   return true;
 }
@@ -288,7 +290,7 @@ ssd_status ssd_compute_out(const ssd_shape* shape, const void* x, const void* Bm
   Work w = carve(workspace, L, bf16);
   ComputeOutMaps maps;
   const void* hp = bf16 ? static_cast<const void*>(w.states_bf16) : static_cast<const void*>(w.states);
-  if (!build_out_maps(*shape, x, Bm, Cm, hp, &maps)) return SSD_ERR_CUDA;
+  if (!build_out_maps(*shape, x, Bm, Cm, hp, y, &maps)) return SSD_ERR_CUDA;
   return from_cuda(launch_compute_out(make_dims(*shape), bf16, maps, D, x, y, w, spin_limit_ns(),
                                       reinterpret_cast<cudaStream_t>(stream)));
 }
@@ -314,7 +316,7 @@ ssd_status ssd_fwd(const ssd_shape* shape, const void* x, const float* dt, const
   ChunkStateMaps smaps;
   ComputeOutMaps omaps;
   const void* hp = bf16 ? static_cast<const void*>(w.states_bf16) : static_cast<const void*>(w.states);
-  if (!build_state_maps(*shape, x, Bm, &smaps) || !build_out_maps(*shape, x, Bm, Cm, hp, &omaps))
+  if (!build_state_maps(*shape, x, Bm, &smaps) || !build_out_maps(*shape, x, Bm, Cm, hp, y, &omaps))
     return SSD_ERR_CUDA;
   const Dims d = make_dims(*shape);
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);

@@ -37,6 +37,7 @@ struct ComputeOutMaps {
   CUtensorMap bm;  // Bm, same box
   CUtensorMap hp;  // entering states [(B*nc*H*P)][N], box {128 B of n, 64 rows}
   CUtensorMap x;   // x [B][L][H*P], box {128 B of p, 128 (bf16) or 32 (fp32) tokens, 1}
+  CUtensorMap y;   // y [B][L][H*P], box {128 B of p, 32 tokens, 1} (TMA stores)
 };
 
 cudaError_t launch_chunk_cumsum(const Dims& d, const float* dt, const float* A, const Work& w,
