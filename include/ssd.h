@@ -80,8 +80,9 @@ typedef struct {
  *   status      int32 device status word (0 = OK)
  *   cumsum      fp32 [B][H][nc*Q]  inclusive cumsum of dt*A within each chunk
  *   dt_t        fp32 [B][H][nc*Q]  dt transposed to head-major order (0 past L)
- *   states      fp32 [B][nc][H][P][N]  chunk states S_c; after the state pass,
- *               for SSD_F32 the state entering each chunk (in place)
+ *   states      [B][nc][H][P][N] chunk states S_c, fp32 for SSD_F32 and bf16
+ *               for SSD_BF16; after the state pass, for SSD_F32 the state
+ *               entering each chunk (in place)
  *   states_bf16 bf16 [B][nc][H][P][N]  (SSD_BF16 only) state entering each
  *               chunk, rounded to bf16 for the output kernel's tensor cores
  * nc = ceil(seqlen / chunk_size). */

@@ -172,7 +172,8 @@ def workspace_views(shape: ssd_shape, ws: torch.Tensor) -> Dict[str, torch.Tenso
         "status": view(L["status"], 1, torch.int32, (1,)),
         "cumsum": view(L["cumsum"], B * H * Lp, torch.float32, (B, H, Lp)),
         "dt_t": view(L["dt_t"], B * H * Lp, torch.float32, (B, H, Lp)),
-        "states": view(L["states"], B * nc * H * P * N, torch.float32, (B, nc, H, P, N)),
+        "states": view(L["states"], B * nc * H * P * N,
+                       torch.bfloat16 if shape.dtype == SSD_BF16 else torch.float32, (B, nc, H, P, N)),
     }
     if shape.dtype == SSD_BF16:
         out["states_bf16"] = view(L["states_bf16"], B * nc * H * P * N, torch.bfloat16, (B, nc, H, P, N))

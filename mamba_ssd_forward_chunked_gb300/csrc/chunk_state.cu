@@ -14,7 +14,10 @@
 // (h, p) contiguous, so one TMA box row covers both), K runs over the chunk's
 // tokens, and the group's B tile is the shared N-side operand.  Both operands
 // come straight from the token-major global layouts, so both are MN-major in
-// shared memory (128-byte swizzle, TMA-written).  The head-dependent token
+// shared memory (128-byte swizzle, TMA-written).  S_c leaves through shared
+// memory and TMA stores, in fp32 for fp32 inputs and in bf16 for bf16 inputs
+// (its rounding, 2^-9 relative, is far inside the bf16 tolerance and halves
+// the bytes this kernel writes and the state pass reads).  The head-dependent token
 // weights w_j are applied in shared memory, in place, between the TMA landing
 // and the MMA -- a row of a 128-byte swizzle atom is one token of one head, so
 // the swizzle never moves data across rows.  The fp32 accumulator lives in
@@ -56,9 +59,9 @@ __host__ __device__ inline uint32_t state_stage_bytes(int N, int atom, int box, 
 
 template <typename T>
 __global__ void __launch_bounds__(StateCfg<T>::kThreads, 1)
-    chunk_state_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap bmap, Dims d,
-                       const float* __restrict__ cumsum, const float* __restrict__ dt_t,
-                       float* __restrict__ states, int* status, uint64_t spin_ns) {
+    chunk_state_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap bmap,
+                       const __grid_constant__ CUtensorMap smap, Dims d, const float* __restrict__ cumsum,
+                       const float* __restrict__ dt_t, int* status, uint64_t spin_ns) {
   using C = StateCfg<T>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -91,6 +94,7 @@ __global__ void __launch_bounds__(StateCfg<T>::kThreads, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&xmap);
     tma_prefetch_desc(&bmap);
+    tma_prefetch_desc(&smap);
   }
   if (warp == 1) {
     tmem_alloc(tmem_holder, tmem_cols);
@@ -219,20 +223,48 @@ __global__ void __launch_bounds__(StateCfg<T>::kThreads, 1)
     }
     if (ok && !mbar_wait(accum, 0, spin_ns)) ok = false;
     tc_fence_after();
-    // drain: TMEM lane = 64 * (head within the pair) + p, column = n
+    // drain: TMEM lane = 64 * (head within the pair) + p, column = n.  Rows go
+    // to shared memory (the pipeline stages are idle now) in the 128-B swizzled
+    // box layout of the states tensor map -- fp32, or bf16 for bf16 inputs --
+    // and leave with TMA tensor stores, so the writes are whole lines.
     const int quad = warp & 3;
     const int row = quad * 32 + lane;
-    const int hl = row >> 6, p = row & 63;
-    float* out = states + ((((static_cast<int64_t>(b) * d.nc + c) * d.H + h0 + hl) * d.P + p) * N);
-    for (int n0 = 0; n0 < N; n0 += 32) {
-      uint32_t v[32];
-      tmem_ld32(tmem + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(n0), v);
-      tmem_ld_wait();
-      float4* o = reinterpret_cast<float4*>(out + n0);
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+    constexpr int kSAtom = C::kAtom;  // states elements per 128-B box row (same dtype as the inputs)
+    uint8_t* stage = smem;
+    auto put = [&](int n0, const uint32_t (&v)[32]) {
+      uint8_t* box = stage + (n0 / kSAtom) * (128 * 128) + row * 128;
+      if constexpr (C::kTF32) {
 #pragma unroll
-      for (int k = 0; k < 8; ++k)
-        o[k] = make_float4(__uint_as_float(v[4 * k]), __uint_as_float(v[4 * k + 1]), __uint_as_float(v[4 * k + 2]),
-                           __uint_as_float(v[4 * k + 3]));
+        for (int k = 0; k < 8; ++k)
+          *reinterpret_cast<uint4*>(box + ((k ^ (row & 7)) << 4)) = make_uint4(v[4 * k], v[4 * k + 1], v[4 * k + 2],
+                                                                                 v[4 * k + 3]);
+      } else {
+        const int c0 = ((n0 / 32) & 1) * 4;  // 32 bf16 fill half of a 128-B row
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          *reinterpret_cast<uint4*>(box + (((c0 + k) ^ (row & 7)) << 4)) =
+              make_uint4(pack_bf16x2(__uint_as_float(v[8 * k]), __uint_as_float(v[8 * k + 1])),
+                         pack_bf16x2(__uint_as_float(v[8 * k + 2]), __uint_as_float(v[8 * k + 3])),
+                         pack_bf16x2(__uint_as_float(v[8 * k + 4]), __uint_as_float(v[8 * k + 5])),
+                         pack_bf16x2(__uint_as_float(v[8 * k + 6]), __uint_as_float(v[8 * k + 7])));
+      }
+    };
+    for (int n0 = 0; n0 < N; n0 += 64) {
+      uint32_t va[32], vb[32];
+      tmem_ld32(lane_addr + static_cast<uint32_t>(n0), va);
+      tmem_ld32(lane_addr + static_cast<uint32_t>(n0 + 32), vb);
+      tmem_ld_wait();
+      put(n0, va);
+      put(n0 + 32, vb);
+    }
+    fence_proxy_async_smem();
+    named_bar_sync(1, 128);
+    if (threadIdx.x == 64) {
+      const int row0 = ((b * d.nc + c) * d.H + h0) * d.P;
+      for (int k = 0; k < N / kSAtom; ++k) tma_store_2d(&smap, stage + k * (128 * 128), k * kSAtom, row0);
+      tma_store_commit();
+      asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
     }
   }
   if (!ok) atomicExch(status, static_cast<int>(SSD_ERR_DEVICE_TIMEOUT));
@@ -259,7 +291,7 @@ cudaError_t launch_impl(const Dims& d, const ChunkStateMaps& maps, const Work& w
     configured = smem;
   }
   const dim3 grid(d.H / 2, d.nc, d.B);
-  chunk_state_kernel<T><<<grid, C::kThreads, smem, stream>>>(maps.x, maps.bm, d, w.cumsum, w.dt_t, w.states,
+  chunk_state_kernel<T><<<grid, C::kThreads, smem, stream>>>(maps.x, maps.bm, maps.s, d, w.cumsum, w.dt_t,
                                                              w.status, spin_ns);
   return cudaGetLastError();
 }

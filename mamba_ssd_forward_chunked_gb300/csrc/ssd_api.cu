@@ -93,7 +93,7 @@ ssd_status layout_of(const ssd_shape* shape, ssd_workspace_layout* out) {
   L.dt_t = off;
   off = align_up(off + heads * lp * sizeof(float));
   L.states = off;
-  off = align_up(off + nstate * sizeof(float));
+  off = align_up(off + nstate * (s.dtype == SSD_BF16 ? sizeof(__nv_bfloat16) : sizeof(float)));
   L.states_bf16 = off;
   if (s.dtype == SSD_BF16) off = align_up(off + nstate * sizeof(__nv_bfloat16));
   L.total = off;
@@ -107,7 +107,7 @@ Work carve(void* ws, const ssd_workspace_layout& L, bool bf16) {
   w.status = reinterpret_cast<int*>(p + L.status);
   w.cumsum = reinterpret_cast<float*>(p + L.cumsum);
   w.dt_t = reinterpret_cast<float*>(p + L.dt_t);
-  w.states = reinterpret_cast<float*>(p + L.states);
+  w.states = p + L.states;
   w.states_bf16 = bf16 ? reinterpret_cast<__nv_bfloat16*>(p + L.states_bf16) : nullptr;
   return w;
 }
@@ -124,7 +124,7 @@ ssd_status from_cuda(cudaError_t e) { return e == cudaSuccess ? SSD_OK : SSD_ERR
 
 size_t esize(const ssd_shape& s) { return s.dtype == SSD_BF16 ? 2 : 4; }
 
-bool build_state_maps(const ssd_shape& s, const void* x, const void* Bm, ChunkStateMaps* m) {
+bool build_state_maps(const ssd_shape& s, const void* x, const void* Bm, const void* states, ChunkStateMaps* m) {
   const bool bf16 = s.dtype == SSD_BF16;
   const uint64_t es = esize(s);
   const uint32_t atom = static_cast<uint32_t>(128 / es);
@@ -142,6 +142,14 @@ bool build_state_maps(const ssd_shape& s, const void* x, const void* Bm, ChunkSt
     const uint64_t str[3] = {s.dstate * es, gn * es, gn * es * s.seqlen};
     const uint32_t box[4] = {atom, 1, 32, 1};
     if (!encode(&m->bm, bf16, 4, Bm, dims, str, box)) return false;
+  }
+  {
+    const int64_t nc = (s.seqlen + s.chunk_size - 1) / s.chunk_size;
+    const uint64_t rows = static_cast<uint64_t>(s.batch) * nc * s.nheads * s.headdim;
+    const uint64_t dims[2] = {static_cast<uint64_t>(s.dstate), rows};
+    const uint64_t str[1] = {s.dstate * es};
+    const uint32_t box[2] = {atom, 128};
+    if (!encode(&m->s, bf16, 2, states, dims, str, box)) return false;
   }
   return true;
 }
@@ -250,9 +258,9 @@ ssd_status ssd_chunk_state(const ssd_shape* shape, const void* x, const void* Bm
   if (empty_problem(*shape)) return SSD_OK;
   if (!x || !Bm || !aligned16(x) || !aligned16(Bm)) return SSD_ERR_INVALID_ARG;
   const bool bf16 = shape->dtype == SSD_BF16;
-  ChunkStateMaps maps;
-  if (!build_state_maps(*shape, x, Bm, &maps)) return SSD_ERR_CUDA;
   Work w = carve(workspace, L, bf16);
+  ChunkStateMaps maps;
+  if (!build_state_maps(*shape, x, Bm, w.states, &maps)) return SSD_ERR_CUDA;
   return from_cuda(
       launch_chunk_state(make_dims(*shape), bf16, maps, w, spin_limit_ns(), reinterpret_cast<cudaStream_t>(stream)));
 }
@@ -316,7 +324,7 @@ ssd_status ssd_fwd(const ssd_shape* shape, const void* x, const float* dt, const
   ChunkStateMaps smaps;
   ComputeOutMaps omaps;
   const void* hp = bf16 ? static_cast<const void*>(w.states_bf16) : static_cast<const void*>(w.states);
-  if (!build_state_maps(*shape, x, Bm, &smaps) || !build_out_maps(*shape, x, Bm, Cm, hp, y, &omaps))
+  if (!build_state_maps(*shape, x, Bm, w.states, &smaps) || !build_out_maps(*shape, x, Bm, Cm, hp, y, &omaps))
     return SSD_ERR_CUDA;
   const Dims d = make_dims(*shape);
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);

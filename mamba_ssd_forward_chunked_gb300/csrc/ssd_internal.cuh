@@ -23,7 +23,7 @@ struct Work {
   int* status;
   float* cumsum;               // [B][H][Lp]
   float* dt_t;                 // [B][H][Lp]
-  float* states;               // [B][nc][H][P][N]
+  void* states;                // [B][nc][H][P][N], fp32 (fp32 inputs) or bf16 (bf16 inputs)
   __nv_bfloat16* states_bf16;  // [B][nc][H][P][N] or null (fp32 problems)
 };
 
@@ -31,6 +31,7 @@ struct Work {
 struct ChunkStateMaps {
   CUtensorMap x;   // x viewed as [B][L][H*P], box {128 B of (h,p), 32 tokens, 1}
   CUtensorMap bm;  // Bm [B][L][G][N], box {128 B of n, 1, 32 tokens, 1}
+  CUtensorMap s;   // chunk states [(B*nc*H*P)][N], box {128 B of n, 128 rows} (TMA stores)
 };
 struct ComputeOutMaps {
   CUtensorMap cm;  // Cm [B][L][G][N], box {128 B of n, 1, 128 tokens, 1}

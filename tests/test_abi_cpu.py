@@ -72,7 +72,8 @@ def test_workspace_layout(ext):
             Lp = nc * 256
             assert all(v % 1024 == 0 for v in lay.values())
             assert lay["dt_t"] - lay["cumsum"] >= 2 * 32 * Lp * 4
-            assert lay["states_bf16"] - lay["states"] >= 2 * nc * 32 * 64 * 128 * 4
+            es = 2 if dt == ext.SSD_BF16 else 4
+            assert lay["states_bf16"] - lay["states"] >= 2 * nc * 32 * 64 * 128 * es
             extra = 2 * nc * 32 * 64 * 128 * 2 if dt == ext.SSD_BF16 else 0
             assert lay["total"] >= lay["states_bf16"] + extra
             assert ext.ssd_fwd_workspace_size(s) == lay["total"]

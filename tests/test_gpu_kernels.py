@@ -56,7 +56,7 @@ def test_each_kernel_against_its_step(name, over):
     ssd.ssd_chunk_state(shape, d["x"], d["Bm"], ws)
     torch.cuda.synchronize()
     S_ref = oracle.chunk_state(inp["x"], inp["dt"], inp["Bm"], G_gpu, Q)
-    S_gpu = V["states"].cpu().numpy().astype(np.float64)
+    S_gpu = V["states"].float().cpu().numpy().astype(np.float64)
     assert rel_err(S_gpu, S_ref) <= TOL[w.dtype], rel_err(S_gpu, S_ref)
 
     # step 3: state passing (fp32 elementwise) vs fp64 on the GPU's S
