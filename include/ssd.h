@@ -85,6 +85,11 @@ typedef struct {
  *               entering each chunk (in place)
  *   states_bf16 bf16 [B][nc][H][P][N]  (SSD_BF16 only) state entering each
  *               chunk, rounded to bf16 for the output kernel's tensor cores
+ *   chain       int32 [1 + B*H/2]  one-pass kernel: tile counter, then per
+ *               (batch, head pair) the number of windows whose state is
+ *               published (cleared by chunk_cumsum)
+ *   hslot       fp32 [B][H][P][N]  one-pass kernel: state after the last
+ *               published window (used when final_state is NULL)
  * nc = ceil(seqlen / chunk_size). */
 typedef struct {
   size_t status;
@@ -92,6 +97,8 @@ typedef struct {
   size_t dt_t;
   size_t states;
   size_t states_bf16;
+  size_t chain;
+  size_t hslot;
   size_t total;
 } ssd_workspace_layout;
 
@@ -108,21 +115,40 @@ ssd_status ssd_fwd_workspace_layout(const ssd_shape* shape, ssd_workspace_layout
  * invalid or unsupported). */
 size_t ssd_fwd_workspace_size(const ssd_shape* shape);
 
-/* The whole forward pass: chunk_cumsum, chunk_state, state_passing and
- * compute_out, enqueued in that order on `stream`.  init_state may be NULL
- * (zero initial state); final_state may be NULL (not written).  The workspace
- * must hold ssd_fwd_workspace_size(shape) bytes. */
+/* The whole forward pass, enqueued on `stream`.  Two schedules give the
+ * recurrence's result (see the steps below for the formulas):
+ *  - one-pass (ssd_fwd_fused): chunk_cumsum, then one persistent kernel that
+ *    computes each window's state on the tensor core, chains the states
+ *    between windows through the workspace (or final_state), and writes y;
+ *    x, Bm and Cm are read once.  SSD_BF16 only.
+ *  - staged: chunk_cumsum, chunk_state, state_passing and compute_out.
+ * ssd_fwd takes the one-pass schedule for SSD_BF16 when dstate <= 128 and
+ * there are at least as many (batch, head pair) sequences as multiprocessors
+ * (below that the chain of windows, not bandwidth, bounds the one-pass kernel);
+ * otherwise the staged one.  init_state may be NULL (zero initial state); final_state
+ * may be NULL (not written; the workspace holds the running state instead).
+ * When given, final_state is also the running state's storage during the
+ * call, so it must not overlap the inputs (it may equal init_state).  The
+ * workspace must hold ssd_fwd_workspace_size(shape) bytes. */
 ssd_status ssd_fwd(const ssd_shape* shape, const void* x, const float* dt, const float* A,
                    const void* Bm, const void* Cm, const float* D, const float* init_state, void* y,
                    float* final_state, void* workspace, size_t workspace_bytes, ssd_stream_t stream);
+
+/* ssd_fwd forced onto the one-pass schedule (same arguments and contract).
+ * SSD_ERR_UNSUPPORTED unless shape->dtype is SSD_BF16. */
+ssd_status ssd_fwd_fused(const ssd_shape* shape, const void* x, const float* dt, const float* A,
+                         const void* Bm, const void* Cm, const float* D, const float* init_state, void* y,
+                         float* final_state, void* workspace, size_t workspace_bytes, ssd_stream_t stream);
 
 /* After the caller has synchronised the stream of a call that used
  * `workspace`: SSD_OK, or SSD_ERR_DEVICE_TIMEOUT if a bounded wait inside a
  * kernel ran out (its outputs are then invalid).  Blocking 4-byte read. */
 ssd_status ssd_fwd_check(const void* workspace);
 
-/* --- The four steps, callable one by one (ssd_fwd is exactly these four
- * calls in order).  Each reads and writes the workspace regions named. ---- */
+/* --- The four steps, callable one by one (for SSD_F32, ssd_fwd is exactly
+ * these four calls in order; for SSD_BF16 the four calls in order give the
+ * same result as ssd_fwd through the staged path).  Each reads and writes the
+ * workspace regions named. ---- */
 
 /* Step 1 (page 1, chunk_cumsum): cumsum[b][h][cQ+i] = sum_{k<=i} dt*A over the
  * chunk, dt_t = dt transposed; tokens past seqlen contribute 0.  Also clears

@@ -25,7 +25,8 @@ STATUS = {0: "SSD_OK", 1: "SSD_ERR_INVALID_ARG", 2: "SSD_ERR_UNSUPPORTED", 3: "S
 # Every entry point include/ssd.h declares.
 EXPORTS = ("ssd_status_string", "ssd_validate_shape", "ssd_fwd_workspace_layout", "ssd_fwd_workspace_size",
            "ssd_fwd", "ssd_fwd_check", "ssd_chunk_cumsum", "ssd_chunk_state", "ssd_state_passing",
-           "ssd_compute_out", "ssd_debug_timeout_probe", "ssd_fwd_kernel_count", "ssd_fwd_static_scratch")
+           "ssd_compute_out", "ssd_debug_timeout_probe", "ssd_fwd_kernel_count", "ssd_fwd_static_scratch",
+           "ssd_fwd_fused")
 
 # Size of the library's own workspace array used by ssd_fwd_static_scratch.
 SSD_STATIC_SCRATCH_BYTES = 32 << 20
@@ -44,7 +45,8 @@ class ssd_shape(ctypes.Structure):
 
 class ssd_workspace_layout(ctypes.Structure):
     _fields_ = [("status", ctypes.c_size_t), ("cumsum", ctypes.c_size_t), ("dt_t", ctypes.c_size_t),
-                ("states", ctypes.c_size_t), ("states_bf16", ctypes.c_size_t), ("total", ctypes.c_size_t)]
+                ("states", ctypes.c_size_t), ("states_bf16", ctypes.c_size_t), ("chain", ctypes.c_size_t),
+                ("hslot", ctypes.c_size_t), ("total", ctypes.c_size_t)]
 
 
 class SSDError(RuntimeError):
@@ -73,6 +75,8 @@ def _load() -> ctypes.CDLL:
     lib.ssd_fwd_kernel_count.argtypes = [sp]
     lib.ssd_fwd.restype = c_int
     lib.ssd_fwd.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    lib.ssd_fwd_fused.restype = c_int
+    lib.ssd_fwd_fused.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     lib.ssd_fwd_check.restype = c_int
     lib.ssd_fwd_check.argtypes = [vp]
     lib.ssd_chunk_cumsum.restype = c_int
@@ -177,6 +181,8 @@ def workspace_views(shape: ssd_shape, ws: torch.Tensor) -> Dict[str, torch.Tenso
     }
     if shape.dtype == SSD_BF16:
         out["states_bf16"] = view(L["states_bf16"], B * nc * H * P * N, torch.bfloat16, (B, nc, H, P, N))
+    out["chain"] = view(L["chain"], 1 + B * (H // 2), torch.int32, (1 + B * (H // 2),))
+    out["hslot"] = view(L["hslot"], B * H * P * N, torch.float32, (B, H, P, N))
     return out
 
 
@@ -197,9 +203,13 @@ def ssd_fwd(x: torch.Tensor, dt: torch.Tensor, A: torch.Tensor, Bm: torch.Tensor
             D: torch.Tensor, chunk_size: int, init_state: Optional[torch.Tensor] = None,
             y: Optional[torch.Tensor] = None, final_state: Optional[torch.Tensor] = None,
             workspace: Optional[torch.Tensor] = None, stream=None,
-            want_final_state: bool = True) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
-    """The whole forward pass (C: ssd_fwd).  Returns (y, final_state)."""
+            want_final_state: bool = True, schedule: str = "auto") -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """The whole forward pass.  Returns (y, final_state).  ``schedule``:
+    "auto" (C: ssd_fwd, which picks the schedule from the shape) or "fused"
+    (C: ssd_fwd_fused, the one-pass kernel; bf16 only)."""
     _check_inputs(x, dt, A, Bm, Cm, D)
+    if schedule not in ("auto", "fused"):
+        raise ValueError("schedule must be 'auto' or 'fused'")
     shape = shape_of(x, Bm, chunk_size)
     B, L, H, P = x.shape
     N = Bm.shape[3]
@@ -211,10 +221,10 @@ def ssd_fwd(x: torch.Tensor, dt: torch.Tensor, A: torch.Tensor, Bm: torch.Tensor
         raise SSDError(1, "init_state must be contiguous float32")
     if workspace is None:
         workspace = new_workspace(shape, x.device)
-    code = lib.ssd_fwd(ctypes.byref(shape), _ptr(x), _ptr(dt), _ptr(A), _ptr(Bm), _ptr(Cm), _ptr(D),
-                       _ptr(init_state), _ptr(y), _ptr(final_state), _ptr(workspace), workspace.numel(),
-                       _stream(stream))
-    _check(code, "ssd_fwd")
+    fn = lib.ssd_fwd if schedule == "auto" else lib.ssd_fwd_fused
+    code = fn(ctypes.byref(shape), _ptr(x), _ptr(dt), _ptr(A), _ptr(Bm), _ptr(Cm), _ptr(D),
+              _ptr(init_state), _ptr(y), _ptr(final_state), _ptr(workspace), workspace.numel(), _stream(stream))
+    _check(code, "ssd_fwd" if schedule == "auto" else "ssd_fwd_fused")
     return y, final_state
 
 

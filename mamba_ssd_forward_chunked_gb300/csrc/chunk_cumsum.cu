@@ -25,7 +25,8 @@ constexpr int kThreads = 256;
 __global__ void __launch_bounds__(kThreads) chunk_cumsum_kernel(Dims d, const float* __restrict__ dt,
                                                                  const float* __restrict__ A,
                                                                  float* __restrict__ cumsum,
-                                                                 float* __restrict__ dt_t, int* status) {
+                                                                 float* __restrict__ dt_t, int* status,
+                                                                 int* chain, int nchain) {
   __shared__ float s_dt[kHeadsPerBlock * 257];
   __shared__ float s_g[kHeadsPerBlock * 257];
   const int Q = d.Q;
@@ -33,7 +34,10 @@ __global__ void __launch_bounds__(kThreads) chunk_cumsum_kernel(Dims d, const fl
   const int c = blockIdx.x;
   const int h0 = blockIdx.y * kHeadsPerBlock;
   const int b = blockIdx.z;
-  if (c == 0 && blockIdx.y == 0 && b == 0 && threadIdx.x == 0) *status = 0;
+  if (c == 0 && blockIdx.y == 0 && b == 0) {
+    if (threadIdx.x == 0) *status = 0;
+    for (int k = threadIdx.x; k < nchain; k += kThreads) chain[k] = 0;  // one-pass kernel's counter and flags
+  }
 
   // all of the block's loads first (Q * 8 / 256 <= 8 per thread), then the stores to shared memory
   float v[8];
@@ -92,7 +96,8 @@ __global__ void __launch_bounds__(kThreads) chunk_cumsum_kernel(Dims d, const fl
 cudaError_t launch_chunk_cumsum(const Dims& d, const float* dt, const float* A, const Work& w,
                                 cudaStream_t stream) {
   const dim3 grid(d.nc, (d.H + kHeadsPerBlock - 1) / kHeadsPerBlock, d.B);
-  chunk_cumsum_kernel<<<grid, kThreads, 0, stream>>>(d, dt, A, w.cumsum, w.dt_t, w.status);
+  chunk_cumsum_kernel<<<grid, kThreads, 0, stream>>>(d, dt, A, w.cumsum, w.dt_t, w.status, w.counter,
+                                                     1 + d.B * (d.H / 2));
   return cudaGetLastError();
 }
 

@@ -96,6 +96,10 @@ ssd_status layout_of(const ssd_shape* shape, ssd_workspace_layout* out) {
   off = align_up(off + nstate * (s.dtype == SSD_BF16 ? sizeof(__nv_bfloat16) : sizeof(float)));
   L.states_bf16 = off;
   if (s.dtype == SSD_BF16) off = align_up(off + nstate * sizeof(__nv_bfloat16));
+  L.chain = off;
+  off = align_up(off + (1 + heads / 2) * sizeof(int));
+  L.hslot = off;
+  off = align_up(off + heads * s.headdim * s.dstate * sizeof(float));
   L.total = off;
   *out = L;
   return SSD_OK;
@@ -109,6 +113,9 @@ Work carve(void* ws, const ssd_workspace_layout& L, bool bf16) {
   w.dt_t = reinterpret_cast<float*>(p + L.dt_t);
   w.states = p + L.states;
   w.states_bf16 = bf16 ? reinterpret_cast<__nv_bfloat16*>(p + L.states_bf16) : nullptr;
+  w.counter = reinterpret_cast<int*>(p + L.chain);
+  w.flags = w.counter + 1;
+  w.hslot = reinterpret_cast<float*>(p + L.hslot);
   return w;
 }
 
@@ -187,6 +194,49 @@ bool build_out_maps(const ssd_shape& s, const void* x, const void* Bm, const voi
   return true;
 }
 
+// Multiprocessors of the current device (cached per device).
+int sm_count() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess) cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+// The one-pass schedule pays a chain of windows per (batch, head pair); it wins
+// once there are enough sequences to fill the multiprocessors.
+bool use_fused(const ssd_shape& s) {
+  if (s.dtype != SSD_BF16 || s.dstate > 128) return false;
+  return s.batch * (s.nheads / 2) >= sm_count();
+}
+
+ssd_status fwd_impl(int path, const ssd_shape* shape, const void* x, const float* dt, const float* A, const void* Bm,
+                    const void* Cm, const float* D, const float* init_state, void* y, float* final_state,
+                    void* workspace, size_t workspace_bytes, ssd_stream_t stream);
+
+bool build_fused_maps(const ssd_shape& s, const void* x, const void* Bm, const void* Cm, const void* y,
+                      FusedMaps* m) {
+  const uint32_t S = static_cast<uint32_t>(s.chunk_size < 128 ? s.chunk_size : 128);
+  const uint64_t es = 2;
+  const uint64_t gn = static_cast<uint64_t>(s.ngroups) * s.dstate;
+  const uint64_t dims4[4] = {static_cast<uint64_t>(s.dstate), static_cast<uint64_t>(s.ngroups),
+                             static_cast<uint64_t>(s.seqlen), static_cast<uint64_t>(s.batch)};
+  const uint64_t str4[3] = {s.dstate * es, gn * es, gn * es * s.seqlen};
+  const uint32_t box4[4] = {64, 1, S, 1};
+  if (!encode(&m->cm, true, 4, Cm, dims4, str4, box4)) return false;
+  if (!encode(&m->bm, true, 4, Bm, dims4, str4, box4)) return false;
+  const uint64_t hp = static_cast<uint64_t>(s.nheads) * s.headdim;
+  const uint64_t dims[3] = {hp, static_cast<uint64_t>(s.seqlen), static_cast<uint64_t>(s.batch)};
+  const uint64_t str[2] = {hp * es, hp * es * s.seqlen};
+  const uint32_t box[3] = {64, S, 1};
+  if (!encode(&m->x, true, 3, x, dims, str, box)) return false;
+  if (!encode(&m->y, true, 3, y, dims, str, box)) return false;
+  return true;
+}
+
 }  // namespace
 }  // namespace ssd
 
@@ -236,7 +286,7 @@ size_t ssd_fwd_workspace_size(const ssd_shape* shape) {
 
 int ssd_fwd_kernel_count(const ssd_shape* shape) {
   if (ssd_validate_shape(shape) != SSD_OK || empty_problem(*shape)) return 0;
-  return 4;
+  return use_fused(*shape) ? 2 : 4;
 }
 
 ssd_status ssd_chunk_cumsum(const ssd_shape* shape, const float* dt, const float* A, void* workspace,
@@ -306,6 +356,26 @@ ssd_status ssd_compute_out(const ssd_shape* shape, const void* x, const void* Bm
 ssd_status ssd_fwd(const ssd_shape* shape, const void* x, const float* dt, const float* A, const void* Bm,
                    const void* Cm, const float* D, const float* init_state, void* y, float* final_state,
                    void* workspace, size_t workspace_bytes, ssd_stream_t stream) {
+  const int path = shape && ssd_validate_shape(shape) == SSD_OK && use_fused(*shape) ? 1 : 0;
+  return fwd_impl(path, shape, x, dt, A, Bm, Cm, D, init_state, y, final_state, workspace, workspace_bytes, stream);
+}
+
+ssd_status ssd_fwd_fused(const ssd_shape* shape, const void* x, const float* dt, const float* A, const void* Bm,
+                         const void* Cm, const float* D, const float* init_state, void* y, float* final_state,
+                         void* workspace, size_t workspace_bytes, ssd_stream_t stream) {
+  if (shape && ssd_validate_shape(shape) == SSD_OK && shape->dtype != SSD_BF16) return SSD_ERR_UNSUPPORTED;
+  return fwd_impl(1, shape, x, dt, A, Bm, Cm, D, init_state, y, final_state, workspace, workspace_bytes, stream);
+}
+
+}  // extern "C"
+
+namespace ssd {
+namespace {
+
+// path: 0 staged, 1 one-pass
+ssd_status fwd_impl(int path, const ssd_shape* shape, const void* x, const float* dt, const float* A, const void* Bm,
+                    const void* Cm, const float* D, const float* init_state, void* y, float* final_state,
+                    void* workspace, size_t workspace_bytes, ssd_stream_t stream) {
   ssd_workspace_layout L;
   ssd_status st = check_workspace(shape, workspace, workspace_bytes, &L);
   if (st != SSD_OK) return st;
@@ -321,6 +391,16 @@ ssd_status ssd_fwd(const ssd_shape* shape, const void* x, const float* dt, const
   // build every tensor map before the first launch, so an encoding failure enqueues nothing
   const bool bf16 = shape->dtype == SSD_BF16;
   Work w = carve(workspace, L, bf16);
+  if (path == 1) {
+    FusedMaps fmaps;
+    if (!build_fused_maps(*shape, x, Bm, Cm, y, &fmaps)) return SSD_ERR_CUDA;
+    const Dims d = make_dims(*shape);
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = launch_chunk_cumsum(d, dt, A, w, cs);
+    if (e == cudaSuccess)
+      e = launch_fused(d, fmaps, D, x, init_state, final_state ? final_state : w.hslot, w, spin_limit_ns(), cs);
+    return from_cuda(e);
+  }
   ChunkStateMaps smaps;
   ComputeOutMaps omaps;
   const void* hp = bf16 ? static_cast<const void*>(w.states_bf16) : static_cast<const void*>(w.states);
@@ -335,6 +415,11 @@ ssd_status ssd_fwd(const ssd_shape* shape, const void* x, const float* dt, const
   if (e == cudaSuccess) e = launch_compute_out(d, bf16, omaps, D, x, y, w, spin, cs);
   return from_cuda(e);
 }
+
+}  // namespace
+}  // namespace ssd
+
+extern "C" {
 
 ssd_status ssd_fwd_check(const void* workspace) {
   if (!workspace) return SSD_ERR_INVALID_ARG;

@@ -1,0 +1,791 @@
+// One-pass SSD forward: chunk state, state passing and output in one
+// persistent kernel (bf16 inputs, fp32 accumulate).
+//
+// What it computes ("Jane Street ML Engineers Map Mamba-2 Recurrent State
+// Computation to Tensor Cores with cuTile", jump-formula, three-kernel and
+// compute_out paragraphs): for each window of S = min(Q, 128) tokens of one
+// (batch, head), with h_in the state entering the window,
+//
+//     y_i   = sum_{j<=i} (c_i . b_j) e^{G_i - G_j} dt_j x_j + e^{G_i} h_in c_i + D x_i
+//     h_out = e^{G_S} h_in + sum_j e^{G_S - G_j} dt_j x_j b_j^T
+//
+// with G the cumsum of dt*A from the window start (the kernel reads it, in
+// log2 units, from the chunk_cumsum output).  Windows never straddle a chunk,
+// and the recurrence gives the same result for any split into windows.
+//
+// Rescaling against one reference token.  Pick m = S/2 - 1 and write
+// e^{G_i - G_j} = e^{G_i - G_m} e^{G_m - G_j}.  With X^_j = e^{G_m - G_j} dt_j x_j,
+// r_i = e^{G_i - G_m} and O = e^{G_m} h_in:
+//
+//     y_i   = r_i [ sum_{j<=i} (c_i . b_j) X^_j + O c_i ] + D x_i
+//     h_out = e^{G_S - G_m} (X^^T B) + e^{G_S} h_in
+//
+// so the masked interaction operand is the causal select of C B^T alone (no
+// exponential per element, the same for both heads of a pair), the decay
+// lives in a per-token scale of X and a per-row scale of the output, and the
+// carried-state term shares the intra accumulator.  This is exact, and it
+// stays inside fp32 range while |G_m| and |G_S - G_m| are at most 100 (log2):
+// every factor is then within 2^+-100.  A window that exceeds that on either
+// head of the pair takes an exact fallback: X^ uses the window end as
+// reference (factors <= 1), the intra sum is done on CUDA cores from
+// C B^T with per-element exponentials, and the output scale is e^{G_i}.
+//
+// Chaining windows: the window state is computed on the tensor core from this
+// window alone; h_in comes from the previous window of the same (batch, head
+// pair) through global memory (one fp32 [P][N] slot per head, L2-resident)
+// and a per-pair flag holding the number of windows published.  Tiles are
+// claimed from a global counter in window-major order, so every tile's
+// predecessor was claimed earlier by a running CTA and is finished or in
+// progress: the look-back wait always ends.  Each tile does its state and
+// masking MMAs before it waits, so the wait overlaps the tensor core.
+//
+// GB300 mapping, per CTA (one per SM, 320 threads, persistent):
+// Runs: a claim is a run of up to R consecutive windows of one (batch, head
+// pair), processed in order by one CTA.  Inside a run the running state stays
+// in tensor memory; only the run's first window reads the predecessor's state
+// (after its flag) and only its last window writes the state and the flag.
+// R = 4 for dstate <= 128 and 1 for dstate = 256 (no tensor memory to spare).
+//
+// GB300 mapping, per CTA (one per SM, 384 threads, persistent):
+//   warp 10   claims runs from the counter and expands them into windows with
+//             their per-head scalars, in an 8-deep window ring.
+//   warp 0    issues TMA: the head pair's X window (double buffered) and a
+//             ring of 32 KB stages, each 128 dstate columns of C or B.  For
+//             dstate <= 128 the C stage stays resident until the
+//             carried-state product; for 256 C is loaded a second time.
+//   warp 1    owns tensor memory and issues every tcgen05.mma from one thread.
+//   warps 2-9 two warpgroups.  Per window: turn C B^T into the packed causal
+//             bf16 operand (in place, TMEM A side); advance the state and
+//             write the carried-state operand O; scale the NEXT window's X;
+//             write y over x in the X buffer.  Scaling one window ahead lets
+//             the tensor core run the next window's C B^T and state products
+//             while this window's epilogue runs.
+//   warp 11   stores y with TMA and hands the X buffer back to warp 0.
+// The window state is accumulated transposed (TMEM lane = dstate index n,
+// columns = (head, p)), so a warp's loads and stores of the fp32 state are
+// 128-byte rows of consecutive n.  Tensor memory: C B^T [0, 128), output pair
+// accumulator [128, 256), window state [256, 384) (to 512 for dstate 256),
+// running state of the run [384, 512).  Every wait is bounded; on expiry the
+// CTA records SSD_ERR_DEVICE_TIMEOUT and winds down.
+#include "ptx.cuh"
+#include "ssd_internal.cuh"
+
+namespace ssd {
+namespace {
+
+constexpr int kThreads = 384;
+constexpr int kTileRing = 8;
+constexpr float kSpan = 100.f;  // log2 bound on either side of the reference token
+constexpr uint32_t kColCB = 0, kColY = 128, kColD = 256, kColH = 384, kTmemCols = 512;
+constexpr uint32_t kStageBytes = 32768, kAtomBytes = 16384, kXBytes = 32768;
+
+// One window, as the scheduler publishes it through the window ring.
+struct TileInfo {
+  int tile;         // window id (window, batch, head pair); -1: no more windows
+  int fast;         // rescaled form valid for both heads
+  int first, last;  // first / last window of its run
+  float base[2];    // cumsum just before the window (natural log), per head
+  float gm[2];      // log2 cumsum at the reference token, relative to the window start
+  float ge[2];      // log2 cumsum at the window end, relative to the window start
+};
+
+struct FusedSmem {
+  uint32_t ring, xbuf, obuf, info, coord, bars, holder, total;
+  int stages;
+};
+
+__host__ __device__ inline FusedSmem fused_smem_layout(int N) {
+  FusedSmem s{};
+  s.stages = N >= 256 ? 3 : 4;
+  s.ring = 0;
+  s.xbuf = s.ring + s.stages * kStageBytes;
+  s.obuf = s.xbuf + 2 * kXBytes;
+  s.info = s.obuf + (N / 64) * kAtomBytes;
+  s.coord = s.info + kTileRing * sizeof(TileInfo);
+  s.bars = s.coord + 32;
+  s.holder = s.bars + 48 * 8;
+  s.total = s.holder + 16;
+  return s;
+}
+
+struct Win {
+  int w, b, pair, h0, g, t0;
+};
+
+__device__ __forceinline__ Win decode(int tile, const Dims& d, int S) {
+  const int hp = d.H / 2;
+  Win W;
+  W.pair = tile % hp;
+  const int rest = tile / hp;
+  W.b = rest % d.B;
+  W.w = rest / d.B;
+  W.h0 = 2 * W.pair;
+  W.g = W.h0 / (d.H / d.G);
+  W.t0 = W.w * S;
+  return W;
+}
+
+// Causal select of one 32-column strip of C B^T (row i, columns j0..j0+31),
+// packed to bf16 pairs and stored at `dst` (16 columns).
+__device__ __forceinline__ void causal_pack_store(uint32_t (&v)[32], int j0, int i, uint32_t dst) {
+  uint32_t o[16];
+#pragma unroll
+  for (int q = 0; q < 16; ++q) {
+    const float lo = (j0 + 2 * q <= i) ? __uint_as_float(v[2 * q]) : 0.f;
+    const float hi = (j0 + 2 * q + 1 <= i) ? __uint_as_float(v[2 * q + 1]) : 0.f;
+    o[q] = pack_bf16x2(lo, hi);
+  }
+  tmem_st16(dst, o);
+}
+
+__device__ __forceinline__ uint32_t scale_bf16x2(uint32_t v, float s) {
+  return pack_bf16x2(bf16_lo(v) * s, bf16_hi(v) * s);
+}
+
+// A warpgroup thread's view of one window: the scalars of its warpgroup's
+// head and its token row's cumsum and dt (loaded one window ahead).
+struct TileCtx {
+  int tile, fast, first, last;
+  float base, gm, ge;  // as in TileInfo, for this warpgroup's head
+  float graw, dt;      // cumsum (natural log, chunk-relative) and dt at token row r
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+    ssd_fused_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap cmap,
+                     const __grid_constant__ CUtensorMap bmap, const __grid_constant__ CUtensorMap ymap, Dims d,
+                     int R, const float* __restrict__ cumsum, const float* __restrict__ dt_t,
+                     const float* __restrict__ Dvec, const float* init, float* hslot, int* flags, int* counter,
+                     const __nv_bfloat16* __restrict__ xg, int* status, uint64_t spin_ns) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const FusedSmem L = fused_smem_layout(d.N);
+  const int S = d.Q < 128 ? d.Q : 128;
+  const int NH = (d.N + 127) / 128;             // 128-column halves of dstate
+  const int NA = (d.N < 128 ? d.N : 128) / 64;  // 64-column atoms per half
+  const bool holdC = NH == 1;                   // C stage kept for the carried-state product
+  const int hp = d.H / 2;
+  const int nw = d.Lp / S;
+  const int nruns = ((nw + R - 1) / R) * d.B * hp;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
+  uint64_t* full = bars;        // [4] stage ring
+  uint64_t* empty = bars + 4;   // [4]
+  uint64_t* xfull = bars + 8;   // [2] X window landed
+  uint64_t* xready = bars + 10; // [2] X scaled (256 arrivals)
+  uint64_t* xempty = bars + 12; // [2] y stored from the buffer (store warp)
+  uint64_t* ystaged = bars + 14;// [2] y written into the buffer (one arrival per warpgroup)
+  uint64_t* tfull = bars + 16;  // [8] window ring
+  uint64_t* tempty = bars + 24; // [8] (258 arrivals: TMA, MMA and the warpgroups)
+  uint64_t* cbfull = bars + 32; // C B^T accumulated
+  uint64_t* dfull = bars + 33;  // window state accumulated
+  uint64_t* mready = bars + 34; // causal operand written (256)
+  uint64_t* cbfree = bars + 35; // C B^T columns reusable (256 + MMA commit)
+  uint64_t* dfree = bars + 36;  // window state drained (256)
+  uint64_t* oready = bars + 37; // carried-state operand in shared memory (256)
+  uint64_t* ofree = bars + 38;  // carried-state products done
+  uint64_t* yfull = bars + 39;  // all products of the window done
+  uint64_t* yfree = bars + 40;  // output accumulator drained (256)
+  TileInfo* info = reinterpret_cast<TileInfo*>(smem + L.info);
+  int* coord = reinterpret_cast<int*>(smem + L.coord);  // [2][3]: batch, t0, h0 of the y in each buffer
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L.holder);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < 4; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int s = 0; s < kTileRing; ++s) {
+      mbar_init(&tfull[s], 1);
+      mbar_init(&tempty[s], 258);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&xfull[s], 1);
+      mbar_init(&xready[s], 256);
+      mbar_init(&xempty[s], 1);
+      mbar_init(&ystaged[s], 2);
+    }
+    mbar_init(cbfull, 1);
+    mbar_init(dfull, 1);
+    mbar_init(mready, 256);
+    mbar_init(cbfree, 257);
+    mbar_init(dfree, 256);
+    mbar_init(oready, 256);
+    mbar_init(ofree, 1);
+    mbar_init(yfull, 1);
+    mbar_init(yfree, 256);
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&xmap);
+    tma_prefetch_desc(&cmap);
+    tma_prefetch_desc(&bmap);
+    tma_prefetch_desc(&ymap);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_holder, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  bool ok = true;
+
+  if (warp == 10) {
+    // ------------------------------------------------------------ run scheduler
+    // lane 0 claims a run; lanes 0 and 1 read the two heads' window scalars
+    int n = 0;  // window ring position
+    for (bool more = true; more && ok;) {
+      int run = 0;
+      if (lane == 0) run = atomicAdd(counter, 1);
+      run = __shfl_sync(0xffffffffu, run, 0);
+      int w0 = 0, w1 = 1, b = 0, pair = 0;
+      if (run < nruns) {
+        pair = run % hp;
+        b = (run / hp) % d.B;
+        w0 = (run / hp / d.B) * R;
+        w1 = w0 + R < nw ? w0 + R : nw;
+      } else {
+        more = false;  // publish one end marker
+      }
+      for (int w = w0; w < w1 && ok; ++w, ++n) {
+        const int tile = more ? (w * d.B + b) * hp + pair : -1;
+        float base = 0.f, gm = 0.f, ge = 0.f;
+        if (more && lane < 2) {
+          const float* row = cumsum + (static_cast<int64_t>(b) * d.H + 2 * pair + lane) * d.Lp;
+          const int t0 = w * S;
+          base = (t0 % d.Q) != 0 ? row[t0 - 1] : 0.f;
+          gm = row[t0 + S / 2 - 1];
+          ge = row[t0 + S - 1];
+        }
+        const float base1 = __shfl_sync(0xffffffffu, base, 1), gm1 = __shfl_sync(0xffffffffu, gm, 1),
+                    ge1 = __shfl_sync(0xffffffffu, ge, 1);
+        const int ts = n % kTileRing;
+        if (lane == 0) {
+          TileInfo ti;
+          ti.tile = tile;
+          ti.fast = 1;
+          ti.first = w == w0;
+          ti.last = w == w1 - 1;
+          const float bs[2] = {base, base1}, ms[2] = {gm, gm1}, es[2] = {ge, ge1};
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            ti.base[hh] = bs[hh];
+            ti.gm[hh] = (ms[hh] - bs[hh]) * kLog2e;
+            ti.ge[hh] = (es[hh] - bs[hh]) * kLog2e;
+            // G is non-increasing, so these two spans bound every exponent of the rescaled form
+            if (!(-ti.gm[hh] <= kSpan && ti.gm[hh] - ti.ge[hh] <= kSpan)) ti.fast = 0;
+          }
+          if (n >= kTileRing && !mbar_wait(&tempty[ts], ((n / kTileRing) - 1) & 1, spin_ns)) ok = false;
+          if (ok) {
+            info[ts] = ti;
+            mbar_arrive(&tfull[ts]);
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      }
+    }
+  } else if (warp == 11) {
+    // ------------------------------------------------------------ y stores
+    if (lane == 0) {
+      for (int n = 0; ok; ++n) {
+        const int buf = n & 1;
+        if (!mbar_wait(&ystaged[buf], (n >> 1) & 1, spin_ns)) {
+          ok = false;
+          break;
+        }
+        const int b = coord[3 * buf], t0 = coord[3 * buf + 1], h0 = coord[3 * buf + 2];
+        if (b < 0) break;
+        uint8_t* xb = smem + L.xbuf + buf * kXBytes;
+        tma_store_3d(&ymap, xb, h0 * d.P, t0, b);
+        tma_store_3d(&ymap, xb + S * 128, (h0 + 1) * d.P, t0, b);
+        tma_store_commit();
+        tma_store_wait_read();
+        mbar_arrive(&xempty[buf]);
+      }
+      tma_store_wait_all();
+    }
+  } else if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int it = 0;
+      for (int n = 0; ok; ++n) {
+        const int ts = n % kTileRing;
+        if (!mbar_wait(&tfull[ts], (n / kTileRing) & 1, spin_ns)) {
+          ok = false;
+          break;
+        }
+        const int tile = info[ts].tile;
+        mbar_arrive(&tempty[ts]);
+        if (tile < 0) break;
+        const Win W = decode(tile, d, S);
+        const int buf = n & 1;
+        if (n >= 2 && !mbar_wait(&xempty[buf], ((n >> 1) - 1) & 1, spin_ns)) {
+          ok = false;
+          break;
+        }
+        uint8_t* xb = smem + L.xbuf + buf * kXBytes;
+        mbar_arrive_expect_tx(&xfull[buf], 2u * S * 128u);
+        tma_load_3d(xb, &xmap, &xfull[buf], W.h0 * d.P, W.t0, W.b);
+        tma_load_3d(xb + S * 128, &xmap, &xfull[buf], (W.h0 + 1) * d.P, W.t0, W.b);
+        // stages: C_0, B_0 (, C_1, B_1) for C B^T and the state, then (dstate 256) C_0, C_1 again
+        const int nq = holdC ? 2 * NH : 3 * NH;
+        for (int q = 0; q < nq && ok; ++q, ++it) {
+          const int s = it % L.stages, r = it / L.stages;
+          if (r > 0 && !mbar_wait(&empty[s], (r - 1) & 1, spin_ns)) {
+            ok = false;
+            break;
+          }
+          uint8_t* st = smem + L.ring + s * kStageBytes;
+          const bool isB = q < 2 * NH && (q & 1);
+          const int hf = q < 2 * NH ? (q >> 1) : q - 2 * NH;
+          const CUtensorMap* map = isB ? &bmap : &cmap;
+          mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(NA) * S * 128u);
+          for (int a = 0; a < NA; ++a)
+            tma_load_4d(st + a * kAtomBytes, map, &full[s], hf * 128 + a * 64, W.g, W.t0, W.b);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t id_cb = idesc_f32acc(1, 128, static_cast<uint32_t>(S), 0, 0);  // C B^T: both K-major
+      const uint32_t id_st = idesc_f32acc(1, 128, 128, 1, 1);  // state^T: B^T (MN-major) x X^ pair (MN-major)
+      const uint32_t id_in = idesc_f32acc(1, 128, 128, 0, 1);  // intra: causal operand (TMEM) x X^ pair
+      const uint32_t id_yo = idesc_f32acc(1, 128, 128, 0, 0);  // carried state: C x O (both K-major)
+      const uint32_t xlbo = static_cast<uint32_t>(S) * 128u;   // head stride in the X buffer
+      const uint32_t ob = smem_u32(smem + L.obuf);
+      int it = 0;
+      auto wait_stage = [&](int i) -> uint32_t {
+        const int s = i % L.stages;
+        if (!mbar_wait(&full[s], (i / L.stages) & 1, spin_ns)) return 0u;
+        return smem_u32(smem + L.ring + s * kStageBytes);
+      };
+      for (int n = 0; ok; ++n) {
+        const int ts = n % kTileRing;
+        if (!mbar_wait(&tfull[ts], (n / kTileRing) & 1, spin_ns)) {
+          ok = false;
+          break;
+        }
+        const int tile = info[ts].tile;
+        const bool fast = info[ts].fast != 0;
+        mbar_arrive(&tempty[ts]);
+        if (tile < 0) break;
+        const int buf = n & 1;
+        const uint32_t xb = smem_u32(smem + L.xbuf + buf * kXBytes);
+        if (!mbar_wait(&xready[buf], (n >> 1) & 1, spin_ns) ||
+            (n > 0 && (!mbar_wait(cbfree, (n - 1) & 1, spin_ns) || !mbar_wait(dfree, (n - 1) & 1, spin_ns)))) {
+          ok = false;
+          break;
+        }
+        // pass 1, per 128-column half of dstate: C B^T (K = n) and the transposed state (K = tokens)
+        uint32_t held = 0;  // the resident C stage (holdC)
+        int held_it = 0;
+        for (int hf = 0; hf < NH; ++hf, it += 2) {
+          const uint32_t sc = wait_stage(it), sb = wait_stage(it + 1);
+          if (!sc || !sb) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          for (int k = 0; k < 4 * NA; ++k)
+            mma_ss<false>(tmem + kColCB, sdesc_sw128(sc + (k >> 2) * kAtomBytes + (k & 3) * 32, 16, 1024),
+                          sdesc_sw128(sb + (k >> 2) * kAtomBytes + (k & 3) * 32, 16, 1024), id_cb,
+                          (hf | k) != 0 ? 1u : 0u);
+          for (int k = 0; k < S / 16; ++k)
+            mma_ss<false>(tmem + kColD + 128 * hf, sdesc_sw128(sb + k * 2048, kAtomBytes, 1024),
+                          sdesc_sw128(xb + k * 2048, xlbo, 1024), id_st, k != 0 ? 1u : 0u);
+          if (holdC) {
+            held = sc;
+            held_it = it;
+          } else {
+            mma_commit(&empty[it % L.stages]);
+          }
+          mma_commit(&empty[(it + 1) % L.stages]);
+        }
+        if (!ok) break;
+        mma_commit(cbfull);
+        mma_commit(dfull);
+        // intra products once the causal operand is in place and the accumulator is free
+        if (!mbar_wait(mready, n & 1, spin_ns) || (n > 0 && !mbar_wait(yfree, (n - 1) & 1, spin_ns))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (fast) {
+          for (int k = 0; k < S / 16; ++k)
+            mma_ts<false>(tmem + kColY, tmem + kColCB + k * 8, sdesc_sw128(xb + k * 2048, xlbo, 1024), id_in,
+                          k != 0 ? 1u : 0u);
+        }
+        mma_commit(cbfree);
+        // pass 2: carried-state products, once O is in shared memory
+        if (!mbar_wait(oready, n & 1, spin_ns)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        for (int hf = 0; hf < NH; ++hf) {
+          uint32_t sc = held;
+          if (!holdC) {
+            sc = wait_stage(it);
+            if (!sc) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+          }
+          for (int k = 0; k < 4 * NA; ++k)
+            mma_ss<false>(tmem + kColY, sdesc_sw128(sc + (k >> 2) * kAtomBytes + (k & 3) * 32, 16, 1024),
+                          sdesc_sw128(ob + (2 * hf + (k >> 2)) * kAtomBytes + (k & 3) * 32, 16, 1024), id_yo,
+                          (fast || (hf | k) != 0) ? 1u : 0u);
+          if (holdC) {
+            mma_commit(&empty[held_it % L.stages]);
+          } else {
+            mma_commit(&empty[it % L.stages]);
+            ++it;
+          }
+        }
+        if (!ok) break;
+        mma_commit(yfull);
+        mma_commit(ofree);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ two warpgroups
+    const int wg = (warp - 2) >> 2;  // head of the pair for the per-head passes
+    const int et = threadIdx.x - 64 - 128 * wg;
+    const int quad = warp & 3;
+    const int r = quad * 32 + lane;  // TMEM lane: token row (output, C B^T) or dstate index (state)
+    const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+    const uint32_t bar_wg = 1 + wg, bar_all = 3;
+    const int rr = r < S ? r : S - 1;
+
+    // next window from the ring; issues this thread's per-token loads.  False at the end.
+    auto fetch = [&](int n, TileCtx& c) -> bool {
+      const int ts = n % kTileRing;
+      if (!mbar_wait(&tfull[ts], (n / kTileRing) & 1, spin_ns)) {
+        ok = false;
+        return false;
+      }
+      c.tile = info[ts].tile;
+      c.fast = info[ts].fast;
+      c.first = info[ts].first;
+      c.last = info[ts].last;
+      c.base = info[ts].base[wg];
+      c.gm = info[ts].gm[wg];
+      c.ge = info[ts].ge[wg];
+      mbar_arrive(&tempty[ts]);
+      if (c.tile < 0) return false;
+      const Win W = decode(c.tile, d, S);
+      const int64_t o = (static_cast<int64_t>(W.b) * d.H + W.h0 + wg) * d.Lp + W.t0 + rr;
+      c.graw = cumsum[o];
+      c.dt = r < S ? dt_t[o] : 0.f;
+      return true;
+    };
+    // X^ = wfac * x for this warpgroup's head, in place (a 128-B row is one token)
+    auto scale = [&](int n, const TileCtx& c) -> bool {
+      const int buf = n & 1;
+      if (!mbar_wait(&xfull[buf], (n >> 1) & 1, spin_ns)) return false;
+      if (r < S) {
+        const float gi = (c.graw - c.base) * kLog2e;
+        const float wfac = fast_exp2((c.fast ? c.gm : c.ge) - gi) * c.dt;
+        uint4* row = reinterpret_cast<uint4*>(smem + L.xbuf + buf * kXBytes + wg * S * 128 + r * 128);
+        // step k touches 16-byte chunk k ^ (r & 7): the warp's 32 rows then spread over all banks
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          uint4* cp = row + (k ^ (r & 7));
+          uint4 v = *cp;
+          v.x = scale_bf16x2(v.x, wfac);
+          v.y = scale_bf16x2(v.y, wfac);
+          v.z = scale_bf16x2(v.z, wfac);
+          v.w = scale_bf16x2(v.w, wfac);
+          *cp = v;
+        }
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(&xready[buf]);
+      return true;
+    };
+
+    TileCtx cur;
+    int n = 0;
+    if (fetch(0, cur) && !scale(0, cur)) ok = false;
+    for (; ok && cur.tile >= 0; ++n) {
+      const Win W = decode(cur.tile, d, S);
+      const bool fast = cur.fast != 0;
+      const int h = W.h0 + wg;
+      const int buf = n & 1;
+      uint8_t* xb = smem + L.xbuf + buf * kXBytes + wg * S * 128;  // this head's X window
+      // the next window's scalars and per-token loads, in flight during this one
+      TileCtx nxt;
+      nxt.tile = -1;
+      const bool more = fetch(n + 1, nxt);
+      if (!ok) break;
+
+      // 1. causal operand, packed in place over the first S/2 columns of C B^T
+      // (timeouts are decided jointly before every 256-thread barrier, so no thread is left waiting there)
+      if (named_bar_or(bar_all, 256, !mbar_wait(cbfull, n & 1, spin_ns))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      if (fast) {
+        const int nst = S / 64;  // strips of 32 columns per warpgroup
+        const int s0 = wg * nst;
+        uint32_t va[32], vb[32];
+        tmem_ld32(tmem + lane_base + kColCB + 32 * s0, va);
+        if (nst > 1) tmem_ld32(tmem + lane_base + kColCB + 32 * (s0 + 1), vb);
+        tmem_ld_wait();
+        named_bar_sync(bar_all, 256);  // all of C B^T is read before the packed operand overwrites it
+        causal_pack_store(va, 32 * s0, r, tmem + lane_base + kColCB + 16 * s0);
+        if (nst > 1) causal_pack_store(vb, 32 * (s0 + 1), r, tmem + lane_base + kColCB + 16 * (s0 + 1));
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(cbfree);
+      }
+      mbar_arrive(mready);
+
+      // 2. state of this warpgroup's head.  Thread = dstate index n.  h_in is the
+      //    run's running state (tensor memory) or, for a run's first window, the
+      //    predecessor's published state; h_out goes back to tensor memory or, for
+      //    a run's last window, to the global slot and the flag.  O = o * h_in.
+      {
+        const float s_fac = fast ? fast_exp2(cur.ge - cur.gm) : 1.f;
+        const float e_fac = fast_exp2(cur.ge);
+        const float o_fac = fast ? fast_exp2(cur.gm) : 1.f;
+        const int64_t hbase = (static_cast<int64_t>(W.b) * d.H + h) * d.P * d.N;
+        float* hs = hslot + hbase;
+        const bool first = cur.first != 0, last = cur.last != 0;
+        const float* hin = first ? (W.w == 0 ? (init ? init + hbase : nullptr) : hs) : nullptr;
+        // the predecessor run has published its state (one poller, joint decision)
+        bool bad = !mbar_wait(dfull, n & 1, spin_ns) || (n > 0 && !mbar_wait(ofree, (n - 1) & 1, spin_ns));
+        if (first && W.w > 0 && wg == 0 && et == 0)
+          bad = bad || !wait_flag_geq(flags + W.b * hp + W.pair, W.w, spin_ns);
+        if (named_bar_or(bar_all, 256, bad)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        for (int hf = 0; hf < NH; ++hf) {
+          const int nn = 128 * hf + r;
+          if (nn >= d.N) continue;  // warp-uniform (N is a multiple of 64)
+          uint8_t* ocol = smem + L.obuf + (nn >> 6) * kAtomBytes + (nn & 7) * 2;
+          const int cchunk = (nn & 63) >> 3;
+#pragma unroll 1
+          for (int pb = 0; pb < 2; ++pb) {
+            float hv[32];
+            if (first) {  // 32 loads in flight (the chain's critical path is their latency)
+              const float* hp_in = hin ? hin + 32 * pb * d.N + nn : nullptr;
+#pragma unroll
+              for (int q = 0; q < 32; ++q) hv[q] = hp_in ? __ldcg(hp_in + q * d.N) : 0.f;
+            } else {
+              uint32_t hr[32];
+              tmem_ld32(tmem + lane_base + kColH + 64 * wg + 32 * pb, hr);
+              tmem_ld_wait();
+#pragma unroll
+              for (int q = 0; q < 32; ++q) hv[q] = __uint_as_float(hr[q]);
+            }
+#pragma unroll
+            for (int pc = 0; pc < 2; ++pc) {
+              uint32_t dv[16];
+              tmem_ld16(tmem + lane_base + kColD + 128 * hf + 64 * wg + 32 * pb + 16 * pc, dv);
+              tmem_ld_wait();
+              uint32_t hn[16];
+#pragma unroll
+              for (int q = 0; q < 16; ++q) {
+                const int p = 32 * pb + 16 * pc + q;
+                const float hq = hv[16 * pc + q];
+                const float ho = fmaf(s_fac, __uint_as_float(dv[q]), e_fac * hq);
+                hn[q] = __float_as_uint(ho);
+                if (last) __stcg(hs + p * d.N + nn, ho);
+                const int row = 64 * wg + p;
+                *reinterpret_cast<__nv_bfloat16*>(ocol + row * 128 + ((cchunk ^ (row & 7)) << 4)) =
+                    __float2bfloat16_rn(o_fac * hq);
+              }
+              if (!last) tmem_st16(tmem + lane_base + kColH + 64 * wg + 32 * pb + 16 * pc, hn);
+            }
+          }
+        }
+        if (last) {
+          __threadfence();
+          named_bar_sync(bar_all, 256);
+          if (wg == 0 && et == 0) st_release_gpu(flags + W.b * hp + W.pair, W.w + 1);
+        } else {
+          tmem_st_wait();
+        }
+        tc_fence_before();
+        mbar_arrive(dfree);
+        fence_proxy_async_smem();
+        mbar_arrive(oready);
+      }
+
+      // 3. the next window's X (its products then overlap this window's epilogue)
+      if (more && !scale(n + 1, nxt)) {
+        ok = false;
+        break;
+      }
+
+      // 4. y = r_i * acc + D x_i, written over x in the X window; warp 11 stores it
+      if (named_bar_or(bar_wg, 128, !mbar_wait(yfull, n & 1, spin_ns))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const float Dh = Dvec[h];
+      const float gi = (cur.graw - cur.base) * kLog2e;
+      const float dti = cur.dt;
+      const int64_t xrow_g = ((static_cast<int64_t>(W.b) * d.L + W.t0 + r) * d.H + h) * d.P;
+      const bool in_seq = r < S && W.t0 + r < d.L;
+      uint8_t* xr = xb + r * 128;
+      if (fast) {
+        uint32_t ya[32], yb[32];
+        tmem_ld32(tmem + lane_base + kColY + 64 * wg, ya);
+        tmem_ld32(tmem + lane_base + kColY + 64 * wg + 32, yb);
+        tmem_ld_wait();
+        tc_fence_before();
+        mbar_arrive(yfree);
+        if (r < S) {
+          const float ri = fast_exp2(gi - cur.gm);
+          const float wfac = fast_exp2(cur.gm - gi) * dti;
+          // D x_i from X^_i = wfac x_i when wfac is well inside the normal range, else from global x
+          const bool rec = wfac >= 0x1p-80f;
+          const float kx = rec ? Dh / dti : 0.f;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            uint4* cp = reinterpret_cast<uint4*>(xr + ((c ^ (r & 7)) << 4));
+            uint4 v = *cp;
+            uint32_t* vw = reinterpret_cast<uint32_t*>(&v);
+            uint4 xv = make_uint4(0, 0, 0, 0);
+            if (!rec && in_seq) xv = __ldg(reinterpret_cast<const uint4*>(xg + xrow_g) + c);
+            const uint32_t* xw = reinterpret_cast<const uint32_t*>(&xv);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int pi = 8 * c + 2 * e;
+              const float a0 = __uint_as_float(pi < 32 ? ya[pi] : yb[pi - 32]);
+              const float a1 = __uint_as_float(pi + 1 < 32 ? ya[pi + 1] : yb[pi + 1 - 32]);
+              float y0, y1;
+              if (rec) {
+                y0 = ri * fmaf(kx, bf16_lo(vw[e]), a0);
+                y1 = ri * fmaf(kx, bf16_hi(vw[e]), a1);
+              } else {
+                y0 = fmaf(Dh, bf16_lo(xw[e]), ri * a0);
+                y1 = fmaf(Dh, bf16_hi(xw[e]), ri * a1);
+              }
+              vw[e] = pack_bf16x2(y0, y1);
+            }
+            *cp = v;
+          }
+        }
+      } else {
+        // exact fallback: the accumulator holds C_i h_in^T; the intra sum runs on
+        // CUDA cores from C B^T with one exponential per element (exponent <= 0)
+        float acc[64];
+#pragma unroll
+        for (int q = 0; q < 64; ++q) acc[q] = 0.f;
+        const float* grow = cumsum + (static_cast<int64_t>(W.b) * d.H + h) * d.Lp;
+        const float* dtrow = dt_t + (static_cast<int64_t>(W.b) * d.H + h) * d.Lp + W.t0;
+        const int jmax = quad * 32 + 31 < S ? quad * 32 + 31 : S - 1;  // last row of this warp
+        for (int j = 0; j <= jmax; ++j) {
+          const float cb = __uint_as_float(tmem_ld1(tmem + lane_base + kColCB + j));
+          tmem_ld_wait();
+          if (W.t0 + j >= d.L) continue;  // warp-uniform
+          const float gj = (grow[W.t0 + j] - cur.base) * kLog2e;
+          const float coef = (j <= r) ? cb * fast_exp2(fminf(gi - gj, 0.f)) * dtrow[j] : 0.f;
+          const uint4* xj =
+              reinterpret_cast<const uint4*>(xg + ((static_cast<int64_t>(W.b) * d.L + W.t0 + j) * d.H + h) * d.P);
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const uint4 xv = __ldg(xj + c);
+            const uint32_t* xw = reinterpret_cast<const uint32_t*>(&xv);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              acc[8 * c + 2 * e] = fmaf(coef, bf16_lo(xw[e]), acc[8 * c + 2 * e]);
+              acc[8 * c + 2 * e + 1] = fmaf(coef, bf16_hi(xw[e]), acc[8 * c + 2 * e + 1]);
+            }
+          }
+        }
+        // the accumulator in two 32-column halves (keeps the register count down)
+        const float ei = fast_exp2(gi);
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          uint32_t ya[32];
+          tmem_ld32(tmem + lane_base + kColY + 64 * wg + 32 * half, ya);
+          tmem_ld_wait();
+          if (r < S) {
+#pragma unroll
+            for (int c = 4 * half; c < 4 * half + 4; ++c) {
+              uint4 xv = make_uint4(0, 0, 0, 0);
+              if (in_seq) xv = __ldg(reinterpret_cast<const uint4*>(xg + xrow_g) + c);
+              const uint32_t* xw = reinterpret_cast<const uint32_t*>(&xv);
+              uint4 v;
+              uint32_t* vw = reinterpret_cast<uint32_t*>(&v);
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int pi = 8 * c + 2 * e;
+                const float a0 = __uint_as_float(ya[pi - 32 * half]);
+                const float a1 = __uint_as_float(ya[pi + 1 - 32 * half]);
+                vw[e] = pack_bf16x2(fmaf(Dh, bf16_lo(xw[e]), fmaf(ei, a0, acc[pi])),
+                                    fmaf(Dh, bf16_hi(xw[e]), fmaf(ei, a1, acc[pi + 1])));
+              }
+              *reinterpret_cast<uint4*>(xr + ((c ^ (r & 7)) << 4)) = v;
+            }
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(yfree);
+        mbar_arrive(cbfree);
+      }
+      fence_proxy_async_smem();
+      named_bar_sync(bar_wg, 128);
+      if (et == 0) {
+        if (wg == 0) {
+          coord[3 * buf] = W.b;
+          coord[3 * buf + 1] = W.t0;
+          coord[3 * buf + 2] = W.h0;
+        }
+        mbar_arrive(&ystaged[buf]);
+      }
+      cur = nxt;
+    }
+    // end marker for the store warp (both warpgroups arrive, as for a window)
+    if (ok && et == 0) {
+      const int buf = n & 1;
+      if (wg == 0) coord[3 * buf] = -1;
+      mbar_arrive(&ystaged[buf]);
+    }
+  }
+
+  if (!ok) atomicExch(status, static_cast<int>(SSD_ERR_DEVICE_TIMEOUT));
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace
+
+size_t fused_smem_bytes(const Dims& d) { return fused_smem_layout(d.N).total + 1024; }
+
+cudaError_t launch_fused(const Dims& d, const FusedMaps& maps, const float* D, const void* x, const float* init,
+                         float* hslot, const Work& w, uint64_t spin_ns, cudaStream_t stream) {
+  const int S = d.Q < 128 ? d.Q : 128;
+  const int R = d.N <= 128 ? 4 : 1;  // windows per run (the running state needs 128 spare TMEM columns)
+  const int nw = d.Lp / S;
+  const int ntiles = ((nw + R - 1) / R) * d.B * (d.H / 2);
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const size_t smem = fused_smem_bytes(d);
+  e = cudaFuncSetAttribute(ssd_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  const int grid = ntiles < sms ? ntiles : sms;
+  ssd_fused_kernel<<<grid, kThreads, smem, stream>>>(maps.x, maps.cm, maps.bm, maps.y, d, R, w.cumsum, w.dt_t, D, init,
+                                                     hslot, w.flags, w.counter,
+                                                     static_cast<const __nv_bfloat16*>(x), w.status, spin_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace ssd

@@ -25,6 +25,9 @@ struct Work {
   float* dt_t;                 // [B][H][Lp]
   void* states;                // [B][nc][H][P][N], fp32 (fp32 inputs) or bf16 (bf16 inputs)
   __nv_bfloat16* states_bf16;  // [B][nc][H][P][N] or null (fp32 problems)
+  int* counter;                // one-pass kernel: tile counter
+  int* flags;                  // one-pass kernel: [B][H/2] windows published
+  float* hslot;                // one-pass kernel: running state [B][H][P][N]
 };
 
 // Tensor maps built on the host for one call.
@@ -41,6 +44,14 @@ struct ComputeOutMaps {
   CUtensorMap y;   // y [B][L][H*P], box {128 B of p, 32 tokens, 1} (TMA stores)
 };
 
+// Tensor maps of the one-pass kernel (bf16), window of S = min(Q, 128) tokens.
+struct FusedMaps {
+  CUtensorMap x;   // x [B][L][H*P], box {64 p, S tokens, 1}
+  CUtensorMap cm;  // Cm [B][L][G][N], box {64 n, 1, S tokens, 1}
+  CUtensorMap bm;  // Bm, same box
+  CUtensorMap y;   // y [B][L][H*P], box {64 p, S tokens, 1} (TMA stores)
+};
+
 cudaError_t launch_chunk_cumsum(const Dims& d, const float* dt, const float* A, const Work& w,
                                 cudaStream_t stream);
 cudaError_t launch_chunk_state(const Dims& d, bool bf16, const ChunkStateMaps& maps, const Work& w,
@@ -49,6 +60,9 @@ cudaError_t launch_state_passing(const Dims& d, bool bf16, const float* init, fl
                                  const Work& w, cudaStream_t stream);
 cudaError_t launch_compute_out(const Dims& d, bool bf16, const ComputeOutMaps& maps, const float* D,
                                const void* x, void* y, const Work& w, uint64_t spin_ns, cudaStream_t stream);
+size_t fused_smem_bytes(const Dims& d);
+cudaError_t launch_fused(const Dims& d, const FusedMaps& maps, const float* D, const void* x, const float* init,
+                         float* hslot, const Work& w, uint64_t spin_ns, cudaStream_t stream);
 cudaError_t launch_timeout_probe(int* status, uint64_t limit_ns, cudaStream_t stream);
 
 }  // namespace ssd

@@ -32,11 +32,12 @@ def to_device(inp: Dict[str, np.ndarray], dtype: str, device="cuda") -> Dict[str
     return out
 
 
-def run_gpu(inp: Dict[str, np.ndarray], dtype: str, Q: int, with_init: Optional[bool] = None):
+def run_gpu(inp: Dict[str, np.ndarray], dtype: str, Q: int, with_init: Optional[bool] = None,
+            schedule: str = "auto"):
     import mamba_ssd_forward_chunked_gb300 as ssd
     d = to_device(inp, dtype)
     init = d.get("init") if (with_init is None or with_init) else None
-    y, fin = ssd.ssd_fwd(d["x"], d["dt"], d["A"], d["Bm"], d["Cm"], d["D"], Q, init_state=init)
+    y, fin = ssd.ssd_fwd(d["x"], d["dt"], d["A"], d["Bm"], d["Cm"], d["D"], Q, init_state=init, schedule=schedule)
     torch.cuda.synchronize()
     return y.float().cpu().numpy().astype(np.float64), fin.cpu().numpy().astype(np.float64)
 
@@ -51,12 +52,12 @@ def sampled_pairs(B: int, H: int, k: int, seed: int = 0) -> np.ndarray:
     return np.array(sorted(pairs), dtype=np.int64)
 
 
-def compare_with_oracle(w: ssd_synth.Workload, inp=None, pairs=None, Q=None):
+def compare_with_oracle(w: ssd_synth.Workload, inp=None, pairs=None, Q=None, schedule: str = "auto"):
     """Run the GPU on workload ``w`` and the oracle recurrence on all (or the
     sampled) (b, h) pairs.  Returns (err_y, err_final, y_gpu, f_gpu)."""
     inp = ssd_synth.make_inputs(w) if inp is None else inp
     Q = w.chunk_size if Q is None else Q
-    y, f = run_gpu(inp, w.dtype, Q)
+    y, f = run_gpu(inp, w.dtype, Q, schedule=schedule)
     yr, fr, _ = oracle.recurrence(inp, pairs=pairs)
     if pairs is None:
         return rel_err(y, yr), rel_err(f, fr), y, f
