@@ -140,6 +140,17 @@ ssd_status ssd_fwd_fused(const ssd_shape* shape, const void* x, const float* dt,
                          const void* Bm, const void* Cm, const float* D, const float* init_state, void* y,
                          float* final_state, void* workspace, size_t workspace_bytes, ssd_stream_t stream);
 
+/* The one-pass schedule's second step alone (ssd_fwd_fused is
+ * ssd_chunk_cumsum followed by this call): for every window of
+ * min(chunk_size, 128) tokens of every (batch, head pair), the window state on
+ * the tensor core, the state carried from the previous window (through the
+ * workspace slot, or final_state, and a per-pair flag), and y.  Needs step 1
+ * (chunk_cumsum), which also clears the flags.  SSD_BF16 only
+ * (SSD_ERR_UNSUPPORTED otherwise); arguments as for ssd_fwd. */
+ssd_status ssd_fused_pass(const ssd_shape* shape, const void* x, const void* Bm, const void* Cm, const float* D,
+                          const float* init_state, void* y, float* final_state, void* workspace,
+                          size_t workspace_bytes, ssd_stream_t stream);
+
 /* After the caller has synchronised the stream of a call that used
  * `workspace`: SSD_OK, or SSD_ERR_DEVICE_TIMEOUT if a bounded wait inside a
  * kernel ran out (its outputs are then invalid).  Blocking 4-byte read. */

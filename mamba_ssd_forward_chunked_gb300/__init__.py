@@ -26,7 +26,7 @@ STATUS = {0: "SSD_OK", 1: "SSD_ERR_INVALID_ARG", 2: "SSD_ERR_UNSUPPORTED", 3: "S
 EXPORTS = ("ssd_status_string", "ssd_validate_shape", "ssd_fwd_workspace_layout", "ssd_fwd_workspace_size",
            "ssd_fwd", "ssd_fwd_check", "ssd_chunk_cumsum", "ssd_chunk_state", "ssd_state_passing",
            "ssd_compute_out", "ssd_debug_timeout_probe", "ssd_fwd_kernel_count", "ssd_fwd_static_scratch",
-           "ssd_fwd_fused")
+           "ssd_fwd_fused", "ssd_fused_pass")
 
 # Size of the library's own workspace array used by ssd_fwd_static_scratch.
 SSD_STATIC_SCRATCH_BYTES = 32 << 20
@@ -77,6 +77,8 @@ def _load() -> ctypes.CDLL:
     lib.ssd_fwd.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     lib.ssd_fwd_fused.restype = c_int
     lib.ssd_fwd_fused.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    lib.ssd_fused_pass.restype = c_int
+    lib.ssd_fused_pass.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     lib.ssd_fwd_check.restype = c_int
     lib.ssd_fwd_check.argtypes = [vp]
     lib.ssd_chunk_cumsum.restype = c_int
@@ -231,6 +233,15 @@ def ssd_fwd(x: torch.Tensor, dt: torch.Tensor, A: torch.Tensor, Bm: torch.Tensor
 def ssd_fwd_check(workspace: torch.Tensor) -> int:
     """Device status word after the caller synchronised (C: ssd_fwd_check)."""
     return lib.ssd_fwd_check(_ptr(workspace))
+
+
+def ssd_fused_pass(shape: ssd_shape, x: torch.Tensor, Bm: torch.Tensor, Cm: torch.Tensor, D: torch.Tensor,
+                   init_state: Optional[torch.Tensor], y: torch.Tensor, final_state: Optional[torch.Tensor],
+                   workspace: torch.Tensor, stream=None) -> None:
+    """The one-pass kernel alone, after ssd_chunk_cumsum (C: ssd_fused_pass)."""
+    _check(lib.ssd_fused_pass(ctypes.byref(shape), _ptr(x), _ptr(Bm), _ptr(Cm), _ptr(D), _ptr(init_state), _ptr(y),
+                              _ptr(final_state), _ptr(workspace), workspace.numel(), _stream(stream)),
+           "ssd_fused_pass")
 
 
 def ssd_chunk_cumsum(shape: ssd_shape, dt: torch.Tensor, A: torch.Tensor, workspace: torch.Tensor,

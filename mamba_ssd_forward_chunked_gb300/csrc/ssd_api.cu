@@ -360,6 +360,26 @@ ssd_status ssd_fwd(const ssd_shape* shape, const void* x, const float* dt, const
   return fwd_impl(path, shape, x, dt, A, Bm, Cm, D, init_state, y, final_state, workspace, workspace_bytes, stream);
 }
 
+ssd_status ssd_fused_pass(const ssd_shape* shape, const void* x, const void* Bm, const void* Cm, const float* D,
+                          const float* init_state, void* y, float* final_state, void* workspace,
+                          size_t workspace_bytes, ssd_stream_t stream) {
+  ssd_workspace_layout L;
+  ssd_status st = check_workspace(shape, workspace, workspace_bytes, &L);
+  if (st != SSD_OK) return st;
+  if (shape->dtype != SSD_BF16) return SSD_ERR_UNSUPPORTED;
+  if ((init_state && !aligned16(init_state)) || (final_state && !aligned16(final_state)))
+    return SSD_ERR_INVALID_ARG;
+  if (empty_problem(*shape)) return SSD_OK;
+  if (!x || !Bm || !Cm || !D || !y || !aligned16(x) || !aligned16(Bm) || !aligned16(Cm) || !aligned16(y) ||
+      !aligned4(D))
+    return SSD_ERR_INVALID_ARG;
+  Work w = carve(workspace, L, true);
+  FusedMaps fmaps;
+  if (!build_fused_maps(*shape, x, Bm, Cm, y, &fmaps)) return SSD_ERR_CUDA;
+  return from_cuda(launch_fused(make_dims(*shape), fmaps, D, x, init_state, final_state ? final_state : w.hslot, w,
+                                spin_limit_ns(), reinterpret_cast<cudaStream_t>(stream)));
+}
+
 ssd_status ssd_fwd_fused(const ssd_shape* shape, const void* x, const float* dt, const float* A, const void* Bm,
                          const void* Cm, const float* D, const float* init_state, void* y, float* final_state,
                          void* workspace, size_t workspace_bytes, ssd_stream_t stream) {

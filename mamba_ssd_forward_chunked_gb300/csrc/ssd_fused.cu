@@ -142,12 +142,76 @@ __device__ __forceinline__ uint32_t scale_bf16x2(uint32_t v, float s) {
   return pack_bf16x2(bf16_lo(v) * s, bf16_hi(v) * s);
 }
 
+// Exact fallback for a window whose decay leaves the fp32 range of the
+// rescaled form: the accumulator holds C_i h_in^T (carried state, unscaled),
+// the intra sum runs on CUDA cores from C B^T with one exponential per element
+// (exponent <= 0), and y_i = e^{G_i} acc + intra + D x_i is written over x.
+// Slow and rare, kept out of line.
+__device__ __noinline__ void fallback_epilogue(const Dims& d, const Win& W, int h, int S, int r, int quad,
+                                               uint32_t tlane, const float* __restrict__ cumsum,
+                                               const float* __restrict__ dt_t, const __nv_bfloat16* __restrict__ xg,
+                                               float base, float gi, float Dh, bool in_seq, int64_t xrow_g,
+                                               uint8_t* xr) {
+  float acc[64];
+#pragma unroll
+  for (int q = 0; q < 64; ++q) acc[q] = 0.f;
+  const float* grow = cumsum + (static_cast<int64_t>(W.b) * d.H + h) * d.Lp;
+  const float* dtrow = dt_t + (static_cast<int64_t>(W.b) * d.H + h) * d.Lp + W.t0;
+  const int jmax = quad * 32 + 31 < S ? quad * 32 + 31 : S - 1;  // last row of this warp
+  for (int j = 0; j <= jmax; ++j) {
+    const float cb = __uint_as_float(tmem_ld1(tlane + kColCB + j));
+    tmem_ld_wait();
+    if (W.t0 + j >= d.L) continue;  // warp-uniform
+    const float gj = (grow[W.t0 + j] - base) * kLog2e;
+    const float coef = (j <= r) ? cb * fast_exp2(fminf(gi - gj, 0.f)) * dtrow[j] : 0.f;
+    const uint4* xj = reinterpret_cast<const uint4*>(xg + ((static_cast<int64_t>(W.b) * d.L + W.t0 + j) * d.H + h) * d.P);
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const uint4 xv = __ldg(xj + c);
+      const uint32_t* xw = reinterpret_cast<const uint32_t*>(&xv);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        acc[8 * c + 2 * e] = fmaf(coef, bf16_lo(xw[e]), acc[8 * c + 2 * e]);
+        acc[8 * c + 2 * e + 1] = fmaf(coef, bf16_hi(xw[e]), acc[8 * c + 2 * e + 1]);
+      }
+    }
+  }
+  const float ei = fast_exp2(gi);
+  const int wg_col = h & 1;  // the head's 64 accumulator columns
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    uint32_t ya[32];
+    tmem_ld32(tlane + kColY + 64 * wg_col + 32 * half, ya);
+    tmem_ld_wait();
+    if (r < S) {
+#pragma unroll
+      for (int c = 4 * half; c < 4 * half + 4; ++c) {
+        uint4 xv = make_uint4(0, 0, 0, 0);
+        if (in_seq) xv = __ldg(reinterpret_cast<const uint4*>(xg + xrow_g) + c);
+        const uint32_t* xw = reinterpret_cast<const uint32_t*>(&xv);
+        uint4 v;
+        uint32_t* vw = reinterpret_cast<uint32_t*>(&v);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int pi = 8 * c + 2 * e;
+          const float a0 = __uint_as_float(ya[pi - 32 * half]);
+          const float a1 = __uint_as_float(ya[pi + 1 - 32 * half]);
+          vw[e] = pack_bf16x2(fmaf(Dh, bf16_lo(xw[e]), fmaf(ei, a0, acc[pi])),
+                              fmaf(Dh, bf16_hi(xw[e]), fmaf(ei, a1, acc[pi + 1])));
+        }
+        *reinterpret_cast<uint4*>(xr + ((c ^ (r & 7)) << 4)) = v;
+      }
+    }
+  }
+}
+
 // A warpgroup thread's view of one window: the scalars of its warpgroup's
 // head and its token row's cumsum and dt (loaded one window ahead).
 struct TileCtx {
   int tile, fast, first, last;
   float base, gm, ge;  // as in TileInfo, for this warpgroup's head
   float graw, dt;      // cumsum (natural log, chunk-relative) and dt at token row r
+  float D;             // skip coefficient of this warpgroup's head
 };
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -480,6 +544,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int64_t o = (static_cast<int64_t>(W.b) * d.H + W.h0 + wg) * d.Lp + W.t0 + rr;
       c.graw = cumsum[o];
       c.dt = r < S ? dt_t[o] : 0.f;
+      c.D = Dvec[W.h0 + wg];
       return true;
     };
     // X^ = wfac * x for this warpgroup's head, in place (a 128-B row is one token)
@@ -566,43 +631,80 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
-        for (int hf = 0; hf < NH; ++hf) {
-          const int nn = 128 * hf + r;
-          if (nn >= d.N) continue;  // warp-uniform (N is a multiple of 64)
+        if (NH == 1) {
+          // dstate <= 128: the run's state lives in tensor memory next to the window state
+          const int nn = r;
+          const bool lane_ok = nn < d.N;  // warp-uniform (N is a multiple of 64)
           uint8_t* ocol = smem + L.obuf + (nn >> 6) * kAtomBytes + (nn & 7) * 2;
           const int cchunk = (nn & 63) >> 3;
+          const uint32_t tD = tmem + lane_base + kColD + 64 * wg, tH = tmem + lane_base + kColH + 64 * wg;
+          if (first && lane_ok) {  // stage h_in (predecessor's state, init or zero) into tensor memory
 #pragma unroll 1
-          for (int pb = 0; pb < 2; ++pb) {
-            float hv[32];
-            if (first) {  // 32 loads in flight (the chain's critical path is their latency)
+            for (int pb = 0; pb < 2; ++pb) {
+              uint32_t hv[32];
               const float* hp_in = hin ? hin + 32 * pb * d.N + nn : nullptr;
 #pragma unroll
-              for (int q = 0; q < 32; ++q) hv[q] = hp_in ? __ldcg(hp_in + q * d.N) : 0.f;
-            } else {
-              uint32_t hr[32];
-              tmem_ld32(tmem + lane_base + kColH + 64 * wg + 32 * pb, hr);
-              tmem_ld_wait();
-#pragma unroll
-              for (int q = 0; q < 32; ++q) hv[q] = __uint_as_float(hr[q]);
+              for (int q = 0; q < 32; ++q) hv[q] = hp_in ? __float_as_uint(__ldcg(hp_in + q * d.N)) : 0u;
+              tmem_st32(tH + 32 * pb, hv);
             }
-#pragma unroll
-            for (int pc = 0; pc < 2; ++pc) {
-              uint32_t dv[16];
-              tmem_ld16(tmem + lane_base + kColD + 128 * hf + 64 * wg + 32 * pb + 16 * pc, dv);
+            tmem_st_wait();
+          }
+          if (lane_ok) {
+#pragma unroll 1
+            for (int pb = 0; pb < 2; ++pb) {
+              uint32_t hv[32], dv[32];
+              tmem_ld32(tD + 32 * pb, dv);
+              tmem_ld32(tH + 32 * pb, hv);
               tmem_ld_wait();
-              uint32_t hn[16];
+              const int row0 = 64 * wg + 32 * pb;
 #pragma unroll
-              for (int q = 0; q < 16; ++q) {
-                const int p = 32 * pb + 16 * pc + q;
-                const float hq = hv[16 * pc + q];
-                const float ho = fmaf(s_fac, __uint_as_float(dv[q]), e_fac * hq);
-                hn[q] = __float_as_uint(ho);
-                if (last) __stcg(hs + p * d.N + nn, ho);
-                const int row = 64 * wg + p;
+              for (int q = 0; q < 32; ++q) {
+                const float hq = __uint_as_float(hv[q]);
+                dv[q] = __float_as_uint(fmaf(s_fac, __uint_as_float(dv[q]), e_fac * hq));
+                const int row = row0 + q;
                 *reinterpret_cast<__nv_bfloat16*>(ocol + row * 128 + ((cchunk ^ (row & 7)) << 4)) =
                     __float2bfloat16_rn(o_fac * hq);
               }
-              if (!last) tmem_st16(tmem + lane_base + kColH + 64 * wg + 32 * pb + 16 * pc, hn);
+              tmem_st32(tH + 32 * pb, dv);
+            }
+            tmem_st_wait();
+            if (last) {  // publish the run's state
+#pragma unroll 1
+              for (int pb = 0; pb < 2; ++pb) {
+                uint32_t hv[32];
+                tmem_ld32(tH + 32 * pb, hv);
+                tmem_ld_wait();
+                float* hp_out = hs + 32 * pb * d.N + nn;
+#pragma unroll
+                for (int q = 0; q < 32; ++q) __stcg(hp_out + q * d.N, __uint_as_float(hv[q]));
+              }
+            }
+          }
+        } else {
+          // dstate 256 (runs of one window): h_in from global, h_out to global
+#pragma unroll 1
+          for (int hf = 0; hf < NH; ++hf) {
+            const int nn = 128 * hf + r;
+            uint8_t* ocol = smem + L.obuf + (nn >> 6) * kAtomBytes + (nn & 7) * 2;
+            const int cchunk = (nn & 63) >> 3;
+#pragma unroll 1
+            for (int pb = 0; pb < 2; ++pb) {
+              uint32_t hv[32], dv[32];
+              tmem_ld32(tmem + lane_base + kColD + 128 * hf + 64 * wg + 32 * pb, dv);
+              const float* hp_in = hin ? hin + 32 * pb * d.N + nn : nullptr;
+#pragma unroll
+              for (int q = 0; q < 32; ++q) hv[q] = hp_in ? __float_as_uint(__ldcg(hp_in + q * d.N)) : 0u;
+              tmem_ld_wait();
+              float* hp_out = hs + 32 * pb * d.N + nn;
+              const int row0 = 64 * wg + 32 * pb;
+#pragma unroll
+              for (int q = 0; q < 32; ++q) {
+                const float hq = __uint_as_float(hv[q]);
+                __stcg(hp_out + q * d.N, fmaf(s_fac, __uint_as_float(dv[q]), e_fac * hq));
+                const int row = row0 + q;
+                *reinterpret_cast<__nv_bfloat16*>(ocol + row * 128 + ((cchunk ^ (row & 7)) << 4)) =
+                    __float2bfloat16_rn(o_fac * hq);
+              }
             }
           }
         }
@@ -610,8 +712,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           __threadfence();
           named_bar_sync(bar_all, 256);
           if (wg == 0 && et == 0) st_release_gpu(flags + W.b * hp + W.pair, W.w + 1);
-        } else {
-          tmem_st_wait();
         }
         tc_fence_before();
         mbar_arrive(dfree);
@@ -631,7 +731,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc_fence_after();
-      const float Dh = Dvec[h];
+      const float Dh = cur.D;
       const float gi = (cur.graw - cur.base) * kLog2e;
       const float dti = cur.dt;
       const int64_t xrow_g = ((static_cast<int64_t>(W.b) * d.L + W.t0 + r) * d.H + h) * d.P;
@@ -647,90 +747,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (r < S) {
           const float ri = fast_exp2(gi - cur.gm);
           const float wfac = fast_exp2(cur.gm - gi) * dti;
-          // D x_i from X^_i = wfac x_i when wfac is well inside the normal range, else from global x
-          const bool rec = wfac >= 0x1p-80f;
-          const float kx = rec ? Dh / dti : 0.f;
+          // D x_i = (D / dt_i) r_i X^_i when X^_i = wfac x_i is well inside the normal range;
+          // otherwise (rare) x_i itself is copied over X^_i from global memory
+          float c = ri * Dh / dti;
+          if (!(wfac >= 0x1p-80f)) {
+            c = Dh;
+#pragma unroll 1
+            for (int k = 0; k < 8; ++k)
+              *reinterpret_cast<uint4*>(xr + ((k ^ (r & 7)) << 4)) =
+                  in_seq ? __ldg(reinterpret_cast<const uint4*>(xg + xrow_g) + k) : make_uint4(0, 0, 0, 0);
+          }
 #pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            uint4* cp = reinterpret_cast<uint4*>(xr + ((c ^ (r & 7)) << 4));
+          for (int k = 0; k < 8; ++k) {
+            uint4* cp = reinterpret_cast<uint4*>(xr + ((k ^ (r & 7)) << 4));
             uint4 v = *cp;
             uint32_t* vw = reinterpret_cast<uint32_t*>(&v);
-            uint4 xv = make_uint4(0, 0, 0, 0);
-            if (!rec && in_seq) xv = __ldg(reinterpret_cast<const uint4*>(xg + xrow_g) + c);
-            const uint32_t* xw = reinterpret_cast<const uint32_t*>(&xv);
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const int pi = 8 * c + 2 * e;
+              const int pi = 8 * k + 2 * e;
               const float a0 = __uint_as_float(pi < 32 ? ya[pi] : yb[pi - 32]);
               const float a1 = __uint_as_float(pi + 1 < 32 ? ya[pi + 1] : yb[pi + 1 - 32]);
-              float y0, y1;
-              if (rec) {
-                y0 = ri * fmaf(kx, bf16_lo(vw[e]), a0);
-                y1 = ri * fmaf(kx, bf16_hi(vw[e]), a1);
-              } else {
-                y0 = fmaf(Dh, bf16_lo(xw[e]), ri * a0);
-                y1 = fmaf(Dh, bf16_hi(xw[e]), ri * a1);
-              }
-              vw[e] = pack_bf16x2(y0, y1);
+              vw[e] = pack_bf16x2(fmaf(c, bf16_lo(vw[e]), ri * a0), fmaf(c, bf16_hi(vw[e]), ri * a1));
             }
             *cp = v;
           }
         }
       } else {
-        // exact fallback: the accumulator holds C_i h_in^T; the intra sum runs on
-        // CUDA cores from C B^T with one exponential per element (exponent <= 0)
-        float acc[64];
-#pragma unroll
-        for (int q = 0; q < 64; ++q) acc[q] = 0.f;
-        const float* grow = cumsum + (static_cast<int64_t>(W.b) * d.H + h) * d.Lp;
-        const float* dtrow = dt_t + (static_cast<int64_t>(W.b) * d.H + h) * d.Lp + W.t0;
-        const int jmax = quad * 32 + 31 < S ? quad * 32 + 31 : S - 1;  // last row of this warp
-        for (int j = 0; j <= jmax; ++j) {
-          const float cb = __uint_as_float(tmem_ld1(tmem + lane_base + kColCB + j));
-          tmem_ld_wait();
-          if (W.t0 + j >= d.L) continue;  // warp-uniform
-          const float gj = (grow[W.t0 + j] - cur.base) * kLog2e;
-          const float coef = (j <= r) ? cb * fast_exp2(fminf(gi - gj, 0.f)) * dtrow[j] : 0.f;
-          const uint4* xj =
-              reinterpret_cast<const uint4*>(xg + ((static_cast<int64_t>(W.b) * d.L + W.t0 + j) * d.H + h) * d.P);
-#pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            const uint4 xv = __ldg(xj + c);
-            const uint32_t* xw = reinterpret_cast<const uint32_t*>(&xv);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              acc[8 * c + 2 * e] = fmaf(coef, bf16_lo(xw[e]), acc[8 * c + 2 * e]);
-              acc[8 * c + 2 * e + 1] = fmaf(coef, bf16_hi(xw[e]), acc[8 * c + 2 * e + 1]);
-            }
-          }
-        }
-        // the accumulator in two 32-column halves (keeps the register count down)
-        const float ei = fast_exp2(gi);
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          uint32_t ya[32];
-          tmem_ld32(tmem + lane_base + kColY + 64 * wg + 32 * half, ya);
-          tmem_ld_wait();
-          if (r < S) {
-#pragma unroll
-            for (int c = 4 * half; c < 4 * half + 4; ++c) {
-              uint4 xv = make_uint4(0, 0, 0, 0);
-              if (in_seq) xv = __ldg(reinterpret_cast<const uint4*>(xg + xrow_g) + c);
-              const uint32_t* xw = reinterpret_cast<const uint32_t*>(&xv);
-              uint4 v;
-              uint32_t* vw = reinterpret_cast<uint32_t*>(&v);
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const int pi = 8 * c + 2 * e;
-                const float a0 = __uint_as_float(ya[pi - 32 * half]);
-                const float a1 = __uint_as_float(ya[pi + 1 - 32 * half]);
-                vw[e] = pack_bf16x2(fmaf(Dh, bf16_lo(xw[e]), fmaf(ei, a0, acc[pi])),
-                                    fmaf(Dh, bf16_hi(xw[e]), fmaf(ei, a1, acc[pi + 1])));
-              }
-              *reinterpret_cast<uint4*>(xr + ((c ^ (r & 7)) << 4)) = v;
-            }
-          }
-        }
+        fallback_epilogue(d, W, h, S, r, quad, tmem + lane_base, cumsum, dt_t, xg, cur.base, gi, Dh, in_seq, xrow_g,
+                          xr);
         tc_fence_before();
         mbar_arrive(yfree);
         mbar_arrive(cbfree);
