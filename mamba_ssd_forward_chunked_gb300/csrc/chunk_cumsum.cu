@@ -75,7 +75,10 @@ __global__ void __launch_bounds__(kThreads) chunk_cumsum_kernel(Dims d, const fl
     const float u = __shfl_up_sync(0xffffffffu, incl, off);
     if (lane >= off) incl += u;
   }
-  const float excl = incl - acc;
+  // exclusive prefix = the previous lane's inclusive one (not incl - acc): each G_t is then
+  // computed from tokens <= t only, so later tokens cannot change it even by rounding
+  float excl = __shfl_up_sync(0xffffffffu, incl, 1);
+  if (lane == 0) excl = 0.f;
 #pragma unroll
   for (int k = 0; k < 8; ++k)
     if (k < per) s_g[hh * ld + lane * per + k] = run[k] + excl;

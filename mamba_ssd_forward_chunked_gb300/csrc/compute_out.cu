@@ -72,6 +72,17 @@ struct OutCfg {
   static constexpr int kWgFloats = 3 * 256;  // per warpgroup: cumsum, dt, strip factors for 256 columns
 };
 
+constexpr float kSpan = 100.f;  // rescaled form: log2 bound on the diagonal block's decay
+
+// Rescaled operands are clamped to finite values: an overflowing product must
+// not become inf, which the causal select's zeros would turn into NaN in rows
+// that never see that token.
+__device__ __forceinline__ float clamp_finite(float v) { return fminf(fmaxf(v, -3.4e38f), 3.4e38f); }
+__device__ __forceinline__ uint32_t scale_bf16x2_clamped(uint32_t v, float s) {
+  constexpr float kMax = 3.38e38f;  // below bf16's largest finite value, so rounding cannot reach inf
+  return pack_bf16x2(fminf(fmaxf(bf16_lo(v) * s, -kMax), kMax), fminf(fmaxf(bf16_hi(v) * s, -kMax), kMax));
+}
+
 struct OutSmem {
   uint32_t ring, xring, wg, bars, holder, total;
 };
@@ -139,13 +150,53 @@ __device__ __forceinline__ void mask_strip(uint32_t (&v)[32], int j0, int i, flo
   }
 }
 
+// Rescaled form (see the kernel comment): the masked operand is the causal
+// select of C B^T alone.  One 32-column strip for row i, stored at `dst`.
+template <bool kTF32>
+__device__ __forceinline__ void causal_strip(uint32_t (&v)[32], int j0, int i, uint32_t dst) {
+  if (j0 > i) {  // strictly right of the diagonal (warp-uniform)
+#pragma unroll
+    for (int q = 0; q < 32; ++q) v[q] = 0u;
+  } else if (j0 + 31 > i) {  // the diagonal block
+#pragma unroll
+    for (int q = 0; q < 32; ++q) v[q] = j0 + q <= i ? v[q] : 0u;
+  }
+  if constexpr (kTF32) {
+    tmem_st32(dst, v);
+  } else {
+    uint32_t o[16];
+#pragma unroll
+    for (int q = 0; q < 16; ++q) o[q] = pack_bf16x2(__uint_as_float(v[2 * q]), __uint_as_float(v[2 * q + 1]));
+    tmem_st16(dst, o);
+  }
+}
+
+// Copies token r's raw x row (64 values, or zeros) over its rescaled copy in
+// the X block, in the layout the epilogue reads: TF32 boxes (r / 32, half)
+// after the transpose, bf16 row r (128-byte swizzle).  Only thread r touches
+// these bytes.
+template <bool kTF32, typename T>
+__device__ __noinline__ void restore_x_row(uint8_t* xy, int r, const T* src) {
+  if constexpr (kTF32) {
+    for (int half = 0; half < 2; ++half) {
+      uint8_t* bx = xy + (r >> 5) * 8192 + half * 4096;
+      for (int q = 0; q < 32; ++q)
+        *reinterpret_cast<float*>(bx + box_t_offset(r & 31, q)) = src ? static_cast<float>(src[32 * half + q]) : 0.f;
+    }
+  } else {
+    for (int k = 0; k < 8; ++k)
+      *reinterpret_cast<uint4*>(xy + r * 128 + ((k ^ (r & 7)) << 4)) =
+          src ? reinterpret_cast<const uint4*>(src)[k] : make_uint4(0, 0, 0, 0);
+  }
+}
+
 template <typename T>
 __global__ void __launch_bounds__(OutCfg<T>::kThreads, 1)
     compute_out_kernel(const __grid_constant__ CUtensorMap cmap, const __grid_constant__ CUtensorMap bmap,
                        const __grid_constant__ CUtensorMap hmap, const __grid_constant__ CUtensorMap xmap,
                        const __grid_constant__ CUtensorMap ymap, Dims d,
                        const float* __restrict__ cumsum, const float* __restrict__ dt_t,
-                       const float* __restrict__ Dvec, int* status, uint64_t spin_ns) {
+                       const float* __restrict__ Dvec, const T* __restrict__ xg, int* status, uint64_t spin_ns) {
   using C = OutCfg<T>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -329,7 +380,7 @@ __global__ void __launch_bounds__(OutCfg<T>::kThreads, 1)
     const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
     const uint32_t colM = C::kColM0 + 128 * hh, colY = C::kColY0 + 64 * hh;
     // per-tile column data (columns et and et + 128) and D_h, loaded one tile ahead
-    float pg[2], pd[2], pD = 0.f;
+    float pg[2], pd[2], pD = 0.f, pm[2], pl[2];
     auto prefetch = [&](int tile) {
       const TileId id = decode_tile(tile, d, ntile);
       const int h = id.h0 + hh;
@@ -339,6 +390,12 @@ __global__ void __launch_bounds__(OutCfg<T>::kThreads, 1)
         const int j = et + 128 * k;
         pg[k] = cumsum[grow + (j < Q ? j : Q - 1)];
         pd[k] = j < Q ? dt_t[grow + j] : 0.f;
+        // both heads of the pair: cumsum at the tile's first row (the reference token) and at
+        // the last column of its diagonal block
+        const int64_t prow = (static_cast<int64_t>(id.b) * d.H + id.h0 + k) * d.Lp + static_cast<int64_t>(id.c) * Q;
+        const int last = id.t * 128 + 127 < Q ? id.t * 128 + 127 : Q - 1;
+        pm[k] = cumsum[prow + id.t * 128];
+        pl[k] = cumsum[prow + last];
       }
       pD = Dvec[h];
     };
@@ -361,9 +418,17 @@ __global__ void __launch_bounds__(OutCfg<T>::kThreads, 1)
         }
       }
       const float Dh = pD;
+      // rescaled form for the whole pair while the diagonal block's decay stays within 2^kSpan
+      // (G is non-increasing: every other factor of the form is <= 1)
+      bool fast = true;
+#pragma unroll
+      for (int k = 0; k < 2; ++k) fast = fast && ((pm[k] - pl[k]) * kLog2e <= kSpan);
+      const float gm = pm[hh] * kLog2e;  // this head's reference, log2 units
       if (tile + static_cast<int>(gridDim.x) < ntiles) prefetch(tile + gridDim.x);  // in flight during this tile
       named_bar_sync(bar_id, 128);
-      for (int j = et; j < ncol; j += 128) vref[j] = fast_exp2(gs[j | 31] - gs[j]) * dts[j];
+      // fast: vref[j] = 2^(G_m - G_j) dt_j, the row scale of X; exact form: strip factors
+      for (int j = et; j < ncol; j += 128)
+        vref[j] = fast_exp2((fast ? gm : gs[j | 31]) - gs[j]) * dts[j];
       named_bar_sync(bar_id, 128);
       const float Gi = gs[i];
 
@@ -377,8 +442,8 @@ __global__ void __launch_bounds__(OutCfg<T>::kThreads, 1)
         const int xs = xit + hh;  // X-ring stage holding this head's X block
         xit += 2;
         uint8_t* xb = smem + L.xring + (xs % C::kXStages) * C::kXBytes;
-        if (jb == 0) {  // carried-state term: scale row i by exp(G_i)
-          const float eGi = fast_exp2(Gi);
+        if (jb == 0) {  // carried-state term: scale row i by exp(G_i) (rescaled form: by exp(G_m))
+          const float eGi = fast_exp2(fast ? gm : Gi);
           uint32_t v0[32], v1[32];
           tmem_ld32(tmem + lane_base + colY, v0);
           tmem_ld32(tmem + lane_base + colY + 32, v1);
@@ -405,17 +470,62 @@ __global__ void __launch_bounds__(OutCfg<T>::kThreads, 1)
           const int m = et & 63;
 #pragma unroll 1
           for (int box0 = 0; box0 < 8; box0 += 2) {
-            uint8_t* bp = xb + (box0 + (et >> 6)) * 4096;
+            const int bi = box0 + (et >> 6);
+            uint8_t* bp = xb + bi * 4096;
             float4 v[4];
             box_read_4x4(bp, m, v);
+            if (fast) {  // rescaled form: X^ = 2^(G_m - G_j) dt_j x_j (tokens 4a..4a+3 of the box)
+              const float* w = vref + jb * 128 + (bi >> 1) * 32 + 4 * (m >> 3);
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                v[q].x = clamp_finite(v[q].x * w[q]);
+                v[q].y = clamp_finite(v[q].y * w[q]);
+                v[q].z = clamp_finite(v[q].z * w[q]);
+                v[q].w = clamp_finite(v[q].w * w[q]);
+              }
+            }
             named_bar_sync(bar_id, 128);
             box_write_4x4_transposed(bp, m, v);
           }
           fence_proxy_async_smem();
         }
+        if constexpr (!C::kTF32) {
+          if (fast) {  // rescaled form: X^ rows scaled in place (row et = token et of the block)
+            if (!mbar_wait(&xfullb[xs % C::kXStages], (xs / C::kXStages) & 1, spin_ns)) {
+              ok = false;
+              break;
+            }
+            const float wj = vref[jb * 128 + et];
+            uint4* row = reinterpret_cast<uint4*>(xb + et * 128);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              uint4* cp = row + (k ^ (et & 7));  // swizzle-ordered steps: the warp spreads over all banks
+              uint4 v = *cp;
+              v.x = scale_bf16x2_clamped(v.x, wj);
+              v.y = scale_bf16x2_clamped(v.y, wj);
+              v.z = scale_bf16x2_clamped(v.z, wj);
+              v.w = scale_bf16x2_clamped(v.w, wj);
+              *cp = v;
+            }
+            fence_proxy_async_smem();
+          }
+        }
         // masked matrix, four 32-column strips; two TMEM loads in flight so the
         // next strip's load overlaps this strip's arithmetic
-        {
+        if (fast) {
+          uint32_t va[32], vb[32];
+          tmem_ld32(tmem + lane_base + C::kColCB, va);
+          tmem_ld32(tmem + lane_base + C::kColCB + 32, vb);
+          tmem_ld_wait();
+          causal_strip<C::kTF32>(va, jb * 128, i, tmem + lane_base + colM);
+          tmem_ld32(tmem + lane_base + C::kColCB + 64, va);
+          causal_strip<C::kTF32>(vb, jb * 128 + 32, i, tmem + lane_base + colM + (C::kTF32 ? 32 : 16));
+          tmem_ld_wait();
+          tmem_ld32(tmem + lane_base + C::kColCB + 96, vb);
+          causal_strip<C::kTF32>(va, jb * 128 + 64, i, tmem + lane_base + colM + (C::kTF32 ? 64 : 32));
+          tmem_ld_wait();
+          causal_strip<C::kTF32>(vb, jb * 128 + 96, i, tmem + lane_base + colM + (C::kTF32 ? 96 : 48));
+        } else {
           uint32_t va[32], vb[32];
           tmem_ld32(tmem + lane_base + C::kColCB, va);
           tmem_ld32(tmem + lane_base + C::kColCB + 32, vb);
@@ -461,6 +571,23 @@ __global__ void __launch_bounds__(OutCfg<T>::kThreads, 1)
       tc_fence_before();
       mbar_arrive(&yfree[hh]);  // Y_h may be overwritten by the next tile's MMAs
       uint8_t* xy = const_cast<uint8_t*>(xlast);
+      // rescaled form: y_i = r_i (acc + (D / dt_i) X^_i) with r_i = 2^(G_i - G_m), while X^_i = w_i x_i
+      // is well inside the normal range; otherwise x_i is copied back over X^_i from global memory
+      float ry = 1.f, kx = Dh;
+      if (fast) {
+        const float dti = dts[i];
+        const float wi = fast_exp2(gm - Gi) * dti;
+        ry = fast_exp2(Gi - gm);
+        if (wi >= 0x1p-80f) {
+          kx = Dh / dti;
+        } else {
+          kx = Dh / ry;
+          const int tok = id.c * Q + i;
+          const bool in_seq = i < Q && tok < d.L;
+          restore_x_row<C::kTF32>(xy, r, in_seq ? xg + ((static_cast<int64_t>(id.b) * d.L + tok) * d.H + h) * d.P
+                                                : nullptr);
+        }
+      }
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         const uint32_t (&yv)[32] = yall[half];
@@ -472,7 +599,7 @@ __global__ void __launch_bounds__(OutCfg<T>::kThreads, 1)
           float out[32];
 #pragma unroll
           for (int q = 0; q < 32; ++q)
-            out[q] = fmaf(Dh, *reinterpret_cast<const float*>(bx + box_t_offset(r & 31, q)), __uint_as_float(yv[q]));
+            out[q] = ry * fmaf(kx, *reinterpret_cast<const float*>(bx + box_t_offset(r & 31, q)), __uint_as_float(yv[q]));
           __syncwarp();
           const int rr = r & 31;
 #pragma unroll
@@ -490,8 +617,8 @@ __global__ void __launch_bounds__(OutCfg<T>::kThreads, 1)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const int q = 8 * k + 2 * e;
-              o[e] = pack_bf16x2(fmaf(Dh, bf16_lo(xw[e]), __uint_as_float(yv[q])),
-                                 fmaf(Dh, bf16_hi(xw[e]), __uint_as_float(yv[q + 1])));
+              o[e] = pack_bf16x2(ry * fmaf(kx, bf16_lo(xw[e]), __uint_as_float(yv[q])),
+                                 ry * fmaf(kx, bf16_hi(xw[e]), __uint_as_float(yv[q + 1])));
             }
             *px = make_uint4(o[0], o[1], o[2], o[3]);
           }
@@ -552,10 +679,10 @@ cudaError_t launch_impl(const Dims& d, const ComputeOutMaps& maps, const float* 
   const int ntile = d.Q >= 128 ? d.Q / 128 : 1;
   const long long ntiles = static_cast<long long>(d.B) * d.nc * ntile * (d.H / 2);
   const int grid = static_cast<int>(ntiles < sm_count() ? ntiles : sm_count());
-  (void)x;  // the D*x term reads x from the X blocks already in shared memory
   (void)y;  // written through maps.y
+  // the D*x term reads x from the X blocks in shared memory; x itself only for rows whose rescaled copy is tiny
   compute_out_kernel<T><<<grid, C::kThreads, smem, stream>>>(maps.cm, maps.bm, maps.hp, maps.x, maps.y, d, w.cumsum,
-                                                             w.dt_t, D, w.status, spin_ns);
+                                                             w.dt_t, D, static_cast<const T*>(x), w.status, spin_ns);
   return cudaGetLastError();
 }
 

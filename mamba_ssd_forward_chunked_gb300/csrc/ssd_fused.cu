@@ -13,22 +13,23 @@
 // log2 units, from the chunk_cumsum output).  Windows never straddle a chunk,
 // and the recurrence gives the same result for any split into windows.
 //
-// Rescaling against one reference token.  Pick m = S/2 - 1 and write
-// e^{G_i - G_j} = e^{G_i - G_m} e^{G_m - G_j}.  With X^_j = e^{G_m - G_j} dt_j x_j,
-// r_i = e^{G_i - G_m} and O = e^{G_m} h_in:
+// Rescaling against the window start.  Write e^{G_i - G_j} = e^{G_i} e^{-G_j}.
+// With X^_j = e^{-G_j} dt_j x_j and r_i = e^{G_i}:
 //
-//     y_i   = r_i [ sum_{j<=i} (c_i . b_j) X^_j + O c_i ] + D x_i
-//     h_out = e^{G_S - G_m} (X^^T B) + e^{G_S} h_in
+//     y_i   = r_i [ sum_{j<=i} (c_i . b_j) X^_j + h_in c_i ] + D x_i
+//     h_out = e^{G_S} (X^^T B + h_in)
 //
 // so the masked interaction operand is the causal select of C B^T alone (no
 // exponential per element, the same for both heads of a pair), the decay
 // lives in a per-token scale of X and a per-row scale of the output, and the
-// carried-state term shares the intra accumulator.  This is exact, and it
-// stays inside fp32 range while |G_m| and |G_S - G_m| are at most 100 (log2):
-// every factor is then within 2^+-100.  A window that exceeds that on either
-// head of the pair takes an exact fallback: X^ uses the window end as
-// reference (factors <= 1), the intra sum is done on CUDA cores from
-// C B^T with per-element exponentials, and the output scale is e^{G_i}.
+// carried-state term shares the intra accumulator.  This is exact; r_i <= 1
+// and X^ grows at most by e^{-G_S}, so it stays inside fp32 range while the
+// window's decay -G_S is at most 100 (log2).  It is also causal to the last
+// bit: y_i reads G only up to token i (X^_j of later tokens meets exact zeros
+// of the causal select).  A window whose decay exceeds that on either head of
+// the pair takes an exact fallback: X^ uses the window end as reference
+// (factors <= 1), the intra sum is done on CUDA cores from C B^T with
+// per-element exponentials, and the output scale is again e^{G_i}.
 //
 // Chaining windows: the window state is computed on the tensor core from this
 // window alone; h_in comes from the previous window of the same (batch, head
@@ -85,7 +86,7 @@ struct TileInfo {
   int fast;         // rescaled form valid for both heads
   int first, last;  // first / last window of its run
   float base[2];    // cumsum just before the window (natural log), per head
-  float gm[2];      // log2 cumsum at the reference token, relative to the window start
+  float gm[2];      // log2 cumsum at the reference token (the window start: 0)
   float ge[2];      // log2 cumsum at the window end, relative to the window start
 };
 
@@ -138,8 +139,12 @@ __device__ __forceinline__ void causal_pack_store(uint32_t (&v)[32], int j0, int
   tmem_st16(dst, o);
 }
 
+// Scaled pair, clamped below bf16's largest finite value: an overflowing
+// product must not become inf, which the causal select's zeros would turn
+// into NaN in rows that never see that token.
 __device__ __forceinline__ uint32_t scale_bf16x2(uint32_t v, float s) {
-  return pack_bf16x2(bf16_lo(v) * s, bf16_hi(v) * s);
+  constexpr float kMax = 3.38e38f;
+  return pack_bf16x2(fminf(fmaxf(bf16_lo(v) * s, -kMax), kMax), fminf(fmaxf(bf16_hi(v) * s, -kMax), kMax));
 }
 
 // Exact fallback for a window whose decay leaves the fp32 range of the
@@ -319,7 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float* row = cumsum + (static_cast<int64_t>(b) * d.H + 2 * pair + lane) * d.Lp;
           const int t0 = w * S;
           base = (t0 % d.Q) != 0 ? row[t0 - 1] : 0.f;
-          gm = row[t0 + S / 2 - 1];
+          gm = base;  // the reference token is the window start
           ge = row[t0 + S - 1];
         }
         const float base1 = __shfl_sync(0xffffffffu, base, 1), gm1 = __shfl_sync(0xffffffffu, gm, 1),
@@ -337,8 +342,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             ti.base[hh] = bs[hh];
             ti.gm[hh] = (ms[hh] - bs[hh]) * kLog2e;
             ti.ge[hh] = (es[hh] - bs[hh]) * kLog2e;
-            // G is non-increasing, so these two spans bound every exponent of the rescaled form
-            if (!(-ti.gm[hh] <= kSpan && ti.gm[hh] - ti.ge[hh] <= kSpan)) ti.fast = 0;
+            // G is non-increasing, so the window's decay bounds every exponent of the rescaled form
+            if (!(-ti.ge[hh] <= kSpan)) ti.fast = 0;
           }
           if (n >= kTileRing && !mbar_wait(&tempty[ts], ((n / kTileRing) - 1) & 1, spin_ns)) ok = false;
           if (ok) {
