@@ -156,6 +156,27 @@ class ClockMonitor:
         return {"sm_mhz": med, "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
 
 
+# ------------------------------------------------------------------ multi-rank host logic
+
+def max_over_ranks(values, world: int, device=None):
+    """Each value's maximum over all ranks (the slowest rank sets the job's
+    time).  world == 1 returns the values unchanged; otherwise every rank must
+    call it inside an initialised process group."""
+    if world == 1:
+        return [float(v) for v in values]
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.cpu()]
+
+
+def whole_job_tokens_per_s(tokens_per_rank: int, world: int, ms: float) -> float:
+    """Weak scaling: every rank runs the full workload, so the job processes
+    world x tokens in the slowest rank's time."""
+    return tokens_per_rank * world / (ms * 1e-3)
+
+
 # ------------------------------------------------------------------ GPU arm
 
 def _profile_traffic(kernel: str, workload: str):
@@ -287,12 +308,7 @@ def run_gpu(args, w: ssd_synth.Workload, rank: int, world: int, local_rank: int)
     if status != 0:
         raise RuntimeError("device status after timing: " + ssd.ssd_status_string(status))
 
-    ms = statistics.mean(step_ms)
-    ms_e2e = statistics.mean(e2e_ms)
-    if world > 1:
-        t = torch.tensor([ms, ms_e2e], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, ms_e2e = float(t[0]), float(t[1])
+    ms, ms_e2e = max_over_ranks([statistics.mean(step_ms), statistics.mean(e2e_ms)], world, dev)
     if rank != 0:
         return None
 
@@ -301,7 +317,7 @@ def run_gpu(args, w: ssd_synth.Workload, rank: int, world: int, local_rank: int)
     pk = peaks()
     tpeak = tensor_peak(pk, w.dtype)
     t_roof_us = max(flops / (tpeak * 1e12), total_bytes / (pk["hbm_gbs"] * 1e9)) * 1e6
-    tokens = w.tokens * world
+    tokens = w.tokens * world  # whole job (weak scaling)
     km = kernel_model(w)
     dom = max(per_kernel, key=per_kernel.get)
     dk = km[dom]
@@ -325,7 +341,7 @@ def run_gpu(args, w: ssd_synth.Workload, rank: int, world: int, local_rank: int)
     d2h = out_y.numel() * out_y.element_size() + out_f.numel() * out_f.element_size()
     line = {
         "metric": METRIC,
-        "value": tokens / (ms * 1e-3),
+        "value": whole_job_tokens_per_s(w.tokens, world, ms),
         "unit": "tokens/s",
         "n_gpus": world,
         "steps": args.steps,
@@ -348,7 +364,7 @@ def run_gpu(args, w: ssd_synth.Workload, rank: int, world: int, local_rank: int)
         "kernels_ms": per_kernel,
         "gpu_launches": len(names) * args.steps,
         "schedule": "one-pass" if fused else "staged",
-        "e2e": {"value": tokens / (ms_e2e * 1e-3), "unit": "tokens/s", "ms_per_step": ms_e2e,
+        "e2e": {"value": whole_job_tokens_per_s(w.tokens, world, ms_e2e), "unit": "tokens/s", "ms_per_step": ms_e2e,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "wall_s_timed_region_1": wall,
         "host_us_per_call": host_s / args.steps * 1e6,

@@ -1,0 +1,67 @@
+"""The N > 1 path of bench.py on CPU: two gloo ranks reduce their step times
+to the slowest one, the whole-job throughput counts every rank's tokens, and
+under torchrun the reference arm prints exactly one line (rank 0) while the
+other rank exits 0.  No GPU is used."""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, out_dir):
+    import torch.distributed as dist
+    sys.path.insert(0, ROOT)
+    import bench
+    dist.init_process_group("gloo", init_method=f"tcp://127.0.0.1:{port}", rank=rank, world_size=world)
+    try:
+        got = bench.max_over_ranks([1.0 + rank, 5.0 - rank, 2.5], world)
+    finally:
+        dist.destroy_process_group()
+    with open(os.path.join(out_dir, f"r{rank}.json"), "w") as f:
+        json.dump(got, f)
+
+
+def test_max_over_ranks_gloo_world2(tmp_path):
+    import torch.multiprocessing as mp
+    port = _free_port()
+    mp.start_processes(_rank_main, args=(2, port, str(tmp_path)), nprocs=2, join=True, start_method="spawn")
+    for r in range(2):
+        got = json.load(open(tmp_path / f"r{r}.json"))
+        assert got == [2.0, 5.0, 2.5]  # every rank sees the slowest rank's values
+
+
+def test_whole_job_throughput_counts_every_rank():
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.max_over_ranks([3.0, 4.0], 1) == [3.0, 4.0]
+    assert bench.whole_job_tokens_per_s(8192, 1, 1.0) == pytest.approx(8.192e6)
+    assert bench.whole_job_tokens_per_s(8192, 4, 2.0) == pytest.approx(4 * 8192 / 2e-3)
+
+
+def test_reference_arm_under_torchrun_world2():
+    import __graft_entry__
+    __graft_entry__.build()  # the oracle library the reference arm times
+    port = _free_port()
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+           "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.join(ROOT, "bench.py"),
+           "--impl", "reference", "--gpus", "2", "--steps", "1", "--warmup", "3", "--workload", "tiny",
+           "--cpu-seconds", "0.2"]
+    env = dict(os.environ, OMP_NUM_THREADS="2")
+    res = subprocess.run(cmd, cwd=ROOT, env=env, capture_output=True, text=True, timeout=300)
+    assert res.returncode == 0, res.stderr[-2000:]
+    lines = [l for l in res.stdout.splitlines() if l.strip().startswith("{")]
+    assert len(lines) == 1, res.stdout
+    line = json.loads(lines[0])
+    assert line["impl"] == "reference" and line["unit"] == "tokens/s" and line["value"] > 0
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"
