@@ -49,7 +49,8 @@ struct StateCfg {
   static constexpr int kBox = kTokens * 128;                        // one TMA box, bytes
   static constexpr int kABoxes = 128 / kAtom;                       // boxes spanning M = 128
   static constexpr int kABytes = kABoxes * kBox;
-  static constexpr int kStages = 4;
+  static constexpr int kMaxStages = 4;
+  static constexpr int kRingBytes = 96 * 1024;  // two CTAs per SM: each keeps its ring within 96 KB
   static constexpr int kThreads = 192;
 };
 
@@ -57,8 +58,14 @@ __host__ __device__ inline uint32_t state_stage_bytes(int N, int atom, int box, 
   return static_cast<uint32_t>(abytes + (N / atom) * box);
 }
 
+// Stages that fit the ring budget (2..4).
+__host__ __device__ inline int state_stages(uint32_t stage_bytes, int ring_bytes, int max_stages) {
+  const int n = ring_bytes / static_cast<int>(stage_bytes);
+  return n < 2 ? 2 : (n > max_stages ? max_stages : n);
+}
+
 template <typename T>
-__global__ void __launch_bounds__(StateCfg<T>::kThreads, 1)
+__global__ void __launch_bounds__(StateCfg<T>::kThreads, 2)
     chunk_state_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap bmap,
                        const __grid_constant__ CUtensorMap smap, Dims d, const float* __restrict__ cumsum,
                        const float* __restrict__ dt_t, int* status, uint64_t spin_ns) {
@@ -71,19 +78,20 @@ __global__ void __launch_bounds__(StateCfg<T>::kThreads, 1)
   const int g = h0 / (d.H / d.G);
   const int bBoxes = N / C::kAtom;
   const uint32_t stage_bytes = state_stage_bytes(N, C::kAtom, C::kBox, C::kABytes);
-  float* w_s = reinterpret_cast<float*>(smem + C::kStages * stage_bytes);  // [2][Q]
+  const int NS = state_stages(stage_bytes, C::kRingBytes, C::kMaxStages);
+  float* w_s = reinterpret_cast<float*>(smem + NS * stage_bytes);  // [2][Q]
   uint64_t* bars = reinterpret_cast<uint64_t*>(w_s + 2 * Q);
   uint64_t* full = bars;
-  uint64_t* scaled = bars + C::kStages;
-  uint64_t* empty = bars + 2 * C::kStages;
-  uint64_t* accum = bars + 3 * C::kStages;
+  uint64_t* scaled = bars + NS;
+  uint64_t* empty = bars + 2 * NS;
+  uint64_t* accum = bars + 3 * NS;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(accum + 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nstages = Q / C::kTokens;
   const uint32_t tmem_cols = static_cast<uint32_t>(N);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < C::kStages; ++s) {
+    for (int s = 0; s < NS; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&scaled[s], 128);
       mbar_init(&empty[s], 1);
@@ -117,7 +125,7 @@ __global__ void __launch_bounds__(StateCfg<T>::kThreads, 1)
   if (warp == 0) {
     if (lane == 0) {
       for (int it = 0; it < nstages; ++it) {
-        const int s = it % C::kStages, r = it / C::kStages;
+        const int s = it % NS, r = it / NS;
         if (r > 0 && !mbar_wait(&empty[s], (r - 1) & 1, spin_ns)) {
           ok = false;
           break;
@@ -138,7 +146,7 @@ __global__ void __launch_bounds__(StateCfg<T>::kThreads, 1)
       const uint32_t mn = C::kTF32 ? 0u : 1u;
       const uint32_t idesc = idesc_f32acc(C::kTF32 ? 2u : 1u, 128u, static_cast<uint32_t>(N), mn, mn);
       for (int it = 0; it < nstages; ++it) {
-        const int s = it % C::kStages, r = it / C::kStages;
+        const int s = it % NS, r = it / NS;
         if (!mbar_wait(&scaled[s], r & 1, spin_ns)) {
           ok = false;
           break;
@@ -169,7 +177,7 @@ __global__ void __launch_bounds__(StateCfg<T>::kThreads, 1)
   } else {
     const int et = threadIdx.x - 64;
     for (int it = 0; it < nstages; ++it) {
-      const int s = it % C::kStages, r = it / C::kStages;
+      const int s = it % NS, r = it / NS;
       if (!mbar_wait(&full[s], r & 1, spin_ns)) {
         ok = false;
         break;
@@ -250,22 +258,34 @@ __global__ void __launch_bounds__(StateCfg<T>::kThreads, 1)
                          pack_bf16x2(__uint_as_float(v[8 * k + 6]), __uint_as_float(v[8 * k + 7])));
       }
     };
-    for (int n0 = 0; n0 < N; n0 += 64) {
-      uint32_t va[32], vb[32];
-      tmem_ld32(lane_addr + static_cast<uint32_t>(n0), va);
-      tmem_ld32(lane_addr + static_cast<uint32_t>(n0 + 32), vb);
-      tmem_ld_wait();
-      put(n0, va);
-      put(n0 + 32, vb);
+    // in rounds of as many 16 KB boxes as the (now idle) ring holds; a round's
+    // stores have read the boxes before the next round overwrites them
+    const int nbox = N / kSAtom;
+    const int per_round = static_cast<int>(NS * stage_bytes / (128 * 128)) < nbox
+                              ? static_cast<int>(NS * stage_bytes / (128 * 128)) : nbox;
+    const int cols_round = per_round * kSAtom;  // a multiple of 64
+    for (int c0 = 0; c0 < N; c0 += cols_round) {
+      const int c1 = c0 + cols_round < N ? c0 + cols_round : N;
+      for (int n0 = c0; n0 < c1; n0 += 64) {
+        uint32_t va[32], vb[32];
+        tmem_ld32(lane_addr + static_cast<uint32_t>(n0), va);
+        tmem_ld32(lane_addr + static_cast<uint32_t>(n0 + 32), vb);
+        tmem_ld_wait();
+        put(n0 - c0, va);
+        put(n0 - c0 + 32, vb);
+      }
+      fence_proxy_async_smem();
+      named_bar_sync(1, 128);
+      if (threadIdx.x == 64) {
+        const int row0 = ((b * d.nc + c) * d.H + h0) * d.P;
+        for (int k = 0; k < (c1 - c0) / kSAtom; ++k)
+          tma_store_2d(&smap, stage + k * (128 * 128), c0 + k * kSAtom, row0);
+        tma_store_commit();
+        asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+      }
+      named_bar_sync(1, 128);
     }
-    fence_proxy_async_smem();
-    named_bar_sync(1, 128);
-    if (threadIdx.x == 64) {
-      const int row0 = ((b * d.nc + c) * d.H + h0) * d.P;
-      for (int k = 0; k < N / kSAtom; ++k) tma_store_2d(&smap, stage + k * (128 * 128), k * kSAtom, row0);
-      tma_store_commit();
-      asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-    }
+    if (threadIdx.x == 64) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
   }
   if (!ok) atomicExch(status, static_cast<int>(SSD_ERR_DEVICE_TIMEOUT));
   tc_fence_before();
@@ -281,8 +301,8 @@ cudaError_t launch_impl(const Dims& d, const ChunkStateMaps& maps, const Work& w
                         cudaStream_t stream) {
   using C = StateCfg<T>;
   const uint32_t stage_bytes = state_stage_bytes(d.N, C::kAtom, C::kBox, C::kABytes);
-  const size_t smem = 1024 + C::kStages * stage_bytes + 2 * d.Q * sizeof(float) +
-                      (3 * C::kStages + 1) * sizeof(uint64_t) + 16;
+  const int ns = state_stages(stage_bytes, C::kRingBytes, C::kMaxStages);
+  const size_t smem = 1024 + ns * stage_bytes + 2 * d.Q * sizeof(float) + (3 * ns + 1) * sizeof(uint64_t) + 16;
   static size_t configured = 0;
   if (smem > configured) {
     cudaError_t e = cudaFuncSetAttribute(chunk_state_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
