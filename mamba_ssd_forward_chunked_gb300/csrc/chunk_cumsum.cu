@@ -14,6 +14,7 @@
 // head's Q values with one warp (serial runs per lane + a warp-shuffle scan of
 // the run totals) and writes cumsum and dt as contiguous [B][H][Lp] rows.
 // Tokens past L read as dt = 0, so the cumsum stays flat in a ragged last chunk.
+#include "ptx.cuh"
 #include "ssd_internal.cuh"
 
 namespace ssd {
@@ -29,6 +30,7 @@ __global__ void __launch_bounds__(kThreads) chunk_cumsum_kernel(Dims d, const fl
                                                                  int* chain, int nchain) {
   __shared__ float s_dt[kHeadsPerBlock * 257];
   __shared__ float s_g[kHeadsPerBlock * 257];
+  grid_dep_launch();  // the next kernel may start its prologue while this one runs
   const int Q = d.Q;
   const int ld = Q + 1;  // odd row stride: the transposing writes hit distinct banks
   const int c = blockIdx.x;

@@ -108,6 +108,8 @@ __global__ void __launch_bounds__(StateCfg<T>::kThreads, 2)
     tmem_alloc(tmem_holder, tmem_cols);
     tmem_relinquish();
   }
+  grid_dep_wait();  // chunk_cumsum's results are visible from here on
+  grid_dep_launch();
   if (warp >= 2) {
     // token weights w_j = exp(G_last - G_j) * dt_j for both heads (exponent <= 0)
     for (int idx = threadIdx.x - 64; idx < 2 * Q; idx += 128) {
@@ -298,7 +300,7 @@ __global__ void __launch_bounds__(StateCfg<T>::kThreads, 2)
 
 template <typename T>
 cudaError_t launch_impl(const Dims& d, const ChunkStateMaps& maps, const Work& w, uint64_t spin_ns,
-                        cudaStream_t stream) {
+                        cudaStream_t stream, bool dependent) {
   using C = StateCfg<T>;
   const uint32_t stage_bytes = state_stage_bytes(d.N, C::kAtom, C::kBox, C::kABytes);
   const int ns = state_stages(stage_bytes, C::kRingBytes, C::kMaxStages);
@@ -311,17 +313,16 @@ cudaError_t launch_impl(const Dims& d, const ChunkStateMaps& maps, const Work& w
     configured = smem;
   }
   const dim3 grid(d.H / 2, d.nc, d.B);
-  chunk_state_kernel<T><<<grid, C::kThreads, smem, stream>>>(maps.x, maps.bm, maps.s, d, w.cumsum, w.dt_t,
-                                                             w.status, spin_ns);
-  return cudaGetLastError();
+  return launch_k(chunk_state_kernel<T>, grid, dim3(C::kThreads), smem, stream, dependent, maps.x, maps.bm, maps.s, d,
+                  static_cast<const float*>(w.cumsum), static_cast<const float*>(w.dt_t), w.status, spin_ns);
 }
 
 }  // namespace
 
 cudaError_t launch_chunk_state(const Dims& d, bool bf16, const ChunkStateMaps& maps, const Work& w,
-                               uint64_t spin_ns, cudaStream_t stream) {
-  return bf16 ? launch_impl<__nv_bfloat16>(d, maps, w, spin_ns, stream)
-              : launch_impl<float>(d, maps, w, spin_ns, stream);
+                               uint64_t spin_ns, cudaStream_t stream, bool dependent) {
+  return bf16 ? launch_impl<__nv_bfloat16>(d, maps, w, spin_ns, stream, dependent)
+              : launch_impl<float>(d, maps, w, spin_ns, stream, dependent);
 }
 
 }  // namespace ssd

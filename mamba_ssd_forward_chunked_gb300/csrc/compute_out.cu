@@ -248,6 +248,7 @@ __global__ void __launch_bounds__(OutCfg<T>::kThreads, 1)
     tmem_alloc(tmem_holder, C::kTmemCols);
     tmem_relinquish();
   }
+  grid_dep_wait();  // the entering states (and the cumsum) are visible from here on
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -666,7 +667,7 @@ int sm_count() {
 
 template <typename T>
 cudaError_t launch_impl(const Dims& d, const ComputeOutMaps& maps, const float* D, const void* x, void* y,
-                        const Work& w, uint64_t spin_ns, cudaStream_t stream) {
+                        const Work& w, uint64_t spin_ns, cudaStream_t stream, bool dependent) {
   using C = OutCfg<T>;
   const size_t smem = 1024 + out_smem_layout<T>().total;
   static bool configured = false;
@@ -681,17 +682,17 @@ cudaError_t launch_impl(const Dims& d, const ComputeOutMaps& maps, const float* 
   const int grid = static_cast<int>(ntiles < sm_count() ? ntiles : sm_count());
   (void)y;  // written through maps.y
   // the D*x term reads x from the X blocks in shared memory; x itself only for rows whose rescaled copy is tiny
-  compute_out_kernel<T><<<grid, C::kThreads, smem, stream>>>(maps.cm, maps.bm, maps.hp, maps.x, maps.y, d, w.cumsum,
-                                                             w.dt_t, D, static_cast<const T*>(x), w.status, spin_ns);
-  return cudaGetLastError();
+  return launch_k(compute_out_kernel<T>, dim3(grid), dim3(C::kThreads), smem, stream, dependent, maps.cm, maps.bm,
+                  maps.hp, maps.x, maps.y, d, static_cast<const float*>(w.cumsum), static_cast<const float*>(w.dt_t), D,
+                  static_cast<const T*>(x), w.status, spin_ns);
 }
 
 }  // namespace
 
 cudaError_t launch_compute_out(const Dims& d, bool bf16, const ComputeOutMaps& maps, const float* D, const void* x,
-                               void* y, const Work& w, uint64_t spin_ns, cudaStream_t stream) {
-  return bf16 ? launch_impl<__nv_bfloat16>(d, maps, D, x, y, w, spin_ns, stream)
-              : launch_impl<float>(d, maps, D, x, y, w, spin_ns, stream);
+                               void* y, const Work& w, uint64_t spin_ns, cudaStream_t stream, bool dependent) {
+  return bf16 ? launch_impl<__nv_bfloat16>(d, maps, D, x, y, w, spin_ns, stream, dependent)
+              : launch_impl<float>(d, maps, D, x, y, w, spin_ns, stream, dependent);
 }
 
 }  // namespace ssd

@@ -418,7 +418,7 @@ ssd_status fwd_impl(int path, const ssd_shape* shape, const void* x, const float
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e = launch_chunk_cumsum(d, dt, A, w, cs);
     if (e == cudaSuccess)
-      e = launch_fused(d, fmaps, D, x, init_state, final_state ? final_state : w.hslot, w, spin_limit_ns(), cs);
+      e = launch_fused(d, fmaps, D, x, init_state, final_state ? final_state : w.hslot, w, spin_limit_ns(), cs, true);
     return from_cuda(e);
   }
   ChunkStateMaps smaps;
@@ -430,9 +430,10 @@ ssd_status fwd_impl(int path, const ssd_shape* shape, const void* x, const float
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   const uint64_t spin = spin_limit_ns();
   cudaError_t e = launch_chunk_cumsum(d, dt, A, w, cs);
-  if (e == cudaSuccess) e = launch_chunk_state(d, bf16, smaps, w, spin, cs);
-  if (e == cudaSuccess) e = launch_state_passing(d, bf16, init_state, final_state, w, cs);
-  if (e == cudaSuccess) e = launch_compute_out(d, bf16, omaps, D, x, y, w, spin, cs);
+  // each kernel after the first is a programmatic dependent of the one before it
+  if (e == cudaSuccess) e = launch_chunk_state(d, bf16, smaps, w, spin, cs, true);
+  if (e == cudaSuccess) e = launch_state_passing(d, bf16, init_state, final_state, w, cs, true);
+  if (e == cudaSuccess) e = launch_compute_out(d, bf16, omaps, D, x, y, w, spin, cs, true);
   return from_cuda(e);
 }
 

@@ -46,6 +46,8 @@
 // in tensor memory; only the run's first window reads the predecessor's state
 // (after its flag) and only its last window writes the state and the flag.
 // R = 4 for dstate <= 128 and 1 for dstate = 256 (no tensor memory to spare).
+// (A sequence whose window count is not a multiple of R ends in single-window
+// runs; each single-window run pays the global state round trip at both ends.)
 //
 // GB300 mapping, per CTA (one per SM, 384 threads, persistent):
 //   warp 10   claims runs from the counter and expands them into windows with
@@ -112,6 +114,17 @@ __host__ __device__ inline FusedSmem fused_smem_layout(int N) {
 struct Win {
   int w, b, pair, h0, g, t0;
 };
+
+// Windows of a sequence: `long_runs` runs of R windows, then single windows.
+struct RunSplit {
+  int long_runs, runs;
+};
+__host__ __device__ inline RunSplit run_split(int nw, int R) {
+  RunSplit rs;
+  rs.long_runs = nw / R;
+  rs.runs = rs.long_runs + (nw - rs.long_runs * R);  // the remainder as single windows
+  return rs;
+}
 
 __device__ __forceinline__ Win decode(int tile, const Dims& d, int S) {
   const int hp = d.H / 2;
@@ -234,7 +247,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const bool holdC = NH == 1;                   // C stage kept for the carried-state product
   const int hp = d.H / 2;
   const int nw = d.Lp / S;
-  const int nruns = ((nw + R - 1) / R) * d.B * hp;
+  const RunSplit rs = run_split(nw, R);
+  const int nruns = rs.runs * d.B * hp;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
   uint64_t* full = bars;        // [4] stage ring
   uint64_t* empty = bars + 4;   // [4]
@@ -294,6 +308,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(tmem_holder, kTmemCols);
     tmem_relinquish();
   }
+  grid_dep_wait();  // chunk_cumsum's results (and its cleared counter and flags) are visible from here on
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -312,8 +327,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (run < nruns) {
         pair = run % hp;
         b = (run / hp) % d.B;
-        w0 = (run / hp / d.B) * R;
-        w1 = w0 + R < nw ? w0 + R : nw;
+        const int rho = run / hp / d.B;
+        w0 = rho < rs.long_runs ? rho * R : rs.long_runs * R + (rho - rs.long_runs);
+        w1 = rho < rs.long_runs ? w0 + R : w0 + 1;
       } else {
         more = false;  // publish one end marker
       }
@@ -818,11 +834,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 size_t fused_smem_bytes(const Dims& d) { return fused_smem_layout(d.N).total + 1024; }
 
 cudaError_t launch_fused(const Dims& d, const FusedMaps& maps, const float* D, const void* x, const float* init,
-                         float* hslot, const Work& w, uint64_t spin_ns, cudaStream_t stream) {
+                         float* hslot, const Work& w, uint64_t spin_ns, cudaStream_t stream, bool dependent) {
   const int S = d.Q < 128 ? d.Q : 128;
   const int R = d.N <= 128 ? 4 : 1;  // windows per run (the running state needs 128 spare TMEM columns)
   const int nw = d.Lp / S;
-  const int ntiles = ((nw + R - 1) / R) * d.B * (d.H / 2);
+  const int ntiles = run_split(nw, R).runs * d.B * (d.H / 2);
   int dev = 0, sms = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -831,10 +847,9 @@ cudaError_t launch_fused(const Dims& d, const FusedMaps& maps, const float* D, c
   e = cudaFuncSetAttribute(ssd_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   const int grid = ntiles < sms ? ntiles : sms;
-  ssd_fused_kernel<<<grid, kThreads, smem, stream>>>(maps.x, maps.cm, maps.bm, maps.y, d, R, w.cumsum, w.dt_t, D, init,
-                                                     hslot, w.flags, w.counter,
-                                                     static_cast<const __nv_bfloat16*>(x), w.status, spin_ns);
-  return cudaGetLastError();
+  return launch_k(ssd_fused_kernel, dim3(grid), dim3(kThreads), smem, stream, dependent, maps.x, maps.cm, maps.bm,
+                  maps.y, d, R, static_cast<const float*>(w.cumsum), static_cast<const float*>(w.dt_t), D, init, hslot,
+                  w.flags, w.counter, static_cast<const __nv_bfloat16*>(x), w.status, spin_ns);
 }
 
 }  // namespace ssd

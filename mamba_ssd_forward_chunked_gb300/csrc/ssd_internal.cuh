@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <utility>
 
 #include "ssd.h"
 
@@ -52,17 +53,37 @@ struct FusedMaps {
   CUtensorMap y;   // y [B][L][H*P], box {64 p, S tokens, 1} (TMA stores)
 };
 
+// Launches `kernel`; as a programmatic dependent of the preceding kernel in the
+// stream when `dependent` (its launch and prologue then overlap that kernel's
+// tail, and it waits in griddepcontrol.wait before reading its results).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                     bool dependent, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = dependent ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 cudaError_t launch_chunk_cumsum(const Dims& d, const float* dt, const float* A, const Work& w,
                                 cudaStream_t stream);
 cudaError_t launch_chunk_state(const Dims& d, bool bf16, const ChunkStateMaps& maps, const Work& w,
-                               uint64_t spin_ns, cudaStream_t stream);
+                               uint64_t spin_ns, cudaStream_t stream, bool dependent = false);
 cudaError_t launch_state_passing(const Dims& d, bool bf16, const float* init, float* final_state,
-                                 const Work& w, cudaStream_t stream);
+                                 const Work& w, cudaStream_t stream, bool dependent = false);
 cudaError_t launch_compute_out(const Dims& d, bool bf16, const ComputeOutMaps& maps, const float* D,
-                               const void* x, void* y, const Work& w, uint64_t spin_ns, cudaStream_t stream);
+                               const void* x, void* y, const Work& w, uint64_t spin_ns, cudaStream_t stream,
+                               bool dependent = false);
 size_t fused_smem_bytes(const Dims& d);
 cudaError_t launch_fused(const Dims& d, const FusedMaps& maps, const float* D, const void* x, const float* init,
-                         float* hslot, const Work& w, uint64_t spin_ns, cudaStream_t stream);
+                         float* hslot, const Work& w, uint64_t spin_ns, cudaStream_t stream, bool dependent = false);
 cudaError_t launch_timeout_probe(int* status, uint64_t limit_ns, cudaStream_t stream);
 
 }  // namespace ssd

@@ -15,6 +15,7 @@
 // in bf16 and write the entering state, rounded to bf16, to a separate array
 // (the compute_out tensor cores read bf16 operands).  The running state is
 // always fp32.
+#include "ptx.cuh"
 #include "ssd_internal.cuh"
 
 namespace ssd {
@@ -38,6 +39,8 @@ __global__ void __launch_bounds__(kThreads) state_passing_kernel(Dims d, const f
                                                                   const float* __restrict__ init,
                                                                   float* __restrict__ final_state) {
   constexpr int kVec = PassVec<kBF16>::kVec;
+  grid_dep_wait();  // chunk_state's results are visible from here on
+  grid_dep_launch();
   const int64_t pnv = static_cast<int64_t>(d.P) * d.N / kVec;  // vectors per (b, h)
   const int64_t gid = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
   const int64_t total = static_cast<int64_t>(d.B) * d.H * pnv;
@@ -119,16 +122,15 @@ __global__ void __launch_bounds__(kThreads) state_passing_kernel(Dims d, const f
 }  // namespace
 
 cudaError_t launch_state_passing(const Dims& d, bool bf16, const float* init, float* final_state,
-                                 const Work& w, cudaStream_t stream) {
+                                 const Work& w, cudaStream_t stream, bool dependent) {
   const int64_t total = static_cast<int64_t>(d.B) * d.H * d.P * d.N / (bf16 ? 8 : 4);
   const unsigned blocks = static_cast<unsigned>((total + kThreads - 1) / kThreads);
+  const float* cs = w.cumsum;
   if (bf16)
-    state_passing_kernel<true><<<blocks, kThreads, 0, stream>>>(d, w.cumsum, w.states, w.states_bf16, init,
-                                                                 final_state);
-  else
-    state_passing_kernel<false><<<blocks, kThreads, 0, stream>>>(d, w.cumsum, w.states, nullptr, init,
-                                                                  final_state);
-  return cudaGetLastError();
+    return launch_k(state_passing_kernel<true>, dim3(blocks), dim3(kThreads), 0, stream, dependent, d, cs, w.states,
+                    w.states_bf16, init, final_state);
+  return launch_k(state_passing_kernel<false>, dim3(blocks), dim3(kThreads), 0, stream, dependent, d, cs, w.states,
+                  static_cast<__nv_bfloat16*>(nullptr), init, final_state);
 }
 
 }  // namespace ssd
