@@ -430,9 +430,11 @@ ssd_status fwd_impl(int path, const ssd_shape* shape, const void* x, const float
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   const uint64_t spin = spin_limit_ns();
   cudaError_t e = launch_chunk_cumsum(d, dt, A, w, cs);
-  // each kernel after the first is a programmatic dependent of the one before it
+  // chunk_state and compute_out are programmatic dependents of the kernel before them (their
+  // launch and prologue overlap its tail).  state_passing is not: launched early, its blocks
+  // sit beside chunk_state's last wave, which measured slower on long sequences.
   if (e == cudaSuccess) e = launch_chunk_state(d, bf16, smaps, w, spin, cs, true);
-  if (e == cudaSuccess) e = launch_state_passing(d, bf16, init_state, final_state, w, cs, true);
+  if (e == cudaSuccess) e = launch_state_passing(d, bf16, init_state, final_state, w, cs, false);
   if (e == cudaSuccess) e = launch_compute_out(d, bf16, omaps, D, x, y, w, spin, cs, true);
   return from_cuda(e);
 }
