@@ -49,21 +49,23 @@
 // (A sequence whose window count is not a multiple of R ends in single-window
 // runs; each single-window run pays the global state round trip at both ends.)
 //
-// GB300 mapping, per CTA (one per SM, 384 threads, persistent):
-//   warp 10   claims runs from the counter and expands them into windows with
+// GB300 mapping, per CTA (one per SM, 512 threads, persistent):
+//   warp 2    claims runs from the counter and expands them into windows with
 //             their per-head scalars, in an 8-deep window ring.
 //   warp 0    issues TMA: the head pair's X window (double buffered) and a
 //             ring of 32 KB stages, each 128 dstate columns of C or B.  For
 //             dstate <= 128 the C stage stays resident until the
 //             carried-state product; for 256 C is loaded a second time.
 //   warp 1    owns tensor memory and issues every tcgen05.mma from one thread.
-//   warps 2-9 two warpgroups.  Per window: turn C B^T into the packed causal
-//             bf16 operand (in place, TMEM A side); advance the state and
-//             write the carried-state operand O; scale the NEXT window's X;
-//             write y over x in the X buffer.  Scaling one window ahead lets
-//             the tensor core run the next window's C B^T and state products
-//             while this window's epilogue runs.
-//   warp 11   stores y with TMA and hands the X buffer back to warp 0.
+//   warps 4-7 warpgroup A, per window: turns C B^T into the packed causal bf16
+//             operand (in place, TMEM A side; each thread owns whole rows, so
+//             no barrier is needed), then advances both heads' states and
+//             writes the carried-state operand O.
+//   warps 8-11, 12-15  warpgroups B and C, one per head, per window: scale the
+//             NEXT window's X (so the tensor core runs its C B^T and state
+//             products meanwhile) and write y over x in the X buffer.
+//   warp 3    stores y with TMA and hands the X buffer back to warp 0.
+// Warpgroup A works on window n + 1 while B and C finish window n.
 // The window state is accumulated transposed (TMEM lane = dstate index n,
 // columns = (head, p)), so a warp's loads and stores of the fp32 state are
 // 128-byte rows of consecutive n.  Tensor memory: C B^T [0, 128), output pair
@@ -76,7 +78,7 @@
 namespace ssd {
 namespace {
 
-constexpr int kThreads = 384;
+constexpr int kThreads = 512;
 constexpr int kTileRing = 8;
 constexpr float kSpan = 100.f;  // log2 bound on either side of the reference token
 constexpr uint32_t kColCB = 0, kColY = 128, kColD = 256, kColH = 384, kTmemCols = 512;
@@ -253,20 +255,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* full = bars;        // [4] stage ring
   uint64_t* empty = bars + 4;   // [4]
   uint64_t* xfull = bars + 8;   // [2] X window landed
-  uint64_t* xready = bars + 10; // [2] X scaled (256 arrivals)
+  uint64_t* xready = bars + 10; // [2] X scaled (warpgroups B and C: 256 arrivals)
   uint64_t* xempty = bars + 12; // [2] y stored from the buffer (store warp)
   uint64_t* ystaged = bars + 14;// [2] y written into the buffer (one arrival per warpgroup)
   uint64_t* tfull = bars + 16;  // [8] window ring
-  uint64_t* tempty = bars + 24; // [8] (258 arrivals: TMA, MMA and the warpgroups)
+  uint64_t* tempty = bars + 24; // [8] (386 arrivals: TMA, MMA and warpgroups A, B, C)
   uint64_t* cbfull = bars + 32; // C B^T accumulated
   uint64_t* dfull = bars + 33;  // window state accumulated
-  uint64_t* mready = bars + 34; // causal operand written (256)
-  uint64_t* cbfree = bars + 35; // C B^T columns reusable (256 + MMA commit)
-  uint64_t* dfree = bars + 36;  // window state drained (256)
-  uint64_t* oready = bars + 37; // carried-state operand in shared memory (256)
+  uint64_t* mready = bars + 34; // causal operand written (warpgroup A: 128)
+  uint64_t* cbfree = bars + 35; // C B^T columns reusable (128 + MMA commit)
+  uint64_t* dfree = bars + 36;  // window state drained (128)
+  uint64_t* oready = bars + 37; // carried-state operand in shared memory (128)
   uint64_t* ofree = bars + 38;  // carried-state products done
   uint64_t* yfull = bars + 39;  // all products of the window done
-  uint64_t* yfree = bars + 40;  // output accumulator drained (256)
+  uint64_t* yfree = bars + 40;  // output accumulator drained (warpgroups B and C: 256)
   TileInfo* info = reinterpret_cast<TileInfo*>(smem + L.info);
   int* coord = reinterpret_cast<int*>(smem + L.coord);  // [2][3]: batch, t0, h0 of the y in each buffer
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L.holder);
@@ -279,7 +281,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int s = 0; s < kTileRing; ++s) {
       mbar_init(&tfull[s], 1);
-      mbar_init(&tempty[s], 258);
+      mbar_init(&tempty[s], 386);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&xfull[s], 1);
@@ -289,10 +291,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(cbfull, 1);
     mbar_init(dfull, 1);
-    mbar_init(mready, 256);
-    mbar_init(cbfree, 257);
-    mbar_init(dfree, 256);
-    mbar_init(oready, 256);
+    mbar_init(mready, 128);
+    mbar_init(cbfree, 129);
+    mbar_init(dfree, 128);
+    mbar_init(oready, 128);
     mbar_init(ofree, 1);
     mbar_init(yfull, 1);
     mbar_init(yfree, 256);
@@ -315,7 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_holder;
   bool ok = true;
 
-  if (warp == 10) {
+  if (warp == 2) {
     // ------------------------------------------------------------ run scheduler
     // lane 0 claims a run; lanes 0 and 1 read the two heads' window scalars
     int n = 0;  // window ring position
@@ -370,7 +372,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
       }
     }
-  } else if (warp == 11) {
+  } else if (warp == 3) {
     // ------------------------------------------------------------ y stores
     if (lane == 0) {
       for (int n = 0; ok; ++n) {
@@ -535,20 +537,171 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(ofree);
       }
     }
-  } else {
-    // ------------------------------------------------------------ two warpgroups
-    const int wg = (warp - 2) >> 2;  // head of the pair for the per-head passes
-    const int et = threadIdx.x - 64 - 128 * wg;
+  } else if (warp < 8) {
+    // ------------------------------------------------------------ warpgroup A: causal operand, states
+    const int et = threadIdx.x - 128;  // 0..127
     const int quad = warp & 3;
-    const int r = quad * 32 + lane;  // TMEM lane: token row (output, C B^T) or dstate index (state)
+    const int r = quad * 32 + lane;  // TMEM lane: C B^T row, or dstate index of the state
     const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
-    const uint32_t bar_wg = 1 + wg, bar_all = 3;
+    constexpr uint32_t bar_a = 1;
+    for (int n = 0; ok; ++n) {
+      const int ts = n % kTileRing;
+      if (named_bar_or(bar_a, 128, !mbar_wait(&tfull[ts], (n / kTileRing) & 1, spin_ns))) {
+        ok = false;
+        break;
+      }
+      const int tile = info[ts].tile;
+      const bool fast = info[ts].fast != 0;
+      const bool first = info[ts].first != 0, last = info[ts].last != 0;
+      const float ge0 = info[ts].ge[0], ge1 = info[ts].ge[1];
+      mbar_arrive(&tempty[ts]);
+      if (tile < 0) break;
+      const Win W = decode(tile, d, S);
+
+      // 1. causal operand, packed in place over the first S/2 columns of C B^T.  A thread
+      //    reads its row's strips before it overwrites any of them, and rows are its own.
+      if (named_bar_or(bar_a, 128, !mbar_wait(cbfull, n & 1, spin_ns))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      if (fast) {
+#pragma unroll 1
+        for (int s0 = 0; s0 < S / 32; s0 += 2) {
+          uint32_t va[32], vb[32];
+          tmem_ld32(tmem + lane_base + kColCB + 32 * s0, va);
+          tmem_ld32(tmem + lane_base + kColCB + 32 * (s0 + 1), vb);
+          tmem_ld_wait();
+          causal_pack_store(va, 32 * s0, r, tmem + lane_base + kColCB + 16 * s0);
+          causal_pack_store(vb, 32 * (s0 + 1), r, tmem + lane_base + kColCB + 16 * (s0 + 1));
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(cbfree);
+      }
+      mbar_arrive(mready);
+
+      // 2. both heads' states.  Thread = dstate index n.  h_in is the run's running state
+      //    (tensor memory) or, for a run's first window, the predecessor's published state;
+      //    h_out = e (X^^T B) + e h_in goes back to tensor memory or, for a run's last window,
+      //    to the global slot and the flag.  O = h_in (the reference is the window start).
+      {
+        bool bad = !mbar_wait(dfull, n & 1, spin_ns) || (n > 0 && !mbar_wait(ofree, (n - 1) & 1, spin_ns));
+        if (first && W.w > 0 && et == 0) bad = bad || !wait_flag_geq(flags + W.b * hp + W.pair, W.w, spin_ns);
+        if (named_bar_or(bar_a, 128, bad)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll 1
+        for (int hd = 0; hd < 2; ++hd) {
+          const float ge = hd ? ge1 : ge0;
+          const float e_fac = fast_exp2(ge);
+          const float s_fac = fast ? e_fac : 1.f;
+          const int64_t hbase = (static_cast<int64_t>(W.b) * d.H + W.h0 + hd) * d.P * d.N;
+          float* hs = hslot + hbase;
+          const float* hin = first ? (W.w == 0 ? (init ? init + hbase : nullptr) : hs) : nullptr;
+          if (NH == 1) {
+            const int nn = r;
+            if (nn < d.N) {  // warp-uniform (N is a multiple of 64)
+              uint8_t* ocol = smem + L.obuf + (nn >> 6) * kAtomBytes + (nn & 7) * 2;
+              const int cchunk = (nn & 63) >> 3;
+              const uint32_t tD = tmem + lane_base + kColD + 64 * hd, tH = tmem + lane_base + kColH + 64 * hd;
+              if (first) {  // stage h_in (predecessor's state, init or zero) into tensor memory
+#pragma unroll 1
+                for (int pb = 0; pb < 2; ++pb) {
+                  uint32_t hv[32];
+                  const float* hp_in = hin ? hin + 32 * pb * d.N + nn : nullptr;
+#pragma unroll
+                  for (int q = 0; q < 32; ++q) hv[q] = hp_in ? __float_as_uint(__ldcg(hp_in + q * d.N)) : 0u;
+                  tmem_st32(tH + 32 * pb, hv);
+                }
+                tmem_st_wait();
+              }
+#pragma unroll 1
+              for (int pb = 0; pb < 4; ++pb) {
+                uint32_t hv[16], dv[16];
+                tmem_ld16(tD + 16 * pb, dv);
+                tmem_ld16(tH + 16 * pb, hv);
+                tmem_ld_wait();
+                const int row0 = 64 * hd + 16 * pb;
+#pragma unroll
+                for (int q = 0; q < 16; ++q) {
+                  const float hq = __uint_as_float(hv[q]);
+                  dv[q] = __float_as_uint(fmaf(s_fac, __uint_as_float(dv[q]), e_fac * hq));
+                  const int row = row0 + q;
+                  *reinterpret_cast<__nv_bfloat16*>(ocol + row * 128 + ((cchunk ^ (row & 7)) << 4)) =
+                      __float2bfloat16_rn(hq);
+                }
+                tmem_st16(tH + 16 * pb, dv);
+              }
+              tmem_st_wait();
+              if (last) {  // publish the run's state
+#pragma unroll 1
+                for (int pb = 0; pb < 2; ++pb) {
+                  uint32_t hv[32];
+                  tmem_ld32(tH + 32 * pb, hv);
+                  tmem_ld_wait();
+                  float* hp_out = hs + 32 * pb * d.N + nn;
+#pragma unroll
+                  for (int q = 0; q < 32; ++q) __stcg(hp_out + q * d.N, __uint_as_float(hv[q]));
+                }
+              }
+            }
+          } else {
+            // dstate 256 (runs of one window): h_in from global, h_out to global
+#pragma unroll 1
+            for (int hf = 0; hf < NH; ++hf) {
+              const int nn = 128 * hf + r;
+              uint8_t* ocol = smem + L.obuf + (nn >> 6) * kAtomBytes + (nn & 7) * 2;
+              const int cchunk = (nn & 63) >> 3;
+#pragma unroll 1
+              for (int pb = 0; pb < 4; ++pb) {
+                uint32_t hv[16], dv[16];
+                tmem_ld16(tmem + lane_base + kColD + 128 * hf + 64 * hd + 16 * pb, dv);
+                const float* hp_in = hin ? hin + 16 * pb * d.N + nn : nullptr;
+#pragma unroll
+                for (int q = 0; q < 16; ++q) hv[q] = hp_in ? __float_as_uint(__ldcg(hp_in + q * d.N)) : 0u;
+                tmem_ld_wait();
+                float* hp_out = hs + 16 * pb * d.N + nn;
+                const int row0 = 64 * hd + 16 * pb;
+#pragma unroll
+                for (int q = 0; q < 16; ++q) {
+                  const float hq = __uint_as_float(hv[q]);
+                  __stcg(hp_out + q * d.N, fmaf(s_fac, __uint_as_float(dv[q]), e_fac * hq));
+                  const int row = row0 + q;
+                  *reinterpret_cast<__nv_bfloat16*>(ocol + row * 128 + ((cchunk ^ (row & 7)) << 4)) =
+                      __float2bfloat16_rn(hq);
+                }
+              }
+            }
+          }
+        }
+        if (last) {
+          __threadfence();
+          named_bar_sync(bar_a, 128);
+          if (et == 0) st_release_gpu(flags + W.b * hp + W.pair, W.w + 1);
+        }
+        tc_fence_before();
+        mbar_arrive(dfree);
+        fence_proxy_async_smem();
+        mbar_arrive(oready);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ warpgroups B, C: X scaling, epilogue
+    const int hh = (warp - 8) >> 2;  // head of the pair
+    const int et = threadIdx.x - 256 - 128 * hh;
+    const int quad = warp & 3;
+    const int r = quad * 32 + lane;  // token row
+    const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+    const uint32_t bar_h = 2 + hh;
     const int rr = r < S ? r : S - 1;
 
     // next window from the ring; issues this thread's per-token loads.  False at the end.
     auto fetch = [&](int n, TileCtx& c) -> bool {
       const int ts = n % kTileRing;
-      if (!mbar_wait(&tfull[ts], (n / kTileRing) & 1, spin_ns)) {
+      if (named_bar_or(bar_h, 128, !mbar_wait(&tfull[ts], (n / kTileRing) & 1, spin_ns))) {
         ok = false;
         return false;
       }
@@ -556,26 +709,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       c.fast = info[ts].fast;
       c.first = info[ts].first;
       c.last = info[ts].last;
-      c.base = info[ts].base[wg];
-      c.gm = info[ts].gm[wg];
-      c.ge = info[ts].ge[wg];
+      c.base = info[ts].base[hh];
+      c.gm = info[ts].gm[hh];
+      c.ge = info[ts].ge[hh];
       mbar_arrive(&tempty[ts]);
       if (c.tile < 0) return false;
       const Win W = decode(c.tile, d, S);
-      const int64_t o = (static_cast<int64_t>(W.b) * d.H + W.h0 + wg) * d.Lp + W.t0 + rr;
+      const int64_t o = (static_cast<int64_t>(W.b) * d.H + W.h0 + hh) * d.Lp + W.t0 + rr;
       c.graw = cumsum[o];
       c.dt = r < S ? dt_t[o] : 0.f;
-      c.D = Dvec[W.h0 + wg];
+      c.D = Dvec[W.h0 + hh];
       return true;
     };
     // X^ = wfac * x for this warpgroup's head, in place (a 128-B row is one token)
     auto scale = [&](int n, const TileCtx& c) -> bool {
       const int buf = n & 1;
-      if (!mbar_wait(&xfull[buf], (n >> 1) & 1, spin_ns)) return false;
+      if (named_bar_or(bar_h, 128, !mbar_wait(&xfull[buf], (n >> 1) & 1, spin_ns))) return false;
       if (r < S) {
         const float gi = (c.graw - c.base) * kLog2e;
         const float wfac = fast_exp2((c.fast ? c.gm : c.ge) - gi) * c.dt;
-        uint4* row = reinterpret_cast<uint4*>(smem + L.xbuf + buf * kXBytes + wg * S * 128 + r * 128);
+        uint4* row = reinterpret_cast<uint4*>(smem + L.xbuf + buf * kXBytes + hh * S * 128 + r * 128);
         // step k touches 16-byte chunk k ^ (r & 7): the warp's 32 rows then spread over all banks
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
@@ -599,155 +752,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (; ok && cur.tile >= 0; ++n) {
       const Win W = decode(cur.tile, d, S);
       const bool fast = cur.fast != 0;
-      const int h = W.h0 + wg;
+      const int h = W.h0 + hh;
       const int buf = n & 1;
-      uint8_t* xb = smem + L.xbuf + buf * kXBytes + wg * S * 128;  // this head's X window
-      // the next window's scalars and per-token loads, in flight during this one
+      uint8_t* xb = smem + L.xbuf + buf * kXBytes + hh * S * 128;  // this head's X window
+      // the next window: scalars, per-token loads, and its X scaled now (its products then
+      // overlap this window's epilogue)
       TileCtx nxt;
       nxt.tile = -1;
       const bool more = fetch(n + 1, nxt);
       if (!ok) break;
-
-      // 1. causal operand, packed in place over the first S/2 columns of C B^T
-      // (timeouts are decided jointly before every 256-thread barrier, so no thread is left waiting there)
-      if (named_bar_or(bar_all, 256, !mbar_wait(cbfull, n & 1, spin_ns))) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      if (fast) {
-        const int nst = S / 64;  // strips of 32 columns per warpgroup
-        const int s0 = wg * nst;
-        uint32_t va[32], vb[32];
-        tmem_ld32(tmem + lane_base + kColCB + 32 * s0, va);
-        if (nst > 1) tmem_ld32(tmem + lane_base + kColCB + 32 * (s0 + 1), vb);
-        tmem_ld_wait();
-        named_bar_sync(bar_all, 256);  // all of C B^T is read before the packed operand overwrites it
-        causal_pack_store(va, 32 * s0, r, tmem + lane_base + kColCB + 16 * s0);
-        if (nst > 1) causal_pack_store(vb, 32 * (s0 + 1), r, tmem + lane_base + kColCB + 16 * (s0 + 1));
-        tmem_st_wait();
-        tc_fence_before();
-        mbar_arrive(cbfree);
-      }
-      mbar_arrive(mready);
-
-      // 2. state of this warpgroup's head.  Thread = dstate index n.  h_in is the
-      //    run's running state (tensor memory) or, for a run's first window, the
-      //    predecessor's published state; h_out goes back to tensor memory or, for
-      //    a run's last window, to the global slot and the flag.  O = o * h_in.
-      {
-        const float s_fac = fast ? fast_exp2(cur.ge - cur.gm) : 1.f;
-        const float e_fac = fast_exp2(cur.ge);
-        const float o_fac = fast ? fast_exp2(cur.gm) : 1.f;
-        const int64_t hbase = (static_cast<int64_t>(W.b) * d.H + h) * d.P * d.N;
-        float* hs = hslot + hbase;
-        const bool first = cur.first != 0, last = cur.last != 0;
-        const float* hin = first ? (W.w == 0 ? (init ? init + hbase : nullptr) : hs) : nullptr;
-        // the predecessor run has published its state (one poller, joint decision)
-        bool bad = !mbar_wait(dfull, n & 1, spin_ns) || (n > 0 && !mbar_wait(ofree, (n - 1) & 1, spin_ns));
-        if (first && W.w > 0 && wg == 0 && et == 0)
-          bad = bad || !wait_flag_geq(flags + W.b * hp + W.pair, W.w, spin_ns);
-        if (named_bar_or(bar_all, 256, bad)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        if (NH == 1) {
-          // dstate <= 128: the run's state lives in tensor memory next to the window state
-          const int nn = r;
-          const bool lane_ok = nn < d.N;  // warp-uniform (N is a multiple of 64)
-          uint8_t* ocol = smem + L.obuf + (nn >> 6) * kAtomBytes + (nn & 7) * 2;
-          const int cchunk = (nn & 63) >> 3;
-          const uint32_t tD = tmem + lane_base + kColD + 64 * wg, tH = tmem + lane_base + kColH + 64 * wg;
-          if (first && lane_ok) {  // stage h_in (predecessor's state, init or zero) into tensor memory
-#pragma unroll 1
-            for (int pb = 0; pb < 2; ++pb) {
-              uint32_t hv[32];
-              const float* hp_in = hin ? hin + 32 * pb * d.N + nn : nullptr;
-#pragma unroll
-              for (int q = 0; q < 32; ++q) hv[q] = hp_in ? __float_as_uint(__ldcg(hp_in + q * d.N)) : 0u;
-              tmem_st32(tH + 32 * pb, hv);
-            }
-            tmem_st_wait();
-          }
-          if (lane_ok) {
-#pragma unroll 1
-            for (int pb = 0; pb < 2; ++pb) {
-              uint32_t hv[32], dv[32];
-              tmem_ld32(tD + 32 * pb, dv);
-              tmem_ld32(tH + 32 * pb, hv);
-              tmem_ld_wait();
-              const int row0 = 64 * wg + 32 * pb;
-#pragma unroll
-              for (int q = 0; q < 32; ++q) {
-                const float hq = __uint_as_float(hv[q]);
-                dv[q] = __float_as_uint(fmaf(s_fac, __uint_as_float(dv[q]), e_fac * hq));
-                const int row = row0 + q;
-                *reinterpret_cast<__nv_bfloat16*>(ocol + row * 128 + ((cchunk ^ (row & 7)) << 4)) =
-                    __float2bfloat16_rn(o_fac * hq);
-              }
-              tmem_st32(tH + 32 * pb, dv);
-            }
-            tmem_st_wait();
-            if (last) {  // publish the run's state
-#pragma unroll 1
-              for (int pb = 0; pb < 2; ++pb) {
-                uint32_t hv[32];
-                tmem_ld32(tH + 32 * pb, hv);
-                tmem_ld_wait();
-                float* hp_out = hs + 32 * pb * d.N + nn;
-#pragma unroll
-                for (int q = 0; q < 32; ++q) __stcg(hp_out + q * d.N, __uint_as_float(hv[q]));
-              }
-            }
-          }
-        } else {
-          // dstate 256 (runs of one window): h_in from global, h_out to global
-#pragma unroll 1
-          for (int hf = 0; hf < NH; ++hf) {
-            const int nn = 128 * hf + r;
-            uint8_t* ocol = smem + L.obuf + (nn >> 6) * kAtomBytes + (nn & 7) * 2;
-            const int cchunk = (nn & 63) >> 3;
-#pragma unroll 1
-            for (int pb = 0; pb < 2; ++pb) {
-              uint32_t hv[32], dv[32];
-              tmem_ld32(tmem + lane_base + kColD + 128 * hf + 64 * wg + 32 * pb, dv);
-              const float* hp_in = hin ? hin + 32 * pb * d.N + nn : nullptr;
-#pragma unroll
-              for (int q = 0; q < 32; ++q) hv[q] = hp_in ? __float_as_uint(__ldcg(hp_in + q * d.N)) : 0u;
-              tmem_ld_wait();
-              float* hp_out = hs + 32 * pb * d.N + nn;
-              const int row0 = 64 * wg + 32 * pb;
-#pragma unroll
-              for (int q = 0; q < 32; ++q) {
-                const float hq = __uint_as_float(hv[q]);
-                __stcg(hp_out + q * d.N, fmaf(s_fac, __uint_as_float(dv[q]), e_fac * hq));
-                const int row = row0 + q;
-                *reinterpret_cast<__nv_bfloat16*>(ocol + row * 128 + ((cchunk ^ (row & 7)) << 4)) =
-                    __float2bfloat16_rn(o_fac * hq);
-              }
-            }
-          }
-        }
-        if (last) {
-          __threadfence();
-          named_bar_sync(bar_all, 256);
-          if (wg == 0 && et == 0) st_release_gpu(flags + W.b * hp + W.pair, W.w + 1);
-        }
-        tc_fence_before();
-        mbar_arrive(dfree);
-        fence_proxy_async_smem();
-        mbar_arrive(oready);
-      }
-
-      // 3. the next window's X (its products then overlap this window's epilogue)
       if (more && !scale(n + 1, nxt)) {
         ok = false;
         break;
       }
 
-      // 4. y = r_i * acc + D x_i, written over x in the X window; warp 11 stores it
-      if (named_bar_or(bar_wg, 128, !mbar_wait(yfull, n & 1, spin_ns))) {
+      // y = r_i * acc + D x_i, written over x in the X window; warp 3 stores it
+      if (named_bar_or(bar_h, 128, !mbar_wait(yfull, n & 1, spin_ns))) {
         ok = false;
         break;
       }
@@ -759,38 +779,42 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool in_seq = r < S && W.t0 + r < d.L;
       uint8_t* xr = xb + r * 128;
       if (fast) {
-        uint32_t ya[32], yb[32];
-        tmem_ld32(tmem + lane_base + kColY + 64 * wg, ya);
-        tmem_ld32(tmem + lane_base + kColY + 64 * wg + 32, yb);
-        tmem_ld_wait();
-        tc_fence_before();
-        mbar_arrive(yfree);
-        if (r < S) {
-          const float ri = fast_exp2(gi - cur.gm);
-          const float wfac = fast_exp2(cur.gm - gi) * dti;
-          // D x_i = (D / dt_i) r_i X^_i when X^_i = wfac x_i is well inside the normal range;
-          // otherwise (rare) x_i itself is copied over X^_i from global memory
-          float c = ri * Dh / dti;
-          if (!(wfac >= 0x1p-80f)) {
-            c = Dh;
+        const float ri = fast_exp2(gi - cur.gm);
+        const float wfac = fast_exp2(cur.gm - gi) * dti;
+        // D x_i = (D / dt_i) r_i X^_i when X^_i = wfac x_i is well inside the normal range;
+        // otherwise (rare) x_i itself is copied over X^_i from global memory
+        float c = ri * Dh / dti;
+        if (r < S && !(wfac >= 0x1p-80f)) {
+          c = Dh;
 #pragma unroll 1
-            for (int k = 0; k < 8; ++k)
-              *reinterpret_cast<uint4*>(xr + ((k ^ (r & 7)) << 4)) =
-                  in_seq ? __ldg(reinterpret_cast<const uint4*>(xg + xrow_g) + k) : make_uint4(0, 0, 0, 0);
+          for (int k = 0; k < 8; ++k)
+            *reinterpret_cast<uint4*>(xr + ((k ^ (r & 7)) << 4)) =
+                in_seq ? __ldg(reinterpret_cast<const uint4*>(xg + xrow_g) + k) : make_uint4(0, 0, 0, 0);
+        }
+        // two halves of 32 headdim columns each (bounds the live registers)
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          uint32_t ya[32];
+          tmem_ld32(tmem + lane_base + kColY + 64 * hh + 32 * half, ya);
+          tmem_ld_wait();
+          if (half == 1) {
+            tc_fence_before();
+            mbar_arrive(yfree);
           }
+          if (r < S) {
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            uint4* cp = reinterpret_cast<uint4*>(xr + ((k ^ (r & 7)) << 4));
-            uint4 v = *cp;
-            uint32_t* vw = reinterpret_cast<uint32_t*>(&v);
+            for (int k = 4 * half; k < 4 * half + 4; ++k) {
+              uint4* cp = reinterpret_cast<uint4*>(xr + ((k ^ (r & 7)) << 4));
+              uint4 v = *cp;
+              uint32_t* vw = reinterpret_cast<uint32_t*>(&v);
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int pi = 8 * k + 2 * e;
-              const float a0 = __uint_as_float(pi < 32 ? ya[pi] : yb[pi - 32]);
-              const float a1 = __uint_as_float(pi + 1 < 32 ? ya[pi + 1] : yb[pi + 1 - 32]);
-              vw[e] = pack_bf16x2(fmaf(c, bf16_lo(vw[e]), ri * a0), fmaf(c, bf16_hi(vw[e]), ri * a1));
+              for (int e = 0; e < 4; ++e) {
+                const int pi = 8 * k + 2 * e - 32 * half;
+                vw[e] = pack_bf16x2(fmaf(c, bf16_lo(vw[e]), ri * __uint_as_float(ya[pi])),
+                                    fmaf(c, bf16_hi(vw[e]), ri * __uint_as_float(ya[pi + 1])));
+              }
+              *cp = v;
             }
-            *cp = v;
           }
         }
       } else {
@@ -798,12 +822,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                           xr);
         tc_fence_before();
         mbar_arrive(yfree);
-        mbar_arrive(cbfree);
+        // C B^T is released once both heads have read it: each of the eight warps adds 16 of
+        // the 128 arrivals that warpgroup A gives on the rescaled path
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cnt(cbfree, 16);
       }
       fence_proxy_async_smem();
-      named_bar_sync(bar_wg, 128);
+      named_bar_sync(bar_h, 128);
       if (et == 0) {
-        if (wg == 0) {
+        if (hh == 0) {
           coord[3 * buf] = W.b;
           coord[3 * buf + 1] = W.t0;
           coord[3 * buf + 2] = W.h0;
@@ -815,7 +842,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // end marker for the store warp (both warpgroups arrive, as for a window)
     if (ok && et == 0) {
       const int buf = n & 1;
-      if (wg == 0) coord[3 * buf] = -1;
+      if (hh == 0) coord[3 * buf] = -1;
       mbar_arrive(&ystaged[buf]);
     }
   }
