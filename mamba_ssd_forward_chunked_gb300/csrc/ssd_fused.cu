@@ -40,7 +40,6 @@
 // progress: the look-back wait always ends.  Each tile does its state and
 // masking MMAs before it waits, so the wait overlaps the tensor core.
 //
-// GB300 mapping, per CTA (one per SM, 320 threads, persistent):
 // Runs: a claim is a run of up to R consecutive windows of one (batch, head
 // pair), processed in order by one CTA.  Inside a run the running state stays
 // in tensor memory; only the run's first window reads the predecessor's state
