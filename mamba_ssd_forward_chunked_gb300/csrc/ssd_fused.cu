@@ -617,22 +617,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tmem_st_wait();
               }
+              // 32 columns per TMEM round trip (both loads in flight before one wait)
 #pragma unroll 1
-              for (int pb = 0; pb < 4; ++pb) {
-                uint32_t hv[16], dv[16];
-                tmem_ld16(tD + 16 * pb, dv);
-                tmem_ld16(tH + 16 * pb, hv);
+              for (int pb = 0; pb < 2; ++pb) {
+                uint32_t hv[32], dv[32];
+                tmem_ld32(tD + 32 * pb, dv);
+                tmem_ld32(tH + 32 * pb, hv);
                 tmem_ld_wait();
-                const int row0 = 64 * hd + 16 * pb;
+                const int row0 = 64 * hd + 32 * pb;
 #pragma unroll
-                for (int q = 0; q < 16; ++q) {
+                for (int q = 0; q < 32; ++q) {
                   const float hq = __uint_as_float(hv[q]);
                   dv[q] = __float_as_uint(fmaf(s_fac, __uint_as_float(dv[q]), e_fac * hq));
                   const int row = row0 + q;
                   *reinterpret_cast<__nv_bfloat16*>(ocol + row * 128 + ((cchunk ^ (row & 7)) << 4)) =
                       __float2bfloat16_rn(hq);
                 }
-                tmem_st16(tH + 16 * pb, dv);
+                tmem_st32(tH + 32 * pb, dv);
               }
               tmem_st_wait();
               if (last) {  // publish the run's state
@@ -790,30 +791,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             *reinterpret_cast<uint4*>(xr + ((k ^ (r & 7)) << 4)) =
                 in_seq ? __ldg(reinterpret_cast<const uint4*>(xg + xrow_g) + k) : make_uint4(0, 0, 0, 0);
         }
-        // two halves of 32 headdim columns each (bounds the live registers)
+        // the head's 64 accumulator columns in one TMEM round trip
+        uint32_t ya[64];
+        tmem_ld32(tmem + lane_base + kColY + 64 * hh, *reinterpret_cast<uint32_t(*)[32]>(ya));
+        tmem_ld32(tmem + lane_base + kColY + 64 * hh + 32, *reinterpret_cast<uint32_t(*)[32]>(ya + 32));
+        tmem_ld_wait();
+        tc_fence_before();
+        mbar_arrive(yfree);
+        if (r < S) {
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          uint32_t ya[32];
-          tmem_ld32(tmem + lane_base + kColY + 64 * hh + 32 * half, ya);
-          tmem_ld_wait();
-          if (half == 1) {
-            tc_fence_before();
-            mbar_arrive(yfree);
-          }
-          if (r < S) {
+          for (int k = 0; k < 8; ++k) {
+            uint4* cp = reinterpret_cast<uint4*>(xr + ((k ^ (r & 7)) << 4));
+            uint4 v = *cp;
+            uint32_t* vw = reinterpret_cast<uint32_t*>(&v);
 #pragma unroll
-            for (int k = 4 * half; k < 4 * half + 4; ++k) {
-              uint4* cp = reinterpret_cast<uint4*>(xr + ((k ^ (r & 7)) << 4));
-              uint4 v = *cp;
-              uint32_t* vw = reinterpret_cast<uint32_t*>(&v);
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const int pi = 8 * k + 2 * e - 32 * half;
-                vw[e] = pack_bf16x2(fmaf(c, bf16_lo(vw[e]), ri * __uint_as_float(ya[pi])),
-                                    fmaf(c, bf16_hi(vw[e]), ri * __uint_as_float(ya[pi + 1])));
-              }
-              *cp = v;
+            for (int e = 0; e < 4; ++e) {
+              const int pi = 8 * k + 2 * e;
+              vw[e] = pack_bf16x2(fmaf(c, bf16_lo(vw[e]), ri * __uint_as_float(ya[pi])),
+                                  fmaf(c, bf16_hi(vw[e]), ri * __uint_as_float(ya[pi + 1])));
             }
+            *cp = v;
           }
         }
       } else {
