@@ -88,8 +88,10 @@ typedef struct {
  *   chain       int32 [1 + B*H/2]  one-pass kernel: tile counter, then per
  *               (batch, head pair) the number of windows whose state is
  *               published (cleared by chunk_cumsum)
- *   hslot       fp32 [B][H][P][N]  one-pass kernel: state after the last
- *               published window (used when final_state is NULL)
+ *   hslot       fp32, B*H*P*N values  one-pass kernel: the state handed from
+ *               one run of windows to the next, per head pair in a layout of
+ *               its own ([N/32][8][2*P rows][4]: a warp's 16-byte accesses are
+ *               consecutive)
  * nc = ceil(seqlen / chunk_size). */
 typedef struct {
   size_t status;

@@ -184,7 +184,7 @@ def workspace_views(shape: ssd_shape, ws: torch.Tensor) -> Dict[str, torch.Tenso
     if shape.dtype == SSD_BF16:
         out["states_bf16"] = view(L["states_bf16"], B * nc * H * P * N, torch.bfloat16, (B, nc, H, P, N))
     out["chain"] = view(L["chain"], 1 + B * (H // 2), torch.int32, (1 + B * (H // 2),))
-    out["hslot"] = view(L["hslot"], B * H * P * N, torch.float32, (B, H, P, N))
+    out["hslot"] = view(L["hslot"], B * H * P * N, torch.float32, (B * H * P * N,))
     return out
 
 

@@ -376,7 +376,7 @@ ssd_status ssd_fused_pass(const ssd_shape* shape, const void* x, const void* Bm,
   Work w = carve(workspace, L, true);
   FusedMaps fmaps;
   if (!build_fused_maps(*shape, x, Bm, Cm, y, &fmaps)) return SSD_ERR_CUDA;
-  return from_cuda(launch_fused(make_dims(*shape), fmaps, D, x, init_state, final_state ? final_state : w.hslot, w,
+  return from_cuda(launch_fused(make_dims(*shape), fmaps, D, x, init_state, final_state, w,
                                 spin_limit_ns(), reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -418,7 +418,7 @@ ssd_status fwd_impl(int path, const ssd_shape* shape, const void* x, const float
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e = launch_chunk_cumsum(d, dt, A, w, cs);
     if (e == cudaSuccess)
-      e = launch_fused(d, fmaps, D, x, init_state, final_state ? final_state : w.hslot, w, spin_limit_ns(), cs, true);
+      e = launch_fused(d, fmaps, D, x, init_state, final_state, w, spin_limit_ns(), cs, true);
     return from_cuda(e);
   }
   ChunkStateMaps smaps;

@@ -65,9 +65,10 @@
 //             products meanwhile) and write y over x in the X buffer.
 //   warp 3    stores y with TMA and hands the X buffer back to warp 0.
 // Warpgroup A works on window n + 1 while B and C finish window n.
-// The window state is accumulated transposed (TMEM lane = dstate index n,
-// columns = (head, p)), so a warp's loads and stores of the fp32 state are
-// 128-byte rows of consecutive n.  Tensor memory: C B^T [0, 128), output pair
+// The window state is accumulated with TMEM lane = row (head, p) of the pair
+// and columns = dstate, so a thread owns a state row: the carried-state
+// operand O is written in 16-byte chunks, and a run's boundary state moves as
+// 512-byte rows of global memory.  Tensor memory: C B^T [0, 128), output pair
 // accumulator [128, 256), window state [256, 384) (to 512 for dstate 256),
 // running state of the run [384, 512).  Every wait is bounded; on expiry the
 // CTA records SSD_ERR_DEVICE_TIMEOUT and winds down.
@@ -237,7 +238,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     ssd_fused_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap cmap,
                      const __grid_constant__ CUtensorMap bmap, const __grid_constant__ CUtensorMap ymap, Dims d,
                      int R, const float* __restrict__ cumsum, const float* __restrict__ dt_t,
-                     const float* __restrict__ Dvec, const float* init, float* hslot, int* flags, int* counter,
+                     const float* __restrict__ Dvec, const float* init, float* final_state, float* hslot,
+                     int* flags, int* counter,
                      const __nv_bfloat16* __restrict__ xg, int* status, uint64_t spin_ns) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -436,7 +438,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       const uint32_t id_cb = idesc_f32acc(1, 128, static_cast<uint32_t>(S), 0, 0);  // C B^T: both K-major
-      const uint32_t id_st = idesc_f32acc(1, 128, 128, 1, 1);  // state^T: B^T (MN-major) x X^ pair (MN-major)
+      const uint32_t id_st = idesc_f32acc(1, 128, d.N < 128 ? d.N : 128, 1, 1);  // state: X^ pair^T x B (MN/MN)
       const uint32_t id_in = idesc_f32acc(1, 128, 128, 0, 1);  // intra: causal operand (TMEM) x X^ pair
       const uint32_t id_yo = idesc_f32acc(1, 128, 128, 0, 0);  // carried state: C x O (both K-major)
       const uint32_t xlbo = static_cast<uint32_t>(S) * 128u;   // head stride in the X buffer
@@ -479,8 +481,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                           sdesc_sw128(sb + (k >> 2) * kAtomBytes + (k & 3) * 32, 16, 1024), id_cb,
                           (hf | k) != 0 ? 1u : 0u);
           for (int k = 0; k < S / 16; ++k)
-            mma_ss<false>(tmem + kColD + 128 * hf, sdesc_sw128(sb + k * 2048, kAtomBytes, 1024),
-                          sdesc_sw128(xb + k * 2048, xlbo, 1024), id_st, k != 0 ? 1u : 0u);
+            mma_ss<false>(tmem + kColD + 128 * hf, sdesc_sw128(xb + k * 2048, xlbo, 1024),
+                          sdesc_sw128(sb + k * 2048, kAtomBytes, 1024), id_st, k != 0 ? 1u : 0u);
           if (holdC) {
             held = sc;
             held_it = it;
@@ -580,10 +582,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       mbar_arrive(mready);
 
-      // 2. both heads' states.  Thread = dstate index n.  h_in is the run's running state
-      //    (tensor memory) or, for a run's first window, the predecessor's published state;
-      //    h_out = e (X^^T B) + e h_in goes back to tensor memory or, for a run's last window,
-      //    to the global slot and the flag.  O = h_in (the reference is the window start).
+      // 2. both heads' states.  Thread = row (head hd, p) of the pair, columns = dstate.  h_in
+      //    is the run's running state (tensor memory) or, for a run's first window, the
+      //    predecessor's published state; h_out = e (X^^T B) + e h_in goes back to tensor memory
+      //    or, for a run's last window, to the global slot and the flag.  O = h_in (the
+      //    reference is the window start), written as 16-byte row chunks.
       {
         bool bad = !mbar_wait(dfull, n & 1, spin_ns) || (n > 0 && !mbar_wait(ofree, (n - 1) & 1, spin_ns));
         if (first && W.w > 0 && et == 0) bad = bad || !wait_flag_geq(flags + W.b * hp + W.pair, W.w, spin_ns);
@@ -592,91 +595,73 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
+        const int hd = r >> 6, p = r & 63;  // warp-uniform head
+        const float ge = hd ? ge1 : ge0;
+        const float e_fac = fast_exp2(ge);
+        const float s_fac = fast ? e_fac : 1.f;
+        // A sequence's first window reads init and its last window writes final_state, both
+        // [B][H][P][N] (a thread's row is 512 contiguous bytes).  Between runs the state goes
+        // through the workspace slot laid out so that a warp's 16-byte accesses are
+        // consecutive: per head pair, [N/32][8][128 rows][4 floats].
+        const bool seq_first = W.w == 0, seq_last = W.w == nw - 1;
+        const int64_t hrow = ((static_cast<int64_t>(W.b) * d.H + W.h0 + hd) * d.P + p) * d.N;  // [B][H][P][N]
+        float4* slot = reinterpret_cast<float4*>(hslot + (static_cast<int64_t>(W.b) * hp + W.pair) * 128 * d.N) + r;
+        const float* hin = first && seq_first ? (init ? init + hrow : nullptr) : nullptr;
+        uint8_t* orow = smem + L.obuf + r * 128;  // this row of O in each 64-column atom
+        // keep: the running state stays in tensor memory (dstate <= 128, not the run's last window)
+        const bool keep = NH == 1 && !last;
 #pragma unroll 1
-        for (int hd = 0; hd < 2; ++hd) {
-          const float ge = hd ? ge1 : ge0;
-          const float e_fac = fast_exp2(ge);
-          const float s_fac = fast ? e_fac : 1.f;
-          const int64_t hbase = (static_cast<int64_t>(W.b) * d.H + W.h0 + hd) * d.P * d.N;
-          float* hs = hslot + hbase;
-          const float* hin = first ? (W.w == 0 ? (init ? init + hbase : nullptr) : hs) : nullptr;
-          if (NH == 1) {
-            const int nn = r;
-            if (nn < d.N) {  // warp-uniform (N is a multiple of 64)
-              uint8_t* ocol = smem + L.obuf + (nn >> 6) * kAtomBytes + (nn & 7) * 2;
-              const int cchunk = (nn & 63) >> 3;
-              const uint32_t tD = tmem + lane_base + kColD + 64 * hd, tH = tmem + lane_base + kColH + 64 * hd;
-              if (first) {  // stage h_in (predecessor's state, init or zero) into tensor memory
-#pragma unroll 1
-                for (int pb = 0; pb < 2; ++pb) {
-                  uint32_t hv[32];
-                  const float* hp_in = hin ? hin + 32 * pb * d.N + nn : nullptr;
+        for (int n0 = 0; n0 < d.N; n0 += 32) {
+          uint32_t hv[32], dv[32];
+          const uint32_t tD = tmem + lane_base + kColD + n0;  // dstate 256: the halves are adjacent
+          tmem_ld32(tD, dv);
+          if (first) {  // h_in from global memory (or zero)
 #pragma unroll
-                  for (int q = 0; q < 32; ++q) hv[q] = hp_in ? __float_as_uint(__ldcg(hp_in + q * d.N)) : 0u;
-                  tmem_st32(tH + 32 * pb, hv);
-                }
-                tmem_st_wait();
-              }
-              // 32 columns per TMEM round trip (both loads in flight before one wait)
-#pragma unroll 1
-              for (int pb = 0; pb < 2; ++pb) {
-                uint32_t hv[32], dv[32];
-                tmem_ld32(tD + 32 * pb, dv);
-                tmem_ld32(tH + 32 * pb, hv);
-                tmem_ld_wait();
-                const int row0 = 64 * hd + 32 * pb;
-#pragma unroll
-                for (int q = 0; q < 32; ++q) {
-                  const float hq = __uint_as_float(hv[q]);
-                  dv[q] = __float_as_uint(fmaf(s_fac, __uint_as_float(dv[q]), e_fac * hq));
-                  const int row = row0 + q;
-                  *reinterpret_cast<__nv_bfloat16*>(ocol + row * 128 + ((cchunk ^ (row & 7)) << 4)) =
-                      __float2bfloat16_rn(hq);
-                }
-                tmem_st32(tH + 32 * pb, dv);
-              }
-              tmem_st_wait();
-              if (last) {  // publish the run's state
-#pragma unroll 1
-                for (int pb = 0; pb < 2; ++pb) {
-                  uint32_t hv[32];
-                  tmem_ld32(tH + 32 * pb, hv);
-                  tmem_ld_wait();
-                  float* hp_out = hs + 32 * pb * d.N + nn;
-#pragma unroll
-                  for (int q = 0; q < 32; ++q) __stcg(hp_out + q * d.N, __uint_as_float(hv[q]));
-                }
-              }
+            for (int q = 0; q < 8; ++q) {
+              const float4 h4 = !seq_first ? __ldcg(slot + ((n0 >> 5) * 8 + q) * 128)
+                                : hin      ? __ldcg(reinterpret_cast<const float4*>(hin + n0) + q)
+                                           : make_float4(0.f, 0.f, 0.f, 0.f);
+              hv[4 * q] = __float_as_uint(h4.x);
+              hv[4 * q + 1] = __float_as_uint(h4.y);
+              hv[4 * q + 2] = __float_as_uint(h4.z);
+              hv[4 * q + 3] = __float_as_uint(h4.w);
             }
           } else {
-            // dstate 256 (runs of one window): h_in from global, h_out to global
-#pragma unroll 1
-            for (int hf = 0; hf < NH; ++hf) {
-              const int nn = 128 * hf + r;
-              uint8_t* ocol = smem + L.obuf + (nn >> 6) * kAtomBytes + (nn & 7) * 2;
-              const int cchunk = (nn & 63) >> 3;
-#pragma unroll 1
-              for (int pb = 0; pb < 4; ++pb) {
-                uint32_t hv[16], dv[16];
-                tmem_ld16(tmem + lane_base + kColD + 128 * hf + 64 * hd + 16 * pb, dv);
-                const float* hp_in = hin ? hin + 16 * pb * d.N + nn : nullptr;
+            tmem_ld32(tmem + lane_base + kColH + n0, hv);
+          }
+          tmem_ld_wait();
+          // O chunks: 8 bf16 per 16-byte chunk, chunk c of atom n0 / 64 at (c ^ (r & 7))
+          uint8_t* oat = orow + (n0 >> 6) * kAtomBytes;
 #pragma unroll
-                for (int q = 0; q < 16; ++q) hv[q] = hp_in ? __float_as_uint(__ldcg(hp_in + q * d.N)) : 0u;
-                tmem_ld_wait();
-                float* hp_out = hs + 16 * pb * d.N + nn;
-                const int row0 = 64 * hd + 16 * pb;
+          for (int c = 0; c < 4; ++c) {
+            uint4 o;
+            o.x = pack_bf16x2(__uint_as_float(hv[8 * c]), __uint_as_float(hv[8 * c + 1]));
+            o.y = pack_bf16x2(__uint_as_float(hv[8 * c + 2]), __uint_as_float(hv[8 * c + 3]));
+            o.z = pack_bf16x2(__uint_as_float(hv[8 * c + 4]), __uint_as_float(hv[8 * c + 5]));
+            o.w = pack_bf16x2(__uint_as_float(hv[8 * c + 6]), __uint_as_float(hv[8 * c + 7]));
+            const int cc = ((n0 & 63) >> 3) + c;
+            *reinterpret_cast<uint4*>(oat + ((cc ^ (r & 7)) << 4)) = o;
+          }
 #pragma unroll
-                for (int q = 0; q < 16; ++q) {
-                  const float hq = __uint_as_float(hv[q]);
-                  __stcg(hp_out + q * d.N, fmaf(s_fac, __uint_as_float(dv[q]), e_fac * hq));
-                  const int row = row0 + q;
-                  *reinterpret_cast<__nv_bfloat16*>(ocol + row * 128 + ((cchunk ^ (row & 7)) << 4)) =
-                      __float2bfloat16_rn(hq);
-                }
-              }
-            }
+          for (int q = 0; q < 32; ++q)
+            dv[q] = __float_as_uint(fmaf(s_fac, __uint_as_float(dv[q]), e_fac * __uint_as_float(hv[q])));
+          if (keep) {
+            tmem_st32(tmem + lane_base + kColH + n0, dv);
+          } else if (!seq_last) {  // publish for the next run
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              __stcg(slot + ((n0 >> 5) * 8 + q) * 128,
+                     make_float4(__uint_as_float(dv[4 * q]), __uint_as_float(dv[4 * q + 1]),
+                                 __uint_as_float(dv[4 * q + 2]), __uint_as_float(dv[4 * q + 3])));
+          } else if (final_state) {
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              reinterpret_cast<float4*>(final_state + hrow + n0)[q] =
+                  make_float4(__uint_as_float(dv[4 * q]), __uint_as_float(dv[4 * q + 1]),
+                              __uint_as_float(dv[4 * q + 2]), __uint_as_float(dv[4 * q + 3]));
           }
         }
+        if (keep) tmem_st_wait();
         if (last) {
           __threadfence();
           named_bar_sync(bar_a, 128);
@@ -857,7 +842,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 size_t fused_smem_bytes(const Dims& d) { return fused_smem_layout(d.N).total + 1024; }
 
 cudaError_t launch_fused(const Dims& d, const FusedMaps& maps, const float* D, const void* x, const float* init,
-                         float* hslot, const Work& w, uint64_t spin_ns, cudaStream_t stream, bool dependent) {
+                         float* final_state, const Work& w, uint64_t spin_ns, cudaStream_t stream, bool dependent) {
   const int S = d.Q < 128 ? d.Q : 128;
   const int R = d.N <= 128 ? 4 : 1;  // windows per run (the running state needs 128 spare TMEM columns)
   const int nw = d.Lp / S;
@@ -871,7 +856,7 @@ cudaError_t launch_fused(const Dims& d, const FusedMaps& maps, const float* D, c
   if (e != cudaSuccess) return e;
   const int grid = ntiles < sms ? ntiles : sms;
   return launch_k(ssd_fused_kernel, dim3(grid), dim3(kThreads), smem, stream, dependent, maps.x, maps.cm, maps.bm,
-                  maps.y, d, R, static_cast<const float*>(w.cumsum), static_cast<const float*>(w.dt_t), D, init, hslot,
+                  maps.y, d, R, static_cast<const float*>(w.cumsum), static_cast<const float*>(w.dt_t), D, init, final_state, w.hslot,
                   w.flags, w.counter, static_cast<const __nv_bfloat16*>(x), w.status, spin_ns);
 }
 

@@ -28,7 +28,7 @@ struct Work {
   __nv_bfloat16* states_bf16;  // [B][nc][H][P][N] or null (fp32 problems)
   int* counter;                // one-pass kernel: tile counter
   int* flags;                  // one-pass kernel: [B][H/2] windows published
-  float* hslot;                // one-pass kernel: running state [B][H][P][N]
+  float* hslot;                // one-pass kernel: states at run boundaries (its own layout)
 };
 
 // Tensor maps built on the host for one call.
@@ -83,7 +83,8 @@ cudaError_t launch_compute_out(const Dims& d, bool bf16, const ComputeOutMaps& m
                                bool dependent = false);
 size_t fused_smem_bytes(const Dims& d);
 cudaError_t launch_fused(const Dims& d, const FusedMaps& maps, const float* D, const void* x, const float* init,
-                         float* hslot, const Work& w, uint64_t spin_ns, cudaStream_t stream, bool dependent = false);
+                         float* final_state, const Work& w, uint64_t spin_ns, cudaStream_t stream,
+                         bool dependent = false);
 cudaError_t launch_timeout_probe(int* status, uint64_t limit_ns, cudaStream_t stream);
 
 }  // namespace ssd
