@@ -400,13 +400,15 @@ __global__ void __launch_bounds__(OutCfg<T>::kThreads, 1)
       }
       pD = Dvec[h];
     };
-    if (static_cast<int>(blockIdx.x) < ntiles) prefetch(blockIdx.x);
-    int xit = 0, ncb = 0, nm = 0, ntd = 0;
-    const uint8_t* xlast = nullptr;  // X block (this head, last column block) read by the epilogue
-    int xs_last = 0;
-    for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x, ++ntd) {
+    // per-tile scalars of this warpgroup's head, set up from the prefetched column data
+    struct TileVars {
+      float Dh, gm, Gi, dti;
+      bool fast;
+    };
+    // writes the tile's gs / dts / vref and issues the next tile's prefetch; runs while the
+    // previous tile's last products are on the tensor core (its epilogue needs none of them)
+    auto setup = [&](int tile) -> TileVars {
       const TileId id = decode_tile(tile, d, ntile);
-      const int h = id.h0 + hh;
       const int i = id.t * 128 + r;  // row within the chunk
       const int ncol = 128 * (id.t + 1);
       named_bar_sync(bar_id, 128);  // the previous tile's readers of gs / dts / vref are done
@@ -418,20 +420,39 @@ __global__ void __launch_bounds__(OutCfg<T>::kThreads, 1)
           dts[j] = pd[k];
         }
       }
-      const float Dh = pD;
+      TileVars v;
+      v.Dh = pD;
       // rescaled form for the whole pair while the diagonal block's decay stays within 2^kSpan
       // (G is non-increasing: every other factor of the form is <= 1)
-      bool fast = true;
+      v.fast = true;
 #pragma unroll
-      for (int k = 0; k < 2; ++k) fast = fast && ((pm[k] - pl[k]) * kLog2e <= kSpan);
-      const float gm = pm[hh] * kLog2e;  // this head's reference, log2 units
+      for (int k = 0; k < 2; ++k) v.fast = v.fast && ((pm[k] - pl[k]) * kLog2e <= kSpan);
+      v.gm = pm[hh] * kLog2e;  // this head's reference, log2 units
       if (tile + static_cast<int>(gridDim.x) < ntiles) prefetch(tile + gridDim.x);  // in flight during this tile
       named_bar_sync(bar_id, 128);
       // fast: vref[j] = 2^(G_m - G_j) dt_j, the row scale of X; exact form: strip factors
       for (int j = et; j < ncol; j += 128)
-        vref[j] = fast_exp2((fast ? gm : gs[j | 31]) - gs[j]) * dts[j];
+        vref[j] = fast_exp2((v.fast ? v.gm : gs[j | 31]) - gs[j]) * dts[j];
       named_bar_sync(bar_id, 128);
-      const float Gi = gs[i];
+      v.Gi = gs[i];
+      v.dti = i < 256 ? dts[i] : 0.f;
+      return v;
+    };
+    TileVars nxt{};
+    if (static_cast<int>(blockIdx.x) < ntiles) {
+      prefetch(blockIdx.x);
+      nxt = setup(blockIdx.x);
+    }
+    int xit = 0, ncb = 0, nm = 0, ntd = 0;
+    const uint8_t* xlast = nullptr;  // X block (this head, last column block) read by the epilogue
+    int xs_last = 0;
+    for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x, ++ntd) {
+      const TileId id = decode_tile(tile, d, ntile);
+      const int h = id.h0 + hh;
+      const int i = id.t * 128 + r;  // row within the chunk
+      const TileVars cur = nxt;
+      const float Dh = cur.Dh, gm = cur.gm, Gi = cur.Gi;
+      const bool fast = cur.fast;
 
       for (int jb = 0; jb <= id.t; ++jb) {
         if (!mbar_wait(cbfull, ncb & 1, spin_ns)) {
@@ -557,6 +578,7 @@ __global__ void __launch_bounds__(OutCfg<T>::kThreads, 1)
         }
       }
       if (!ok) break;
+      if (tile + static_cast<int>(gridDim.x) < ntiles) nxt = setup(tile + gridDim.x);
 
       // epilogue: y_i = Y_h[i] + D_h x_i, written over x in the X block and
       // stored with TMA (rows past Q are not stored; TMA clips rows past L)
@@ -576,7 +598,7 @@ __global__ void __launch_bounds__(OutCfg<T>::kThreads, 1)
       // is well inside the normal range; otherwise x_i is copied back over X^_i from global memory
       float ry = 1.f, kx = Dh;
       if (fast) {
-        const float dti = dts[i];
+        const float dti = cur.dti;
         const float wi = fast_exp2(gm - Gi) * dti;
         ry = fast_exp2(Gi - gm);
         if (wi >= 0x1p-80f) {
