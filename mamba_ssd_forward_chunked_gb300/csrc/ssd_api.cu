@@ -431,10 +431,13 @@ ssd_status fwd_impl(int path, const ssd_shape* shape, const void* x, const float
   const uint64_t spin = spin_limit_ns();
   cudaError_t e = launch_chunk_cumsum(d, dt, A, w, cs);
   // chunk_state and compute_out are programmatic dependents of the kernel before them (their
-  // launch and prologue overlap its tail).  state_passing is not: launched early, its blocks
-  // sit beside chunk_state's last wave, which measured slower on long sequences.
+  // launch and prologue overlap its tail).  state_passing is one only while chunk_state runs
+  // in a single wave (two CTAs per SM): launched early beside a later wave, its blocks slowed
+  // long sequences (16k tokens x dstate 256: 0.397 against 0.381 ms), while on a one-wave
+  // problem the early launch saves about 1 us (370M layer: 0.0897 against 0.0908 ms).
+  const bool one_wave = static_cast<int64_t>(d.B) * d.nc * (d.H / 2) <= 2 * static_cast<int64_t>(sm_count());
   if (e == cudaSuccess) e = launch_chunk_state(d, bf16, smaps, w, spin, cs, true);
-  if (e == cudaSuccess) e = launch_state_passing(d, bf16, init_state, final_state, w, cs, false);
+  if (e == cudaSuccess) e = launch_state_passing(d, bf16, init_state, final_state, w, cs, one_wave);
   if (e == cudaSuccess) e = launch_compute_out(d, bf16, omaps, D, x, y, w, spin, cs, true);
   return from_cuda(e);
 }
