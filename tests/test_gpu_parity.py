@@ -185,6 +185,28 @@ def test_host_buffers_end_to_end():
     assert rel_err(y.float().numpy(), yr) <= TOL["bf16"] and rel_err(f.numpy(), fr) <= TOL["bf16"]
 
 
+@pytest.mark.parametrize("batch,pieces", [(3, None), (3, 2), (4, 4)])
+def test_host_buffers_pipelined_over_batch(batch, pieces):
+    """The host entry point splits the batch into slices whose copies and
+    kernels overlap; every slice must still match the oracle (uneven slices
+    included), and the result must not depend on the split."""
+    import mamba_ssd_forward_chunked_gb300 as ssd
+    w = ssd_synth.custom("hp", batch=batch, seqlen=300, nheads=4, dstate=64, chunk_size=128, dtype="bf16",
+                         init_state=True)
+    inp = ssd_synth.make_inputs(w)
+    h = {k: torch.from_numpy(v).pin_memory() for k, v in inp.items()}
+    for k in ("x", "Bm", "Cm"):
+        h[k] = h[k].to(torch.bfloat16).pin_memory()
+    y, f = ssd.ssd_fwd_host(h["x"], h["dt"], h["A"], h["Bm"], h["Cm"], h["D"], 128, init_state=h["init"],
+                            pieces=pieces)
+    y1, f1 = ssd.ssd_fwd_host(h["x"], h["dt"], h["A"], h["Bm"], h["Cm"], h["D"], 128, init_state=h["init"],
+                              pieces=1)
+    torch.cuda.synchronize()
+    yr, fr, _ = oracle.recurrence(inp)
+    assert rel_err(y.float().numpy(), yr) <= TOL["bf16"] and rel_err(f.numpy(), fr) <= TOL["bf16"]
+    assert torch.equal(y, y1) and torch.equal(f, f1)
+
+
 def test_argument_errors_raise():
     import mamba_ssd_forward_chunked_gb300 as ssd
     x = torch.randn(1, 64, 4, 32, device="cuda")  # headdim 32: unsupported
