@@ -292,13 +292,16 @@ def ssd_fwd_host(x, dt, A, Bm, Cm, D, chunk_size: int, init_state=None, device="
     tensors.  Inputs are CPU tensors (pinned for asynchronous copies).
     Returns (y_host, final_host); synchronise the stream before reading them.
 
-    Batch entries are independent problems, so the call is pipelined over
-    ``pieces`` batch slices (default: one per ~16 MB moved, at most 4): slice k + 1's inputs are copied
-    in on one side stream while slice k runs on ``stream`` and slice k - 1's
-    outputs are copied out on another, so the two copy directions and the
-    kernels overlap.  Everything is ordered after the work already on
-    ``stream`` and before the work queued on it later.  Each slice picks its
-    schedule from its own shape (as ssd_fwd does)."""
+    The call is pipelined over ``pieces`` slices (default: one per ~16 MB
+    moved, at most 4): slice k + 1's inputs are copied in on one side stream
+    while slice k runs on ``stream`` and slice k - 1's outputs are copied out
+    on another, so the two copy directions and the kernels overlap.  Slices are
+    batch ranges (independent problems); a batch of one is cut along the
+    sequence at chunk boundaries instead, each segment starting from the
+    previous one's final state (the recurrence resumed, so the chunking is
+    unchanged).  Everything is ordered after the work already on ``stream``
+    and before the work queued on it later.  Each slice picks its schedule
+    from its own shape (as ssd_fwd does)."""
     dev = torch.device(device)
     if dev.index is None:
         dev = torch.device("cuda", torch.cuda.current_device())
@@ -311,8 +314,17 @@ def ssd_fwd_host(x, dt, A, Bm, Cm, D, chunk_size: int, init_state=None, device="
         # layer, 370 MB: 1.55 ms in four against 2.14 in one); small problems stay in one
         moved = sum(t.numel() * t.element_size() for t in (x, dt, Bm, Cm)) * 2
         pieces = max(1, min(4, moved // (16 << 20)))
-    n = max(1, min(B, int(pieces)))
-    bounds = [(B * k) // n for k in range(n + 1)]
+    pieces = max(1, int(pieces))
+    if B > 1 or pieces == 1:
+        n = min(B, pieces)
+        cuts = [(B * k) // n for k in range(n + 1)]
+        slices = [(cuts[k], cuts[k + 1], 0, L) for k in range(n)]
+    else:  # one sequence: segments of whole chunks
+        nc = -(-L // chunk_size)
+        n = min(nc, pieces)
+        cuts = [min(L, ((nc * k) // n) * chunk_size) for k in range(n + 1)]
+        slices = [(0, 1, cuts[k], cuts[k + 1]) for k in range(n)]
+    seq_split = slices[0][3] - slices[0][2] < L
     if out_y is None:
         out_y = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
     if out_final is None:
@@ -323,10 +335,11 @@ def ssd_fwd_host(x, dt, A, Bm, Cm, D, chunk_size: int, init_state=None, device="
         Ad, Dd = torch.empty(A.shape, dtype=A.dtype, device=dev), torch.empty(D.shape, dtype=D.dtype, device=dev)
         hd = torch.empty(init_state.shape, dtype=init_state.dtype, device=dev) if init_state is not None else None
         yd = torch.empty(x.shape, dtype=x.dtype, device=dev)
-        fd = torch.empty((B, H, P, N), dtype=torch.float32, device=dev)
+        fd = torch.empty((2 if seq_split else 1, B, H, P, N), dtype=torch.float32, device=dev)
         if workspace is None:
-            bmax = max(bounds[k + 1] - bounds[k] for k in range(n))
-            workspace = new_workspace(shape_of(xd[:bmax], Bd[:bmax], chunk_size), dev)
+            bmax = max(b1 - b0 for b0, b1, _, _ in slices)
+            lmax = max(l1 - l0 for _, _, l0, l1 in slices)
+            workspace = new_workspace(shape_of(xd[:bmax, :lmax], Bd[:bmax, :lmax], chunk_size), dev)
     cin, cout = _copy_streams(dev)
     cin.wait_stream(st)
     cout.wait_stream(st)
@@ -334,25 +347,33 @@ def ssd_fwd_host(x, dt, A, Bm, Cm, D, chunk_size: int, init_state=None, device="
     with torch.cuda.stream(cin):
         Ad.copy_(A, non_blocking=True)
         Dd.copy_(D, non_blocking=True)
-        for k in range(n):
-            b0, b1 = bounds[k], bounds[k + 1]
-            for dst, src in ((xd, x), (dtd, dt), (Bd, Bm), (Cd, Cm)) + (((hd, init_state),) if hd is not None else ()):
-                dst[b0:b1].copy_(src[b0:b1], non_blocking=True)
+        if hd is not None:
+            hd.copy_(init_state, non_blocking=True)
+        for b0, b1, l0, l1 in slices:
+            for dst, src in ((xd, x), (dtd, dt), (Bd, Bm), (Cd, Cm)):
+                dst[b0:b1, l0:l1].copy_(src[b0:b1, l0:l1], non_blocking=True)
             e = torch.cuda.Event()
             e.record(cin)
             ev_in.append(e)
-    for k in range(n):
-        b0, b1 = bounds[k], bounds[k + 1]
+    for k, (b0, b1, l0, l1) in enumerate(slices):
         st.wait_event(ev_in[k])
-        ssd_fwd(xd[b0:b1], dtd[b0:b1], Ad, Bd[b0:b1], Cd[b0:b1], Dd, chunk_size,
-                init_state=hd[b0:b1] if hd is not None else None, y=yd[b0:b1], final_state=fd[b0:b1],
-                workspace=workspace, stream=st)
+        if seq_split:  # segment k resumes from segment k - 1's final state
+            h_in = hd if k == 0 else fd[(k - 1) % 2]
+            fin = fd[k % 2]
+        else:
+            h_in = hd[b0:b1] if hd is not None else None
+            fin = fd[0, b0:b1]
+        ssd_fwd(xd[b0:b1, l0:l1], dtd[b0:b1, l0:l1], Ad, Bd[b0:b1, l0:l1], Cd[b0:b1, l0:l1], Dd, chunk_size,
+                init_state=h_in, y=yd[b0:b1, l0:l1], final_state=fin, workspace=workspace, stream=st)
         e = torch.cuda.Event()
         e.record(st)
         cout.wait_event(e)
         with torch.cuda.stream(cout):
-            out_y[b0:b1].copy_(yd[b0:b1], non_blocking=True)
-            out_final[b0:b1].copy_(fd[b0:b1], non_blocking=True)
+            out_y[b0:b1, l0:l1].copy_(yd[b0:b1, l0:l1], non_blocking=True)
+            if not seq_split:
+                out_final[b0:b1].copy_(fin, non_blocking=True)
+            elif k == len(slices) - 1:
+                out_final.copy_(fin, non_blocking=True)
     st.wait_stream(cout)
     return out_y, out_final
 

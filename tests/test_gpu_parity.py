@@ -185,13 +185,17 @@ def test_host_buffers_end_to_end():
     assert rel_err(y.float().numpy(), yr) <= TOL["bf16"] and rel_err(f.numpy(), fr) <= TOL["bf16"]
 
 
-@pytest.mark.parametrize("batch,pieces", [(3, None), (3, 2), (4, 4)])
-def test_host_buffers_pipelined_over_batch(batch, pieces):
-    """The host entry point splits the batch into slices whose copies and
-    kernels overlap; every slice must still match the oracle (uneven slices
-    included), and the result must not depend on the split."""
+@pytest.mark.parametrize("batch,seqlen,pieces", [(3, 300, None), (3, 300, 2), (4, 300, 4), (1, 700, 3),
+                                                 (1, 700, 8)])
+def test_host_buffers_pipelined(batch, seqlen, pieces):
+    """The host entry point splits the work into slices whose copies and
+    kernels overlap: batch ranges, or for one sequence, segments of whole
+    chunks resumed from each other's final state.  Every slice must still
+    match the oracle (uneven slices and a ragged last segment included), and
+    the result must not depend on the split (bitwise for batch ranges, within
+    rounding for segments)."""
     import mamba_ssd_forward_chunked_gb300 as ssd
-    w = ssd_synth.custom("hp", batch=batch, seqlen=300, nheads=4, dstate=64, chunk_size=128, dtype="bf16",
+    w = ssd_synth.custom("hp", batch=batch, seqlen=seqlen, nheads=4, dstate=64, chunk_size=128, dtype="bf16",
                          init_state=True)
     inp = ssd_synth.make_inputs(w)
     h = {k: torch.from_numpy(v).pin_memory() for k, v in inp.items()}
@@ -204,7 +208,11 @@ def test_host_buffers_pipelined_over_batch(batch, pieces):
     torch.cuda.synchronize()
     yr, fr, _ = oracle.recurrence(inp)
     assert rel_err(y.float().numpy(), yr) <= TOL["bf16"] and rel_err(f.numpy(), fr) <= TOL["bf16"]
-    assert torch.equal(y, y1) and torch.equal(f, f1)
+    if batch > 1:
+        assert torch.equal(y, y1) and torch.equal(f, f1)
+    else:
+        assert rel_err(y.float().numpy(), y1.float().numpy()) <= 1e-2
+        assert rel_err(f.numpy(), f1.numpy()) <= 1e-2
 
 
 def test_argument_errors_raise():
