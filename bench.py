@@ -366,7 +366,7 @@ def run_gpu(args, w: ssd_synth.Workload, rank: int, world: int, local_rank: int)
                           "hbm_peak_gbs": pk["hbm_gbs"], "peak_source": pk["source"]},
         "roofline": roof,
         "kernels_ms": per_kernel,
-        "gpu_launches": len(names) * args.steps,
+        "gpu_launches": ssd.ssd_fwd_kernel_count(shape) * args.steps,
         "schedule": "one-pass" if fused else "staged",
         "e2e": {"value": whole_job_tokens_per_s(w.tokens, world, ms_e2e), "unit": "tokens/s", "ms_per_step": ms_e2e,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},

@@ -92,7 +92,13 @@ typedef struct {
  *               one run of windows to the next, per head pair in a layout of
  *               its own ([N/32][8][2*P rows][4]: a warp's 16-byte accesses are
  *               consecutive)
- * nc = ceil(seqlen / chunk_size). */
+ *   bT          (SSD_F32 only) fp32, B*G*Lp*N values: Bm in 4 KB boxes of 32
+ *               tokens x 32 dstate, transposed (a row is one dstate index),
+ *               rounded to TF32 and 128-byte swizzled -- the K-major operand
+ *               layout chunk_state's tensor cores read -- as
+ *               [B][G][Lp/32][N/32][box]; written once per call and shared by
+ *               every head of the group
+ * nc = ceil(seqlen / chunk_size), Lp = nc * chunk_size. */
 typedef struct {
   size_t status;
   size_t cumsum;
@@ -101,6 +107,7 @@ typedef struct {
   size_t states_bf16;
   size_t chain;
   size_t hslot;
+  size_t bT;
   size_t total;
 } ssd_workspace_layout;
 
@@ -123,7 +130,9 @@ size_t ssd_fwd_workspace_size(const ssd_shape* shape);
  *    computes each window's state on the tensor core, chains the states
  *    between windows through the workspace (or final_state), and writes y;
  *    x, Bm and Cm are read once.  SSD_BF16 only.
- *  - staged: chunk_cumsum, chunk_state, state_passing and compute_out.
+ *  - staged: chunk_cumsum, chunk_state, state_passing and compute_out
+ *    (SSD_F32: preceded by one transpose of Bm into the workspace, shared by
+ *    every head of a group).
  * ssd_fwd takes the one-pass schedule for SSD_BF16 when dstate <= 128 and
  * there are at least as many (batch, head pair) sequences as multiprocessors
  * (below that the chain of windows, not bandwidth, bounds the one-pass kernel);

@@ -46,7 +46,7 @@ class ssd_shape(ctypes.Structure):
 class ssd_workspace_layout(ctypes.Structure):
     _fields_ = [("status", ctypes.c_size_t), ("cumsum", ctypes.c_size_t), ("dt_t", ctypes.c_size_t),
                 ("states", ctypes.c_size_t), ("states_bf16", ctypes.c_size_t), ("chain", ctypes.c_size_t),
-                ("hslot", ctypes.c_size_t), ("total", ctypes.c_size_t)]
+                ("hslot", ctypes.c_size_t), ("bT", ctypes.c_size_t), ("total", ctypes.c_size_t)]
 
 
 class SSDError(RuntimeError):

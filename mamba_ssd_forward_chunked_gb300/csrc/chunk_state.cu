@@ -58,6 +58,33 @@ __host__ __device__ inline uint32_t state_stage_bytes(int N, int atom, int box, 
   return static_cast<uint32_t>(abytes + (N / atom) * box);
 }
 
+// fp32 problems: Bm in the K-major TF32 box layout, once per (batch, group).
+// Every head of a group multiplies by the same B, so its transpose (and TF32
+// rounding) is done here once instead of in each head pair's CTA.  One CTA per
+// (32-token stage, batch * group); thread (a, e) of a box writes the 16-byte
+// chunk holding tokens 4a..4a+3 of dstate row e, reading those four tokens'
+// values of column e (coalesced along e).  Tokens past L read as 0.
+constexpr int kBtThreads = 256;
+
+__global__ void __launch_bounds__(kBtThreads) b_transpose_kernel(Dims d, const float* __restrict__ Bm,
+                                                                  float* __restrict__ bT) {
+  const int stage = blockIdx.x;          // 32-token stage of the padded sequence
+  const int bg = blockIdx.y;             // batch * G + group
+  const int b = bg / d.G, g = bg % d.G;
+  const int a = threadIdx.x >> 5, e = threadIdx.x & 31;
+  const int nbox = d.N / 32;
+  uint8_t* out = reinterpret_cast<uint8_t*>(bT) + (static_cast<int64_t>(bg) * (d.Lp / 32) + stage) * nbox * 4096;
+  for (int k = 0; k < nbox; ++k) {
+    float v[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int tok = stage * 32 + 4 * a + q;
+      v[q] = tok < d.L ? round_tf32(Bm[((static_cast<int64_t>(b) * d.L + tok) * d.G + g) * d.N + k * 32 + e]) : 0.f;
+    }
+    *reinterpret_cast<float4*>(out + k * 4096 + box_t_offset(4 * a, e)) = make_float4(v[0], v[1], v[2], v[3]);
+  }
+}
+
 // Stages that fit the ring budget (2..4).
 __host__ __device__ inline int state_stages(uint32_t stage_bytes, int ring_bytes, int max_stages) {
   const int n = ring_bytes / static_cast<int>(stage_bytes);
@@ -68,7 +95,8 @@ template <typename T>
 __global__ void __launch_bounds__(StateCfg<T>::kThreads, 2)
     chunk_state_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap bmap,
                        const __grid_constant__ CUtensorMap smap, Dims d, const float* __restrict__ cumsum,
-                       const float* __restrict__ dt_t, int* status, uint64_t spin_ns) {
+                       const float* __restrict__ dt_t, const float* __restrict__ bT, int* status,
+                       uint64_t spin_ns) {
   using C = StateCfg<T>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -138,8 +166,14 @@ __global__ void __launch_bounds__(StateCfg<T>::kThreads, 2)
         const int tok = c * Q + it * C::kTokens;
         for (int k = 0; k < C::kABoxes; ++k)
           tma_load_3d(sa + k * C::kBox, &xmap, &full[s], h0 * d.P + k * C::kAtom, tok, b);
-        for (int k = 0; k < bBoxes; ++k)
-          tma_load_4d(sb + k * C::kBox, &bmap, &full[s], k * C::kAtom, g, tok, b);
+        if constexpr (C::kTF32) {  // B already transposed: the stage's boxes are contiguous
+          const uint8_t* src = reinterpret_cast<const uint8_t*>(bT) +
+                               ((static_cast<int64_t>(b) * d.G + g) * (d.Lp / 32) + tok / 32) * bBoxes * C::kBox;
+          bulk_g2s(sb, src, static_cast<uint32_t>(bBoxes * C::kBox), &full[s]);
+        } else {
+          for (int k = 0; k < bBoxes; ++k)
+            tma_load_4d(sb + k * C::kBox, &bmap, &full[s], k * C::kAtom, g, tok, b);
+        }
       }
     }
   } else if (warp == 1) {
@@ -186,8 +220,8 @@ __global__ void __launch_bounds__(StateCfg<T>::kThreads, 2)
       }
       uint8_t* sa = smem + s * stage_bytes;
       if constexpr (C::kTF32) {
-        // two boxes per round: the A boxes (x, scaled by w) then the B boxes
-        const int nboxes = C::kABoxes + bBoxes;
+        // two boxes per round: the A boxes (x, scaled by w); B arrives transposed
+        const int nboxes = C::kABoxes;
         const int m = et & 63;
         for (int box0 = 0; box0 < nboxes; box0 += 2) {
           const int box = box0 + (et >> 6);
@@ -314,10 +348,16 @@ cudaError_t launch_impl(const Dims& d, const ChunkStateMaps& maps, const Work& w
   }
   const dim3 grid(d.H / 2, d.nc, d.B);
   return launch_k(chunk_state_kernel<T>, grid, dim3(C::kThreads), smem, stream, dependent, maps.x, maps.bm, maps.s, d,
-                  static_cast<const float*>(w.cumsum), static_cast<const float*>(w.dt_t), w.status, spin_ns);
+                  static_cast<const float*>(w.cumsum), static_cast<const float*>(w.dt_t),
+                  static_cast<const float*>(w.bT), w.status, spin_ns);
 }
 
 }  // namespace
+
+cudaError_t launch_b_transpose(const Dims& d, const void* Bm, const Work& w, cudaStream_t stream) {
+  b_transpose_kernel<<<dim3(d.Lp / 32, d.B * d.G), kBtThreads, 0, stream>>>(d, static_cast<const float*>(Bm), w.bT);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_chunk_state(const Dims& d, bool bf16, const ChunkStateMaps& maps, const Work& w,
                                uint64_t spin_ns, cudaStream_t stream, bool dependent) {

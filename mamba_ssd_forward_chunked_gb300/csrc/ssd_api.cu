@@ -100,6 +100,8 @@ ssd_status layout_of(const ssd_shape* shape, ssd_workspace_layout* out) {
   off = align_up(off + (1 + heads / 2) * sizeof(int));
   L.hslot = off;
   off = align_up(off + heads * s.headdim * s.dstate * sizeof(float));
+  L.bT = off;
+  if (s.dtype == SSD_F32) off = align_up(off + static_cast<size_t>(s.batch) * s.ngroups * lp * s.dstate * sizeof(float));
   L.total = off;
   *out = L;
   return SSD_OK;
@@ -116,6 +118,7 @@ Work carve(void* ws, const ssd_workspace_layout& L, bool bf16) {
   w.counter = reinterpret_cast<int*>(p + L.chain);
   w.flags = w.counter + 1;
   w.hslot = reinterpret_cast<float*>(p + L.hslot);
+  w.bT = bf16 ? nullptr : reinterpret_cast<float*>(p + L.bT);
   return w;
 }
 
@@ -286,7 +289,8 @@ size_t ssd_fwd_workspace_size(const ssd_shape* shape) {
 
 int ssd_fwd_kernel_count(const ssd_shape* shape) {
   if (ssd_validate_shape(shape) != SSD_OK || empty_problem(*shape)) return 0;
-  return use_fused(*shape) ? 2 : 4;
+  if (use_fused(*shape)) return 2;
+  return shape->dtype == SSD_BF16 ? 4 : 5;  // fp32: the transpose of Bm comes first
 }
 
 ssd_status ssd_chunk_cumsum(const ssd_shape* shape, const float* dt, const float* A, void* workspace,
@@ -311,8 +315,11 @@ ssd_status ssd_chunk_state(const ssd_shape* shape, const void* x, const void* Bm
   Work w = carve(workspace, L, bf16);
   ChunkStateMaps maps;
   if (!build_state_maps(*shape, x, Bm, w.states, &maps)) return SSD_ERR_CUDA;
-  return from_cuda(
-      launch_chunk_state(make_dims(*shape), bf16, maps, w, spin_limit_ns(), reinterpret_cast<cudaStream_t>(stream)));
+  const Dims d = make_dims(*shape);
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = bf16 ? cudaSuccess : launch_b_transpose(d, Bm, w, cs);
+  if (e == cudaSuccess) e = launch_chunk_state(d, bf16, maps, w, spin_limit_ns(), cs);
+  return from_cuda(e);
 }
 
 ssd_status ssd_state_passing(const ssd_shape* shape, const float* init_state, float* final_state,
@@ -429,7 +436,10 @@ ssd_status fwd_impl(int path, const ssd_shape* shape, const void* x, const float
   const Dims d = make_dims(*shape);
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   const uint64_t spin = spin_limit_ns();
-  cudaError_t e = launch_chunk_cumsum(d, dt, A, w, cs);
+  // fp32: Bm transposed once for every head of its group (chunk_state waits for chunk_cumsum,
+  // which is launched after this kernel has finished)
+  cudaError_t e = bf16 ? cudaSuccess : launch_b_transpose(d, Bm, w, cs);
+  if (e == cudaSuccess) e = launch_chunk_cumsum(d, dt, A, w, cs);
   // chunk_state and compute_out are programmatic dependents of the kernel before them (their
   // launch and prologue overlap its tail).  state_passing is one only while chunk_state runs
   // in a single wave (two CTAs per SM): launched early beside a later wave, its blocks slowed

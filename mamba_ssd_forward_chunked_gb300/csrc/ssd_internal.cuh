@@ -29,6 +29,7 @@ struct Work {
   int* counter;                // one-pass kernel: tile counter
   int* flags;                  // one-pass kernel: [B][H/2] windows published
   float* hslot;                // one-pass kernel: states at run boundaries (its own layout)
+  float* bT;                   // fp32 problems: Bm as K-major TF32 boxes for chunk_state, or null
 };
 
 // Tensor maps built on the host for one call.
@@ -74,6 +75,8 @@ cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t sme
 
 cudaError_t launch_chunk_cumsum(const Dims& d, const float* dt, const float* A, const Work& w,
                                 cudaStream_t stream);
+// fp32 problems: Bm into the workspace's K-major TF32 box layout (w.bT), for chunk_state.
+cudaError_t launch_b_transpose(const Dims& d, const void* Bm, const Work& w, cudaStream_t stream);
 cudaError_t launch_chunk_state(const Dims& d, bool bf16, const ChunkStateMaps& maps, const Work& w,
                                uint64_t spin_ns, cudaStream_t stream, bool dependent = false);
 cudaError_t launch_state_passing(const Dims& d, bool bf16, const float* init, float* final_state,

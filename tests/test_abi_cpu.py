@@ -76,6 +76,9 @@ def test_workspace_layout(ext):
             assert lay["states_bf16"] - lay["states"] >= 2 * nc * 32 * 64 * 128 * es
             extra = 2 * nc * 32 * 64 * 128 * 2 if dt == ext.SSD_BF16 else 0
             assert lay["total"] >= lay["states_bf16"] + extra
+            # fp32: room for Bm as transposed TF32 boxes (B * G * Lp * N floats), bf16: none
+            bT = 2 * 1 * Lp * 128 * 4 if dt == ext.SSD_F32 else 0
+            assert lay["total"] - lay["bT"] >= bT and lay["bT"] >= lay["hslot"] + 2 * 32 * 64 * 128 * 4
             assert ext.ssd_fwd_workspace_size(s) == lay["total"]
     assert ext.ssd_fwd_workspace_size(shape(ext, dstate=100)) == 0
 
@@ -110,4 +113,5 @@ def test_empty_batch_needs_no_device(ext):
     n = ext.ssd_fwd_workspace_size(s)
     assert ext.lib.ssd_fwd(ctypes.byref(s), None, None, None, None, None, None, None, None, None, ws, n, None) == 0
     assert ext.ssd_fwd_kernel_count(s) == 0
-    assert ext.ssd_fwd_kernel_count(shape(ext)) == 4
+    assert ext.ssd_fwd_kernel_count(shape(ext)) == 5  # fp32 staged: Bm transpose + four steps
+    assert ext.ssd_fwd_kernel_count(shape(ext, dtype=ext.SSD_BF16, dstate=256)) == 4  # bf16 staged
