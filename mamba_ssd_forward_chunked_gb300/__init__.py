@@ -315,15 +315,15 @@ def ssd_fwd_host(x, dt, A, Bm, Cm, D, chunk_size: int, init_state=None, device="
         moved = sum(t.numel() * t.element_size() for t in (x, dt, Bm, Cm)) * 2
         pieces = max(1, min(4, moved // (16 << 20)))
     pieces = max(1, int(pieces))
-    if B > 1 or pieces == 1:
+    if B > 1 or pieces == 1:  # batch ranges (segments of several sequences cost more host time than they save)
         n = min(B, pieces)
         cuts = [(B * k) // n for k in range(n + 1)]
         slices = [(cuts[k], cuts[k + 1], 0, L) for k in range(n)]
     else:  # one sequence: segments of whole chunks
         nc = -(-L // chunk_size)
-        n = min(nc, pieces)
-        cuts = [min(L, ((nc * k) // n) * chunk_size) for k in range(n + 1)]
-        slices = [(0, 1, cuts[k], cuts[k + 1]) for k in range(n)]
+        per = min(nc, -(-pieces // B))
+        cuts = [min(L, ((nc * k) // per) * chunk_size) for k in range(per + 1)]
+        slices = [(b, b + 1, cuts[k], cuts[k + 1]) for b in range(B) for k in range(per)]
     seq_split = slices[0][3] - slices[0][2] < L
     if out_y is None:
         out_y = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
@@ -335,7 +335,7 @@ def ssd_fwd_host(x, dt, A, Bm, Cm, D, chunk_size: int, init_state=None, device="
         Ad, Dd = torch.empty(A.shape, dtype=A.dtype, device=dev), torch.empty(D.shape, dtype=D.dtype, device=dev)
         hd = torch.empty(init_state.shape, dtype=init_state.dtype, device=dev) if init_state is not None else None
         yd = torch.empty(x.shape, dtype=x.dtype, device=dev)
-        fd = torch.empty((2 if seq_split else 1, B, H, P, N), dtype=torch.float32, device=dev)
+        fd = torch.empty((2 if seq_split else 1, B, H, P, N), dtype=torch.float32, device=dev)  # [ping-pong]
         if workspace is None:
             bmax = max(b1 - b0 for b0, b1, _, _ in slices)
             lmax = max(l1 - l0 for _, _, l0, l1 in slices)
@@ -357,9 +357,10 @@ def ssd_fwd_host(x, dt, A, Bm, Cm, D, chunk_size: int, init_state=None, device="
             ev_in.append(e)
     for k, (b0, b1, l0, l1) in enumerate(slices):
         st.wait_event(ev_in[k])
-        if seq_split:  # segment k resumes from segment k - 1's final state
-            h_in = hd if k == 0 else fd[(k - 1) % 2]
-            fin = fd[k % 2]
+        seg = k % len(cuts[:-1]) if seq_split else 0  # segment index within its sequence
+        if seq_split:  # a segment resumes from its sequence's previous segment's final state
+            h_in = (hd[b0:b1] if hd is not None else None) if seg == 0 else fd[(seg - 1) % 2, b0:b1]
+            fin = fd[seg % 2, b0:b1]
         else:
             h_in = hd[b0:b1] if hd is not None else None
             fin = fd[0, b0:b1]
@@ -370,10 +371,8 @@ def ssd_fwd_host(x, dt, A, Bm, Cm, D, chunk_size: int, init_state=None, device="
         cout.wait_event(e)
         with torch.cuda.stream(cout):
             out_y[b0:b1, l0:l1].copy_(yd[b0:b1, l0:l1], non_blocking=True)
-            if not seq_split:
+            if not seq_split or l1 == L:  # a sequence's last slice holds its final state
                 out_final[b0:b1].copy_(fin, non_blocking=True)
-            elif k == len(slices) - 1:
-                out_final.copy_(fin, non_blocking=True)
     st.wait_stream(cout)
     return out_y, out_final
 
