@@ -285,6 +285,21 @@ def _copy_streams(dev: torch.device):
     return pair
 
 
+def host_slices(batch: int, seqlen: int, chunk_size: int, pieces: int):
+    """The slices ssd_fwd_host pipelines over, as (b0, b1, l0, l1): up to ``pieces`` batch ranges,
+    or, for one sequence, up to ``pieces`` segments whose boundaries are chunk boundaries.
+    Together they cover [0, batch) x [0, seqlen) once, in the order they run."""
+    pieces = max(1, int(pieces))
+    if batch > 1 or pieces == 1:  # batch ranges (segments of several sequences cost more host time than they save)
+        n = min(batch, pieces)
+        cuts = [(batch * k) // n for k in range(n + 1)]
+        return [(cuts[k], cuts[k + 1], 0, seqlen) for k in range(n)]
+    nc = -(-seqlen // chunk_size)  # one sequence: segments of whole chunks
+    n = min(nc, pieces)
+    cuts = [min(seqlen, ((nc * k) // n) * chunk_size) for k in range(n + 1)]
+    return [(0, 1, cuts[k], cuts[k + 1]) for k in range(n)]
+
+
 def ssd_fwd_host(x, dt, A, Bm, Cm, D, chunk_size: int, init_state=None, device="cuda",
                  out_y=None, out_final=None, workspace=None, stream=None, pieces: Optional[int] = None):
     """End-to-end call from host memory: copies the inputs to the device,
@@ -314,16 +329,7 @@ def ssd_fwd_host(x, dt, A, Bm, Cm, D, chunk_size: int, init_state=None, device="
         # layer, 370 MB: 1.55 ms in four against 2.14 in one); small problems stay in one
         moved = sum(t.numel() * t.element_size() for t in (x, dt, Bm, Cm)) * 2
         pieces = max(1, min(4, moved // (16 << 20)))
-    pieces = max(1, int(pieces))
-    if B > 1 or pieces == 1:  # batch ranges (segments of several sequences cost more host time than they save)
-        n = min(B, pieces)
-        cuts = [(B * k) // n for k in range(n + 1)]
-        slices = [(cuts[k], cuts[k + 1], 0, L) for k in range(n)]
-    else:  # one sequence: segments of whole chunks
-        nc = -(-L // chunk_size)
-        per = min(nc, -(-pieces // B))
-        cuts = [min(L, ((nc * k) // per) * chunk_size) for k in range(per + 1)]
-        slices = [(b, b + 1, cuts[k], cuts[k + 1]) for b in range(B) for k in range(per)]
+    slices = host_slices(B, L, chunk_size, pieces)
     seq_split = slices[0][3] - slices[0][2] < L
     if out_y is None:
         out_y = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
@@ -357,7 +363,7 @@ def ssd_fwd_host(x, dt, A, Bm, Cm, D, chunk_size: int, init_state=None, device="
             ev_in.append(e)
     for k, (b0, b1, l0, l1) in enumerate(slices):
         st.wait_event(ev_in[k])
-        seg = k % len(cuts[:-1]) if seq_split else 0  # segment index within its sequence
+        seg = k if seq_split else 0  # segment index within the (single) sequence
         if seq_split:  # a segment resumes from its sequence's previous segment's final state
             h_in = (hd[b0:b1] if hd is not None else None) if seg == 0 else fd[(seg - 1) % 2, b0:b1]
             fin = fd[seg % 2, b0:b1]
