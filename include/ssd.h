@@ -131,8 +131,9 @@ size_t ssd_fwd_workspace_size(const ssd_shape* shape);
  *    between windows through the workspace (or final_state), and writes y;
  *    x, Bm and Cm are read once.  SSD_BF16 only.
  *  - staged: chunk_cumsum, chunk_state, state_passing and compute_out
- *    (SSD_F32: preceded by one transpose of Bm into the workspace, shared by
- *    every head of a group).
+ *    (SSD_F32: the chunk_cumsum launch also transposes Bm into the workspace,
+ *    once for every head of a group; ssd_chunk_state called alone does that
+ *    transpose itself).
  * ssd_fwd takes the one-pass schedule for SSD_BF16 when dstate <= 128 and
  * there are at least as many (batch, head pair) sequences as multiprocessors
  * (below that the chain of windows, not bandwidth, bounds the one-pass kernel);
@@ -167,8 +168,8 @@ ssd_status ssd_fused_pass(const ssd_shape* shape, const void* x, const void* Bm,
  * kernel ran out (its outputs are then invalid).  Blocking 4-byte read. */
 ssd_status ssd_fwd_check(const void* workspace);
 
-/* --- The four steps, callable one by one (for SSD_F32, ssd_fwd is exactly
- * these four calls in order; for SSD_BF16 the four calls in order give the
+/* --- The four steps, callable one by one (for SSD_F32, ssd_fwd computes
+ * exactly what these four calls in order compute; for SSD_BF16 the four calls in order give the
  * same result as ssd_fwd through the staged path).  Each reads and writes the
  * workspace regions named. ---- */
 

@@ -60,29 +60,15 @@ __host__ __device__ inline uint32_t state_stage_bytes(int N, int atom, int box, 
 
 // fp32 problems: Bm in the K-major TF32 box layout, once per (batch, group).
 // Every head of a group multiplies by the same B, so its transpose (and TF32
-// rounding) is done here once instead of in each head pair's CTA.  One CTA per
-// (32-token stage, batch * group); thread (a, e) of a box writes the 16-byte
-// chunk holding tokens 4a..4a+3 of dstate row e, reading those four tokens'
-// values of column e (coalesced along e).  Tokens past L read as 0.
+// rounding) is done once here instead of in each head pair's CTA.  The full
+// forward runs the same stages inside the chunk_cumsum launch; this kernel
+// serves the standalone chunk_state step.  One CTA per (32-token stage,
+// batch * group).
 constexpr int kBtThreads = 256;
 
 __global__ void __launch_bounds__(kBtThreads) b_transpose_kernel(Dims d, const float* __restrict__ Bm,
                                                                   float* __restrict__ bT) {
-  const int stage = blockIdx.x;          // 32-token stage of the padded sequence
-  const int bg = blockIdx.y;             // batch * G + group
-  const int b = bg / d.G, g = bg % d.G;
-  const int a = threadIdx.x >> 5, e = threadIdx.x & 31;
-  const int nbox = d.N / 32;
-  uint8_t* out = reinterpret_cast<uint8_t*>(bT) + (static_cast<int64_t>(bg) * (d.Lp / 32) + stage) * nbox * 4096;
-  for (int k = 0; k < nbox; ++k) {
-    float v[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int tok = stage * 32 + 4 * a + q;
-      v[q] = tok < d.L ? round_tf32(Bm[((static_cast<int64_t>(b) * d.L + tok) * d.G + g) * d.N + k * 32 + e]) : 0.f;
-    }
-    *reinterpret_cast<float4*>(out + k * 4096 + box_t_offset(4 * a, e)) = make_float4(v[0], v[1], v[2], v[3]);
-  }
+  b_transpose_stage(Bm, bT, d.L, d.G, d.N, d.Lp, blockIdx.x, blockIdx.y, threadIdx.x);
 }
 
 // Stages that fit the ring budget (2..4).

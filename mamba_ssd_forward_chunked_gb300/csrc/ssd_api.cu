@@ -290,7 +290,7 @@ size_t ssd_fwd_workspace_size(const ssd_shape* shape) {
 int ssd_fwd_kernel_count(const ssd_shape* shape) {
   if (ssd_validate_shape(shape) != SSD_OK || empty_problem(*shape)) return 0;
   if (use_fused(*shape)) return 2;
-  return shape->dtype == SSD_BF16 ? 4 : 5;  // fp32: the transpose of Bm comes first
+  return 4;
 }
 
 ssd_status ssd_chunk_cumsum(const ssd_shape* shape, const float* dt, const float* A, void* workspace,
@@ -436,10 +436,8 @@ ssd_status fwd_impl(int path, const ssd_shape* shape, const void* x, const float
   const Dims d = make_dims(*shape);
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   const uint64_t spin = spin_limit_ns();
-  // fp32: Bm transposed once for every head of its group (chunk_state waits for chunk_cumsum,
-  // which is launched after this kernel has finished)
-  cudaError_t e = bf16 ? cudaSuccess : launch_b_transpose(d, Bm, w, cs);
-  if (e == cudaSuccess) e = launch_chunk_cumsum(d, dt, A, w, cs);
+  // fp32: the chunk_cumsum launch also transposes Bm once for every head of its group
+  cudaError_t e = launch_chunk_cumsum(d, dt, A, w, cs, bf16 ? nullptr : Bm);
   // chunk_state and compute_out are programmatic dependents of the kernel before them (their
   // launch and prologue overlap its tail).  state_passing is one only while chunk_state runs
   // in a single wave (two CTAs per SM): launched early beside a later wave, its blocks slowed

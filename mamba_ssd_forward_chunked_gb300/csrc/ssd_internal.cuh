@@ -73,9 +73,11 @@ cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t sme
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
+// With Bm non-null (fp32 problems) the same launch also writes Bm into the workspace's
+// K-major TF32 box layout (w.bT) that chunk_state reads.
 cudaError_t launch_chunk_cumsum(const Dims& d, const float* dt, const float* A, const Work& w,
-                                cudaStream_t stream);
-// fp32 problems: Bm into the workspace's K-major TF32 box layout (w.bT), for chunk_state.
+                                cudaStream_t stream, const void* Bm = nullptr);
+// fp32 problems: the same Bm layout alone, for the standalone chunk_state step.
 cudaError_t launch_b_transpose(const Dims& d, const void* Bm, const Work& w, cudaStream_t stream);
 cudaError_t launch_chunk_state(const Dims& d, bool bf16, const ChunkStateMaps& maps, const Work& w,
                                uint64_t spin_ns, cudaStream_t stream, bool dependent = false);

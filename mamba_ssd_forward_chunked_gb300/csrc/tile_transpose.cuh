@@ -52,4 +52,26 @@ __device__ __forceinline__ uint32_t box_t_offset(int t, int e) {
   return static_cast<uint32_t>(e * 128 + (((t >> 2) ^ (e & 7)) << 4) + (t & 3) * 4);
 }
 
+// One 32-token stage of a (batch, group) slice of Bm [B][L][G][N] written in the
+// K-major TF32 box layout [B][G][Lp/32][N/32][4 KB] (what the fp32 chunk_state
+// MMA reads).  256 threads: thread (a = tid / 32, e = tid % 32) of box k reads
+// tokens 4a..4a+3 of column 32k+e (coalesced along e) and writes them as one
+// 16-byte chunk.  Tokens past L read as 0.
+__device__ __forceinline__ void b_transpose_stage(const float* __restrict__ Bm, float* __restrict__ bT, int L,
+                                                  int G, int N, int Lp, int stage, int bg, int tid) {
+  const int b = bg / G, g = bg % G;
+  const int a = tid >> 5, e = tid & 31;
+  const int nbox = N / 32;
+  uint8_t* out = reinterpret_cast<uint8_t*>(bT) + (static_cast<int64_t>(bg) * (Lp / 32) + stage) * nbox * 4096;
+  for (int k = 0; k < nbox; ++k) {
+    float v[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int tok = stage * 32 + 4 * a + q;
+      v[q] = tok < L ? round_tf32(Bm[((static_cast<int64_t>(b) * L + tok) * G + g) * N + k * 32 + e]) : 0.f;
+    }
+    *reinterpret_cast<float4*>(out + k * 4096 + box_t_offset(4 * a, e)) = make_float4(v[0], v[1], v[2], v[3]);
+  }
+}
+
 }  // namespace ssd
