@@ -185,6 +185,9 @@ def workspace_views(shape: ssd_shape, ws: torch.Tensor) -> Dict[str, torch.Tenso
         out["states_bf16"] = view(L["states_bf16"], B * nc * H * P * N, torch.bfloat16, (B, nc, H, P, N))
     out["chain"] = view(L["chain"], 1 + B * (H // 2), torch.int32, (1 + B * (H // 2),))
     out["hslot"] = view(L["hslot"], B * H * P * N, torch.float32, (B * H * P * N,))
+    if shape.dtype != SSD_BF16:  # Bm in 4 KB TF32 boxes, [B][G][Lp/32][N/32][box]
+        G = shape.ngroups
+        out["bT"] = view(L["bT"], B * G * Lp * N, torch.float32, (B * G * Lp * N,))
     return out
 
 

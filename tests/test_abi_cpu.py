@@ -115,3 +115,24 @@ def test_empty_batch_needs_no_device(ext):
     assert ext.ssd_fwd_kernel_count(s) == 0
     assert ext.ssd_fwd_kernel_count(shape(ext)) == 4  # fp32 staged: the Bm transpose rides in chunk_cumsum
     assert ext.ssd_fwd_kernel_count(shape(ext, dtype=ext.SSD_BF16, dstate=256)) == 4  # bf16 staged
+
+
+def test_workspace_views_are_disjoint_and_inside(ext):
+    """The typed views the tests read (workspace_views) lie inside the workspace
+    and never share a byte, for both dtypes and a ragged length."""
+    import torch
+    for dt in (ext.SSD_F32, ext.SSD_BF16):
+        for L, G in ((300, 1), (2048, 2)):
+            s = shape(ext, seqlen=L, dtype=dt, ngroups=G)
+            ws = torch.zeros(ext.ssd_fwd_workspace_size(s), dtype=torch.uint8)
+            base = ws.data_ptr()
+            spans = []
+            for name, v in ext.workspace_views(s, ws).items():
+                lo = v.data_ptr() - base
+                hi = lo + v.numel() * v.element_size()
+                assert 0 <= lo < hi <= ws.numel(), name
+                spans.append((lo, hi, name))
+            spans.sort()
+            for (a0, a1, na), (b0, b1, nb) in zip(spans, spans[1:]):
+                assert a1 <= b0, (na, nb)
+            assert ("bT" in dict((n, 1) for _, _, n in spans)) == (dt == ext.SSD_F32)

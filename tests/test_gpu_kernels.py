@@ -94,3 +94,29 @@ def test_compute_out_causal_upper_triangle_is_exactly_zero():
     torch.cuda.synchronize()
     assert torch.equal(y1[:, :100], y2[:, :100])
     assert torch.isfinite(y1).all()
+
+
+@pytest.mark.parametrize("name,over", [CASES[1], CASES[3], CASES[5]], ids=[CASES[1][0], CASES[3][0], CASES[5][0]])
+def test_full_forward_equals_the_four_steps(name, over):
+    """ssd_fwd on the staged schedule (fp32 inputs; bf16 at dstate 256) gives
+    bit for bit what the four step calls give in order: the full forward folds
+    the fp32 Bm transpose into the chunk_cumsum launch and chains the kernels
+    with programmatic dependent launch, and neither may change a result."""
+    ssd, w, inp, d, shape, ws = _setup(over)
+    assert ssd.ssd_fwd_kernel_count(shape) == 4
+    B, L, H = inp["dt"].shape
+    y1, f1 = ssd.ssd_fwd(d["x"], d["dt"], d["A"], d["Bm"], d["Cm"], d["D"], w.chunk_size,
+                         init_state=d.get("init"), workspace=ws)
+    torch.cuda.synchronize()
+    ws2 = torch.zeros_like(ws)
+    y2 = torch.empty_like(d["x"])
+    f2 = torch.empty(B, H, 64, w.dstate, device="cuda")
+    ssd.ssd_chunk_cumsum(shape, d["dt"], d["A"], ws2)
+    ssd.ssd_chunk_state(shape, d["x"], d["Bm"], ws2)
+    ssd.ssd_state_passing(shape, d.get("init"), f2, ws2)
+    ssd.ssd_compute_out(shape, d["x"], d["Bm"], d["Cm"], d["D"], y2, ws2)
+    torch.cuda.synchronize()
+    assert torch.equal(y1, y2)
+    assert torch.equal(f1, f2)
+    if w.dtype == "f32":
+        assert torch.equal(ssd.workspace_views(shape, ws)["bT"], ssd.workspace_views(shape, ws2)["bT"])
