@@ -24,10 +24,16 @@
 // tensor memory (dstate columns) and is drained by tcgen05.ld.
 //
 // fp32 inputs run the MMA as TF32, whose shared-memory operands must be
-// K-major: there each 32-token x 32-element TMA box is transposed in place
-// (scaled and rounded to TF32 on the way), so both operands become K-major
-// tiles with the tokens along the 128-byte rows.  bf16 keeps the MN-major
-// tiles and only scales.
+// K-major.  B arrives K-major (transposed once per group by the Bm transpose
+// blocks).  For x there are two forms.  While dstate plus one 32-column slot
+// per ring stage fits in 256 tensor-memory columns (dstate <= 128; two CTAs per
+// SM still fit), each thread reads its (head, p) row's 32 tokens from the
+// landed box, scales and rounds them and stores them to tensor memory, where
+// the MMA takes them as its A operand: shared memory then carries the TMA
+// writes, one read of x and the MMA's B reads, about two thirds of the traffic
+// of the in-place form.  At dstate 256 each 32-token x 32-element box is
+// transposed in place in shared memory instead (scaled and rounded on the
+// way).  bf16 keeps the MN-major tiles and only scales.
 //
 // Warp roles (192 threads): warp 0 issues TMA, warp 1 owns TMEM and issues
 // the MMAs (one thread), warps 2-5 compute the weights, transform each stage
@@ -102,7 +108,11 @@ __global__ void __launch_bounds__(StateCfg<T>::kThreads, 2)
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(accum + 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nstages = Q / C::kTokens;
-  const uint32_t tmem_cols = static_cast<uint32_t>(N);
+  // TF32 with the x operand in tensor memory: the accumulator's N columns, then one
+  // 32-column slot per ring stage
+  const bool ts = C::kTF32 && N + NS * C::kTokens <= 256;
+  const uint32_t a_col = static_cast<uint32_t>(N);
+  const uint32_t tmem_cols = ts ? 256u : static_cast<uint32_t>(N);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
@@ -182,8 +192,13 @@ __global__ void __launch_bounds__(StateCfg<T>::kThreads, 2)
           if constexpr (C::kTF32) {
             // K-major, 128-B swizzle: rows of 32 tokens; a K step of 8 tokens
             // is 32 B along the row; SBO = 1024 B between 8-row groups.
-            ad = sdesc_sw128(sa + k * 32, 16, 1024);
             bd = sdesc_sw128(sb + k * 32, 16, 1024);
+            if (ts) {  // A: the stage's tensor-memory slot, one column per token
+              mma_ts<true>(tmem, tmem + a_col + static_cast<uint32_t>(s * C::kTokens + k * C::kKStep), bd, idesc,
+                           (it | k) != 0 ? 1u : 0u);
+              continue;
+            }
+            ad = sdesc_sw128(sa + k * 32, 16, 1024);
           } else {
             // MN-major, 128-B swizzle: LBO = stride between 128-B atom columns
             // (one TMA box), SBO = stride between 8-row groups along K.
@@ -205,7 +220,23 @@ __global__ void __launch_bounds__(StateCfg<T>::kThreads, 2)
         break;
       }
       uint8_t* sa = smem + s * stage_bytes;
-      if constexpr (C::kTF32) {
+      if (ts) {
+        // thread = row quad * 32 + lane of M = (head in pair, p): box `quad` holds its 32
+        // tokens as one 4-byte column (conflict-free: a warp reads one 128-B row at a time)
+        const int quad = warp & 3;
+        const uint8_t* bp = sa + quad * C::kBox;
+        const float* w = w_s + (quad >> 1) * Q + it * C::kTokens;
+        uint32_t v[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const float xv = *reinterpret_cast<const float*>(bp + j * 128 + ((((lane >> 2) ^ (j & 7)) << 4) |
+                                                                                ((lane & 3) << 2)));
+          v[j] = __float_as_uint(round_tf32(xv * w[j]));
+        }
+        tmem_st32(tmem + (static_cast<uint32_t>(quad * 32) << 16) + a_col + static_cast<uint32_t>(s * C::kTokens), v);
+        tmem_st_wait();
+        tc_fence_before();
+      } else if constexpr (C::kTF32) {
         // two boxes per round: the A boxes (x, scaled by w); B arrives transposed
         const int nboxes = C::kABoxes;
         const int m = et & 63;

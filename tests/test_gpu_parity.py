@@ -54,6 +54,7 @@ SMALL = [
     dict(seqlen=513, chunk_size=256, dstate=128, dtype="bf16", init_state=True),
     dict(batch=3, seqlen=130, chunk_size=64, nheads=8, ngroups=4, dstate=64, dtype="bf16"),
     dict(batch=2, seqlen=1000, chunk_size=256, nheads=6, ngroups=3, dstate=256, dtype="f32", init_state=True),
+    dict(batch=2, seqlen=333, chunk_size=128, nheads=8, ngroups=2, dstate=128, dtype="f32", init_state=True),
 ]
 
 
