@@ -234,6 +234,36 @@ def check_extreme_decay(rec: Rec) -> bool:
     return bool(np.all(np.isfinite(y)) and np.all(np.isfinite(f)) and rel_err(y, yc) < 1e-12)
 
 
+def check_bidiagonal_solve(rec: Rec) -> bool:
+    """Time-varying decay: every state entry (b, h, p, n) obeys the first-order
+    linear recurrence h_t - alpha_t h_{t-1} = dt_t x_t[p] b_t[n] with
+    alpha_t = exp(dt_t A_h), i.e. a lower-bidiagonal linear system in
+    (h_0 .. h_{L-1}).  scipy's banded solver gives the states without any loop
+    of the oracle's; y_t = h_t c_t + D x_t and the final state follow."""
+    from scipy.linalg import solve_banded
+    B, L, H, P, N, G = 2, 17, 4, 3, 5, 2
+    inp = tiny_inputs(B=B, L=L, H=H, P=P, N=N, G=G, seed=29, dt_scale=4.0)
+    x, dt, A = (inp[k].astype(np.float64) for k in ("x", "dt", "A"))
+    Bm, Cm, D, h0 = (inp[k].astype(np.float64) for k in ("Bm", "Cm", "D", "init"))
+    r = H // G
+    y_ref = np.empty((B, L, H, P))
+    f_ref = np.empty((B, H, P, N))
+    for b in range(B):
+        for h in range(H):
+            g = h // r
+            alpha = np.exp(dt[b, :, h] * A[h])                      # [L]
+            ab = np.zeros((2, L))
+            ab[0] = 1.0
+            ab[1, :L - 1] = -alpha[1:]                               # row t, column t - 1
+            rhs = dt[b, :, h, None, None] * x[b, :, h, :, None] * Bm[b, :, g, None, :]   # [L, P, N]
+            rhs[0] += alpha[0] * h0[b, h]
+            states = solve_banded((1, 0), ab, rhs.reshape(L, P * N)).reshape(L, P, N)
+            y_ref[b, :, h] = np.einsum("tpn,tn->tp", states, Cm[b, :, g]) + D[h] * x[b, :, h]
+            f_ref[b, h] = states[-1]
+    y, f = rec(inp)
+    return bool(rel_err(y, y_ref) < 1e-12 and rel_err(f, f_ref) < 1e-12)
+
+
 ALL_CHECKS = {
     "golden_jump_no_decay": lambda r: check_golden(r, "jump_no_decay.txt"),
     "golden_decay_half": lambda r: check_golden(r, "decay_half.txt"),
@@ -248,6 +278,7 @@ ALL_CHECKS = {
     "resume": check_resume,
     "group_map": check_group_map,
     "extreme_decay": check_extreme_decay,
+    "bidiagonal_solve": check_bidiagonal_solve,
 }
 
 

@@ -21,7 +21,7 @@ def test_pin_recurrence(name):
 
 @pytest.mark.parametrize("name", ["golden_jump_no_decay", "golden_decay_half", "golden_dt_scaling",
                                   "jump_formula_integers", "geometric_series", "single_token",
-                                  "causality", "group_map", "extreme_decay"])
+                                  "causality", "group_map", "extreme_decay", "bidiagonal_solve"])
 @pytest.mark.parametrize("Q", [1, 2, 5, 64])
 def test_pin_chunked_form(name, Q):
     """The chunked form (the per-kernel reference) passes the same pins."""
