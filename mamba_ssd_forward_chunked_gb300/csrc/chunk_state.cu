@@ -37,8 +37,9 @@
 //
 // Warp roles (192 threads): warp 0 issues TMA, warp 1 owns TMEM and issues
 // the MMAs (one thread), warps 2-5 compute the weights, transform each stage
-// and write S_c.  A 4-deep mbarrier ring (full -> scaled -> empty) pipelines
-// the 32-token stages.  All waits are bounded (device-timeout status, no hang).
+// and write S_c.  A ring of 2-4 stages (as many as fit 96 KB; mbarriers full ->
+// scaled -> empty) pipelines the 32-token stages.  All waits are bounded
+// (device-timeout status, no hang).
 #include "ptx.cuh"
 #include "ssd_internal.cuh"
 #include "tile_transpose.cuh"
