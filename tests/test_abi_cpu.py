@@ -136,3 +136,44 @@ def test_workspace_views_are_disjoint_and_inside(ext):
             for (a0, a1, na), (b0, b1, nb) in zip(spans, spans[1:]):
                 assert a1 <= b0, (na, nb)
             assert ("bT" in dict((n, 1) for _, _, n in spans)) == (dt == ext.SSD_F32)
+
+
+def test_step_entry_points_reject_bad_arguments_before_any_launch(ext):
+    """Every step entry point checks its workspace, pointers and alignment (and
+    the one-pass ones the dtype) before touching the device; the static-scratch
+    entry point rejects a problem whose workspace exceeds its array.  All the
+    pointers are fake and never dereferenced."""
+    lib, by = ext.lib, ctypes.byref
+    fake, odd4, odd2 = ctypes.c_void_p(1 << 20), ctypes.c_void_p((1 << 20) + 4), ctypes.c_void_p((1 << 20) + 2)
+    for dt in (ext.SSD_F32, ext.SSD_BF16):
+        s = shape(ext, dtype=dt)
+        need = ext.ssd_fwd_workspace_size(s)
+        # workspace: too small, missing, misaligned
+        for call in (lambda w, n: lib.ssd_chunk_cumsum(by(s), fake, fake, w, n, None),
+                     lambda w, n: lib.ssd_chunk_state(by(s), fake, fake, w, n, None),
+                     lambda w, n: lib.ssd_state_passing(by(s), None, None, w, n, None),
+                     lambda w, n: lib.ssd_compute_out(by(s), fake, fake, fake, fake, fake, w, n, None)):
+            assert call(fake, need - 1) == 3
+            assert call(None, need) == 1
+            assert call(odd4, need) == 1
+        assert lib.ssd_chunk_cumsum(by(s), None, fake, fake, need, None) == 1
+        assert lib.ssd_chunk_cumsum(by(s), fake, odd2, fake, need, None) == 1
+        assert lib.ssd_chunk_state(by(s), None, fake, fake, need, None) == 1
+        assert lib.ssd_chunk_state(by(s), fake, odd4, fake, need, None) == 1
+        assert lib.ssd_state_passing(by(s), odd4, None, fake, need, None) == 1
+        assert lib.ssd_state_passing(by(s), None, odd4, fake, need, None) == 1
+        assert lib.ssd_compute_out(by(s), fake, fake, fake, fake, None, fake, need, None) == 1
+        assert lib.ssd_compute_out(by(s), fake, fake, odd4, fake, fake, fake, need, None) == 1
+        assert lib.ssd_compute_out(by(s), fake, fake, fake, odd2, fake, fake, need, None) == 1
+        if dt == ext.SSD_F32:  # the one-pass schedule is bf16 only
+            assert lib.ssd_fused_pass(by(s), fake, fake, fake, fake, None, fake, None, fake, need, None) == 2
+            assert lib.ssd_fwd_fused(by(s), fake, fake, fake, fake, fake, fake, None, fake, None, fake, need,
+                                     None) == 2
+        else:
+            assert lib.ssd_fused_pass(by(s), None, fake, fake, fake, None, fake, None, fake, need, None) == 1
+            assert lib.ssd_fused_pass(by(s), fake, fake, fake, fake, odd4, fake, None, fake, need, None) == 1
+    big = shape(ext, batch=4, seqlen=4096, nheads=80, dtype=ext.SSD_BF16)
+    assert ext.ssd_fwd_workspace_size(big) > (32 << 20)
+    assert lib.ssd_fwd_static_scratch(by(big), fake, fake, fake, fake, fake, fake, None, fake, None, None) == 3
+    assert lib.ssd_fwd_static_scratch(by(shape(ext, dstate=96)), fake, fake, fake, fake, fake, fake, None, fake,
+                                      None, None) == 2
