@@ -177,3 +177,15 @@ def test_step_entry_points_reject_bad_arguments_before_any_launch(ext):
     assert lib.ssd_fwd_static_scratch(by(big), fake, fake, fake, fake, fake, fake, None, fake, None, None) == 3
     assert lib.ssd_fwd_static_scratch(by(shape(ext, dstate=96)), fake, fake, fake, fake, fake, fake, None, fake,
                                       None, None) == 2
+
+
+def test_binding_refuses_host_tensors(ext):
+    """The Python entry points run only on the GPU path: host (CPU) tensors are
+    rejected with an error, never computed some other way."""
+    import torch
+    x = torch.zeros(1, 64, 2, 64)
+    dt, A, D = torch.zeros(1, 64, 2), torch.zeros(2), torch.zeros(2)
+    Bm = Cm = torch.zeros(1, 64, 1, 64)
+    with pytest.raises(ext.SSDError) as e:
+        ext.ssd_fwd(x, dt, A, Bm, Cm, D, 64)
+    assert e.value.code == 1 and "CUDA" in str(e.value)
