@@ -214,8 +214,8 @@ int ssd_fwd_kernel_count(const ssd_shape* shape);
 /* Bytes of the device array that ssd_fwd_static_scratch uses as its workspace. */
 #define SSD_STATIC_SCRATCH_BYTES ((size_t)32 << 20)
 
-/* ssd_fwd for callers that may not allocate device memory.  The paper has no
- * counterpart: this is a service of the library, not a step of the method.
+/* ssd_fwd for callers that may not allocate device memory.  The pages describe
+ * no counterpart: this is a service of the library, not a step of the method.
  *
  * Who needs it: code that runs inside a host which owns all device memory
  * (a plugin of another runtime with its own pool), serving processes that
