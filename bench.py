@@ -1,13 +1,16 @@
 #!/usr/bin/env python3
 """Throughput of the Mamba-2 chunked SSD forward pass on GB300.
 
-One step = one ssd_fwd call (chunk_cumsum -> chunk_state -> state_passing ->
+One step = one ssd_fwd call (the schedule it picks for the shape: chunk_cumsum
+then the one-pass kernel, or chunk_cumsum -> chunk_state -> state_passing ->
 compute_out) over one batch of seeded synthetic inputs already resident in HBM.
-Prints ONE JSON line (rank 0).
+Prints ONE JSON line (rank 0).  The default workload is the 2.7B-layer shape
+(bf16, batch 4 x 4096 tokens, 80 heads, dstate 128).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
-N > 1 runs under torchrun, one rank per GPU: every rank solves its own
+N > 1 runs one rank per GPU (launched under torch.distributed.run, which
+bench.py does itself when started without it): every rank solves its own
 independent problem of the same size (weak scaling; no collective on the data
 path) and the value is all ranks' tokens over the slowest rank's time.
 
@@ -34,13 +37,15 @@ import numpy as np  # noqa: E402
 import ssd_synth  # noqa: E402
 
 METRIC = "SSD forward tokens/s and % of roofline (TF32 / bf16), 1xGB300"
-DEFAULT_WORKLOAD = "mamba2-370m"
+DEFAULT_WORKLOAD = "mamba2-2.7b"
 L2_FLUSH_BYTES = 256 << 20
 # Device-side spin before each timed step (outside its events) so the host has
 # enqueued the whole step before the first event fires: the events then time
 # the kernels, not the host's launch latency (reported separately).
 PRE_STEP_SLEEP_CYCLES = 200_000
-NOMINAL_TF32_OVER_BF16 = 1.1 / 2.25  # dense tensor-core rate ratio (nominal)
+# GB300's nominal dense tensor-core rates: TF32 1.1 PFLOP/s against bf16 2.25 PFLOP/s.  Used only
+# when the live measurement below cannot run.
+NOMINAL_TF32_OVER_BF16 = 1.1 / 2.25
 KERNELS = ("chunk_cumsum", "chunk_state", "state_passing", "compute_out")  # staged schedule
 FUSED_KERNELS = ("chunk_cumsum", "ssd_fused")                                # one-pass schedule
 
@@ -97,9 +102,44 @@ def peaks():
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
 
 
-def tensor_peak(pk, dtype):
+def tensor_peak(pk, dtype, tf32_ratio=None):
+    """Dense tensor-core peak for the problem's MMA type: the measured bf16
+    rate, times the TF32/bf16 rate ratio for fp32 problems (measured on this
+    device when given, else the nominal one)."""
     base = pk["bf16_tflops"]
-    return base * NOMINAL_TF32_OVER_BF16 if dtype == "f32" else base
+    if dtype != "f32":
+        return base
+    return base * (NOMINAL_TF32_OVER_BF16 if tf32_ratio is None else tf32_ratio)
+
+
+def measure_tf32_over_bf16(dev, n: int = 8192, reps: int = 10):
+    """Ratio of cuBLAS's dense TF32 rate to its bf16 rate on this device: the
+    best of ``reps`` n^3 products each (CUDA events), both at the same clocks
+    and with the same method as the measured bf16 peak.  The bf16 peak times
+    this ratio is the TF32 roofline denominator."""
+    import torch
+    rates = {}
+    old = torch.backends.cuda.matmul.allow_tf32
+    try:
+        torch.backends.cuda.matmul.allow_tf32 = True
+        for name, dt in (("bf16", torch.bfloat16), ("tf32", torch.float32)):
+            a = torch.randn(n, n, device=dev, dtype=dt)
+            b = torch.randn(n, n, device=dev, dtype=dt)
+            for _ in range(3):
+                torch.matmul(a, b)
+            best = float("inf")
+            for _ in range(reps):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                torch.matmul(a, b)
+                e1.record()
+                torch.cuda.synchronize(dev)
+                best = min(best, e0.elapsed_time(e1) * 1e-3)
+            rates[name] = 2.0 * n ** 3 / best / 1e12
+            del a, b
+    finally:
+        torch.backends.cuda.matmul.allow_tf32 = old
+    return rates["tf32"] / rates["bf16"], rates
 
 
 # ------------------------------------------------------------------ clocks
@@ -227,25 +267,23 @@ def run_gpu(args, w: ssd_synth.Workload, rank: int, world: int, local_rank: int)
     names = FUSED_KERNELS if fused else KERNELS
 
     def staged(ev):
-        # the same launches ssd_fwd makes, in its order, with events between them
-        ev[0].record(stream)
-        ssd.ssd_chunk_cumsum(shape, d["dt"], d["A"], ws, stream)
-        ev[1].record(stream)
-        if fused:
-            ssd.ssd_fused_pass(shape, d["x"], d["Bm"], d["Cm"], d["D"], init, y, fin, ws, stream)
-            ev[2].record(stream)
-            return
-        ssd.ssd_chunk_state(shape, d["x"], d["Bm"], ws, stream)
-        ev[2].record(stream)
-        ssd.ssd_state_passing(shape, init, fin, ws, stream)
-        ev[3].record(stream)
-        ssd.ssd_compute_out(shape, d["x"], d["Bm"], d["Cm"], d["D"], y, ws, stream)
-        ev[4].record(stream)
+        # the same launches ssd_fwd makes, in its order, one ssd_fwd_range call each with events between them
+        for i in range(len(names)):
+            ev[i].record(stream)
+            ssd.ssd_fwd_range(d["x"], d["dt"], d["A"], d["Bm"], d["Cm"], d["D"], w.chunk_size, i, i + 1,
+                              init_state=init, y=y, final_state=fin, workspace=ws, stream=stream)
+        ev[len(names)].record(stream)
 
     def barrier():
         if world > 1:
             dist.barrier()
 
+    tf32_ratio, tf32_rates = None, None
+    if w.dtype == "f32":  # the TF32 roofline denominator, measured on this device before any timing
+        try:
+            tf32_ratio, tf32_rates = measure_tf32_over_bf16(dev)
+        except Exception:
+            tf32_ratio = None
     for _ in range(args.warmup):
         flush.zero_()
         fwd()
@@ -284,7 +322,8 @@ def run_gpu(args, w: ssd_synth.Workload, rank: int, world: int, local_rank: int)
             staged(ev)
         torch.cuda.synchronize(dev)
         barrier()
-        per_kernel = {n: statistics.mean(ev[i].elapsed_time(ev[i + 1]) for ev in kev) for i, n in enumerate(names)}
+        per_kernel = {n: statistics.median(ev[i].elapsed_time(ev[i + 1]) for ev in kev)
+                      for i, n in enumerate(names)}
 
         # timed region 3: end to end from pinned host memory (copies inside the events)
         out_y = torch.empty(y.shape, dtype=y.dtype, pin_memory=True)
@@ -312,14 +351,17 @@ def run_gpu(args, w: ssd_synth.Workload, rank: int, world: int, local_rank: int)
     if status != 0:
         raise RuntimeError("device status after timing: " + ssd.ssd_status_string(status))
 
-    ms, ms_e2e = max_over_ranks([statistics.mean(step_ms), statistics.mean(e2e_ms)], world, dev)
+    ms, ms_e2e = max_over_ranks([statistics.median(step_ms), statistics.median(e2e_ms)], world, dev)
     if rank != 0:
         return None
 
     flops, by = algorithmic(w)
     total_bytes = sum(by.values())
     pk = peaks()
-    tpeak = tensor_peak(pk, w.dtype)
+    tpeak = tensor_peak(pk, w.dtype, tf32_ratio)
+    tsrc = pk["source"] if w.dtype != "f32" else (
+        pk["source"] + " bf16 x " + ("tf32/bf16 cuBLAS rate ratio measured in this run" if tf32_ratio is not None
+                                     else "nominal GB300 tf32/bf16 ratio (1.1/2.25)"))
     t_roof_us = max(flops / (tpeak * 1e12), total_bytes / (pk["hbm_gbs"] * 1e9)) * 1e6
     tokens = w.tokens * world  # whole job (weak scaling)
     km = kernel_model(w)
@@ -338,8 +380,7 @@ def run_gpu(args, w: ssd_synth.Workload, rank: int, world: int, local_rank: int)
         "traffic": traffic,
         "kernel": dom,
         "algorithmic_per_launch": dk["flops"] if roof["bound"] == "tensor" else dk["bytes"],
-        "peak_source": pk["source"] + (" bf16 x nominal tf32/bf16 ratio" if roof["bound"] == "tensor"
-                                       and w.dtype == "f32" else ""),
+        "peak_source": tsrc if roof["bound"] == "tensor" else pk["source"],
     })
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = out_y.numel() * out_y.element_size() + out_f.numel() * out_f.element_size()
@@ -363,9 +404,11 @@ def run_gpu(args, w: ssd_synth.Workload, rank: int, world: int, local_rank: int)
         "tflops": flops * world / (ms * 1e-3) / 1e12,
         "step_roofline": {"t_roof_us": t_roof_us, "t_us": ms * 1e3, "frac": t_roof_us / (ms * 1e3),
                           "flops": flops, "bytes": total_bytes, "tensor_peak_tflops": tpeak,
-                          "hbm_peak_gbs": pk["hbm_gbs"], "peak_source": pk["source"]},
+                          "hbm_peak_gbs": pk["hbm_gbs"], "peak_source": tsrc,
+                          "tf32_over_bf16": tf32_ratio, "cublas_tflops": tf32_rates},
         "roofline": roof,
         "kernels_ms": per_kernel,
+        "timing": "median over steps (CUDA events on the launching stream)",
         "gpu_launches": ssd.ssd_fwd_kernel_count(shape) * args.steps,
         "schedule": "one-pass" if fused else "staged",
         "e2e": {"value": whole_job_tokens_per_s(w.tokens, world, ms_e2e), "unit": "tokens/s", "ms_per_step": ms_e2e,
@@ -441,6 +484,20 @@ def run_reference(args, w: ssd_synth.Workload):
 
 # ------------------------------------------------------------------ main
 
+def relaunch_one_rank_per_gpu(n: int, argv) -> int:
+    """``--gpus N`` started as a plain process: run this script again under
+    torch.distributed.run with N ranks on this node (rendezvous on 127.0.0.1,
+    a free port), passing the same arguments.  The ranks print through this
+    process's stdout (rank 0 alone prints the line); returns their exit code."""
+    import socket
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", str(n),
+           "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.abspath(__file__), *argv]
+    return subprocess.run(cmd).returncode
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -458,8 +515,8 @@ def main(argv=None):
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
-    if world == 1 and args.gpus > 1:
-        ap.error("--gpus N > 1 must be launched with torchrun (one rank per GPU)")
+    if world == 1 and args.gpus > 1 and "RANK" not in os.environ:
+        return relaunch_one_rank_per_gpu(args.gpus, sys.argv[1:] if argv is None else list(argv))
 
     if args.impl == "reference":
         if rank == 0:

@@ -163,6 +163,20 @@ ssd_status ssd_fused_pass(const ssd_shape* shape, const void* x, const void* Bm,
                           const float* init_state, void* y, float* final_state, void* workspace,
                           size_t workspace_bytes, ssd_stream_t stream);
 
+/* The launches ssd_fwd makes for `shape`, numbered 0 .. ssd_fwd_kernel_count()-1
+ * in the order ssd_fwd enqueues them, restricted to those with index in
+ * [first_launch, end_launch): the same kernels with the same arguments, so
+ * that calls covering consecutive ranges on one stream compute exactly what
+ * one ssd_fwd call computes.  Inside one call a launch overlaps the tail of
+ * the launch before it as in ssd_fwd; the first launch of a call waits for
+ * the work already on the stream.  Used to time the schedule's kernels one by
+ * one with events between the calls.  Arguments as for ssd_fwd;
+ * SSD_ERR_INVALID_ARG if first_launch < 0 or end_launch < first_launch. */
+ssd_status ssd_fwd_range(const ssd_shape* shape, const void* x, const float* dt, const float* A,
+                         const void* Bm, const void* Cm, const float* D, const float* init_state, void* y,
+                         float* final_state, void* workspace, size_t workspace_bytes, int first_launch,
+                         int end_launch, ssd_stream_t stream);
+
 /* After the caller has synchronised the stream of a call that used
  * `workspace`: SSD_OK, or SSD_ERR_DEVICE_TIMEOUT if a bounded wait inside a
  * kernel ran out (its outputs are then invalid).  Blocking 4-byte read. */
@@ -224,16 +238,23 @@ int ssd_fwd_kernel_count(const ssd_shape* shape);
  * can fail under memory pressure).  Such a caller passes only the inputs and
  * outputs of ssd_fwd; the workspace is a fixed array of
  * SSD_STATIC_SCRATCH_BYTES in the library's own device data, which every GPU
- * that loads the library holds until the process exits.  Nothing is
- * allocated by this call.
+ * that loads the library holds until the process exits.  The call itself
+ * allocates nothing.  Under lazy module loading (the CUDA default) the
+ * array's memory is committed when the library's device code first loads on
+ * a device, which is at the latest this entry point's first call there; make
+ * that first call at start-up (where an out-of-memory error can still be
+ * handled) and before any stream capture.
  *
  * Arguments, layouts, dtypes and supported shapes are those of ssd_fwd.
  * Returns SSD_ERR_WORKSPACE, before enqueuing anything, when
  * ssd_fwd_workspace_size(shape) is larger than SSD_STATIC_SCRATCH_BYTES.
- * The first call on a device looks up the array's device address
- * (cudaGetSymbolAddress) for that device, so make that first call before any
- * stream capture.  Each call clears the status word and then overwrites the
- * rest of the array; the array keeps the last call's intermediate results.
+ * The first call on a device also looks up the array's device address
+ * (cudaGetSymbolAddress) for that device; this set-up is one more reason to
+ * make it before any stream capture.  Argument errors are returned before
+ * anything is enqueued.
+ * A non-empty call's first kernel clears the status word and the one-pass
+ * counters before the rest of the array is overwritten; the array keeps the
+ * last call's intermediate results.
  * All calls share the one array: calls whose GPU work can overlap in time
  * (different streams, or threads without ordering between them) race and
  * give wrong results.  A device-timeout status (see ssd_fwd_check) is left in

@@ -26,7 +26,7 @@ STATUS = {0: "SSD_OK", 1: "SSD_ERR_INVALID_ARG", 2: "SSD_ERR_UNSUPPORTED", 3: "S
 EXPORTS = ("ssd_status_string", "ssd_validate_shape", "ssd_fwd_workspace_layout", "ssd_fwd_workspace_size",
            "ssd_fwd", "ssd_fwd_check", "ssd_chunk_cumsum", "ssd_chunk_state", "ssd_state_passing",
            "ssd_compute_out", "ssd_debug_timeout_probe", "ssd_fwd_kernel_count", "ssd_fwd_static_scratch",
-           "ssd_fwd_fused", "ssd_fused_pass")
+           "ssd_fwd_fused", "ssd_fused_pass", "ssd_fwd_range")
 
 # Size of the library's own workspace array used by ssd_fwd_static_scratch.
 SSD_STATIC_SCRATCH_BYTES = 32 << 20
@@ -77,6 +77,8 @@ def _load() -> ctypes.CDLL:
     lib.ssd_fwd.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     lib.ssd_fwd_fused.restype = c_int
     lib.ssd_fwd_fused.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    lib.ssd_fwd_range.restype = c_int
+    lib.ssd_fwd_range.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, c_int, c_int, vp]
     lib.ssd_fused_pass.restype = c_int
     lib.ssd_fused_pass.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     lib.ssd_fwd_check.restype = c_int
@@ -191,15 +193,66 @@ def workspace_views(shape: ssd_shape, ws: torch.Tensor) -> Dict[str, torch.Tenso
     return out
 
 
-def _check_inputs(x, dt, A, Bm, Cm, D):
-    for name, t in (("x", x), ("dt", dt), ("A", A), ("Bm", Bm), ("Cm", Cm), ("D", D)):
-        if not t.is_cuda or not t.is_contiguous():
+def expected_layouts(shape: ssd_shape) -> Dict[str, Tuple[Tuple[int, ...], Tuple[torch.dtype, ...]]]:
+    """Shape and dtype every tensor argument must have for ``shape`` (the
+    layouts include/ssd.h states): x, y [B,L,H,P] and Bm, Cm [B,L,G,N] in the
+    problem dtype; dt [B,L,H], A and D [H], init_state and final_state
+    [B,H,P,N] in fp32; the workspace a flat byte buffer."""
+    B, L, H, P, G, N = shape.batch, shape.seqlen, shape.nheads, shape.headdim, shape.ngroups, shape.dstate
+    io = torch.bfloat16 if shape.dtype == SSD_BF16 else torch.float32
+    f32 = (torch.float32,)
+    return {"x": ((B, L, H, P), (io,)), "y": ((B, L, H, P), (io,)), "Bm": ((B, L, G, N), (io,)),
+            "Cm": ((B, L, G, N), (io,)), "dt": ((B, L, H), f32), "A": ((H,), f32), "D": ((H,), f32),
+            "init_state": ((B, H, P, N), f32), "final_state": ((B, H, P, N), f32)}
+
+
+def check_tensors(shape: ssd_shape, device: Optional[torch.device] = None, require_cuda: bool = True,
+                  **tensors) -> torch.device:
+    """Checks every tensor argument of a call before anything reaches the C
+    library: each given tensor (None means "not passed") must live on the same
+    CUDA device, be contiguous and have exactly the shape and dtype of
+    ``expected_layouts(shape)``; ``workspace`` must be a byte tensor of at least
+    ssd_fwd_workspace_size(shape) bytes.  A host tensor or a short buffer would
+    otherwise become a device pointer or a tensor map the kernels read or write
+    past its end.  Raises SSDError (code 1, or 2 for an unsupported dtype);
+    returns the device.  ``require_cuda=False`` is for tests without a GPU."""
+    want = expected_layouts(shape)
+    for name, t in tensors.items():
+        if t is None:
+            continue
+        if not isinstance(t, torch.Tensor):
+            raise SSDError(1, f"{name} must be a torch.Tensor")
+        if require_cuda and not t.is_cuda:
+            raise SSDError(1, f"{name} must be a contiguous CUDA tensor (got {t.device})")
+        if device is None:
+            device = t.device
+        elif t.device != device:
+            raise SSDError(1, f"{name} is on {t.device}, the other arguments on {device}")
+        if not t.is_contiguous():
             raise SSDError(1, f"{name} must be a contiguous CUDA tensor")
-    if x.dtype not in (torch.float32, torch.bfloat16) or Bm.dtype != x.dtype or Cm.dtype != x.dtype:
+        if name == "workspace":
+            need = ssd_fwd_workspace_size(shape)
+            if t.dtype != torch.uint8 or t.dim() != 1:
+                raise SSDError(1, "workspace must be a 1-D uint8 tensor")
+            if t.numel() < need:
+                raise SSDError(3, f"workspace holds {t.numel()} bytes, the shape needs {need}")
+            continue
+        dims, dtypes = want[name]
+        if t.dtype not in dtypes:
+            code = 2 if name in ("x", "Bm", "Cm", "y") else 1
+            raise SSDError(code, f"{name} has dtype {t.dtype}, expected {dtypes[0]}")
+        if tuple(t.shape) != dims:
+            raise SSDError(1, f"{name} has shape {tuple(t.shape)}, expected {dims}")
+    return device
+
+
+def _shape_from(x, Bm, chunk_size: int) -> ssd_shape:
+    for name, t in (("x", x), ("Bm", Bm)):
+        if not isinstance(t, torch.Tensor) or t.dim() != 4:
+            raise SSDError(1, f"{name} must be a 4-D tensor")
+    if x.dtype not in (torch.float32, torch.bfloat16):
         raise SSDError(2, "x, Bm and Cm must share dtype float32 or bfloat16")
-    for name, t in (("dt", dt), ("A", A), ("D", D)):
-        if t.dtype != torch.float32:
-            raise SSDError(1, f"{name} must be float32")
+    return shape_of(x, Bm, chunk_size)
 
 
 # ------------------------------------------------------------------ entry points
@@ -212,18 +265,17 @@ def ssd_fwd(x: torch.Tensor, dt: torch.Tensor, A: torch.Tensor, Bm: torch.Tensor
     """The whole forward pass.  Returns (y, final_state).  ``schedule``:
     "auto" (C: ssd_fwd, which picks the schedule from the shape) or "fused"
     (C: ssd_fwd_fused, the one-pass kernel; bf16 only)."""
-    _check_inputs(x, dt, A, Bm, Cm, D)
     if schedule not in ("auto", "fused"):
         raise ValueError("schedule must be 'auto' or 'fused'")
-    shape = shape_of(x, Bm, chunk_size)
+    shape = _shape_from(x, Bm, chunk_size)
+    check_tensors(shape, x=x, dt=dt, A=A, Bm=Bm, Cm=Cm, D=D, init_state=init_state, y=y, final_state=final_state,
+                  workspace=workspace)
     B, L, H, P = x.shape
     N = Bm.shape[3]
     if y is None:
         y = torch.empty_like(x)
     if final_state is None and want_final_state:
         final_state = torch.empty(B, H, P, N, dtype=torch.float32, device=x.device)
-    if init_state is not None and (init_state.dtype != torch.float32 or not init_state.is_contiguous()):
-        raise SSDError(1, "init_state must be contiguous float32")
     if workspace is None:
         workspace = new_workspace(shape, x.device)
     fn = lib.ssd_fwd if schedule == "auto" else lib.ssd_fwd_fused
@@ -231,6 +283,24 @@ def ssd_fwd(x: torch.Tensor, dt: torch.Tensor, A: torch.Tensor, Bm: torch.Tensor
               _ptr(init_state), _ptr(y), _ptr(final_state), _ptr(workspace), workspace.numel(), _stream(stream))
     _check(code, "ssd_fwd" if schedule == "auto" else "ssd_fwd_fused")
     return y, final_state
+
+
+def ssd_fwd_range(x: torch.Tensor, dt: torch.Tensor, A: torch.Tensor, Bm: torch.Tensor, Cm: torch.Tensor,
+                  D: torch.Tensor, chunk_size: int, first_launch: int, end_launch: int,
+                  init_state: Optional[torch.Tensor] = None, y: Optional[torch.Tensor] = None,
+                  final_state: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                  stream=None) -> None:
+    """Launches [first_launch, end_launch) of the ones ssd_fwd makes for this
+    shape, with all of ssd_fwd's arguments (C: ssd_fwd_range).  The caller
+    passes the outputs and the workspace, which consecutive ranges share."""
+    shape = _shape_from(x, Bm, chunk_size)
+    check_tensors(shape, x=x, dt=dt, A=A, Bm=Bm, Cm=Cm, D=D, init_state=init_state, y=y, final_state=final_state,
+                  workspace=workspace)
+    if y is None or workspace is None:
+        raise SSDError(1, "ssd_fwd_range needs y and the workspace")
+    _check(lib.ssd_fwd_range(ctypes.byref(shape), _ptr(x), _ptr(dt), _ptr(A), _ptr(Bm), _ptr(Cm), _ptr(D),
+                             _ptr(init_state), _ptr(y), _ptr(final_state), _ptr(workspace), workspace.numel(),
+                             int(first_launch), int(end_launch), _stream(stream)), "ssd_fwd_range")
 
 
 def ssd_fwd_check(workspace: torch.Tensor) -> int:
@@ -242,6 +312,8 @@ def ssd_fused_pass(shape: ssd_shape, x: torch.Tensor, Bm: torch.Tensor, Cm: torc
                    init_state: Optional[torch.Tensor], y: torch.Tensor, final_state: Optional[torch.Tensor],
                    workspace: torch.Tensor, stream=None) -> None:
     """The one-pass kernel alone, after ssd_chunk_cumsum (C: ssd_fused_pass)."""
+    check_tensors(shape, x=x, Bm=Bm, Cm=Cm, D=D, init_state=init_state, y=y, final_state=final_state,
+                  workspace=workspace)
     _check(lib.ssd_fused_pass(ctypes.byref(shape), _ptr(x), _ptr(Bm), _ptr(Cm), _ptr(D), _ptr(init_state), _ptr(y),
                               _ptr(final_state), _ptr(workspace), workspace.numel(), _stream(stream)),
            "ssd_fused_pass")
@@ -249,24 +321,28 @@ def ssd_fused_pass(shape: ssd_shape, x: torch.Tensor, Bm: torch.Tensor, Cm: torc
 
 def ssd_chunk_cumsum(shape: ssd_shape, dt: torch.Tensor, A: torch.Tensor, workspace: torch.Tensor,
                      stream=None) -> None:
+    check_tensors(shape, dt=dt, A=A, workspace=workspace)
     _check(lib.ssd_chunk_cumsum(ctypes.byref(shape), _ptr(dt), _ptr(A), _ptr(workspace), workspace.numel(),
                                 _stream(stream)), "ssd_chunk_cumsum")
 
 
 def ssd_chunk_state(shape: ssd_shape, x: torch.Tensor, Bm: torch.Tensor, workspace: torch.Tensor,
                     stream=None) -> None:
+    check_tensors(shape, x=x, Bm=Bm, workspace=workspace)
     _check(lib.ssd_chunk_state(ctypes.byref(shape), _ptr(x), _ptr(Bm), _ptr(workspace), workspace.numel(),
                                _stream(stream)), "ssd_chunk_state")
 
 
 def ssd_state_passing(shape: ssd_shape, init_state: Optional[torch.Tensor], final_state: Optional[torch.Tensor],
                       workspace: torch.Tensor, stream=None) -> None:
+    check_tensors(shape, init_state=init_state, final_state=final_state, workspace=workspace)
     _check(lib.ssd_state_passing(ctypes.byref(shape), _ptr(init_state), _ptr(final_state), _ptr(workspace),
                                  workspace.numel(), _stream(stream)), "ssd_state_passing")
 
 
 def ssd_compute_out(shape: ssd_shape, x: torch.Tensor, Bm: torch.Tensor, Cm: torch.Tensor, D: torch.Tensor,
                     y: torch.Tensor, workspace: torch.Tensor, stream=None) -> None:
+    check_tensors(shape, x=x, Bm=Bm, Cm=Cm, D=D, y=y, workspace=workspace)
     _check(lib.ssd_compute_out(ctypes.byref(shape), _ptr(x), _ptr(Bm), _ptr(Cm), _ptr(D), _ptr(y),
                                _ptr(workspace), workspace.numel(), _stream(stream)), "ssd_compute_out")
 
@@ -397,8 +473,10 @@ def ssd_fwd_static_scratch(x: torch.Tensor, dt: torch.Tensor, A: torch.Tensor, B
     library's fixed SSD_STATIC_SCRATCH_BYTES device array, shared by every
     call (calls whose GPU work overlaps race).  Nothing is allocated here.
     """
-    _check_inputs(x, dt, A, Bm, Cm, D)
-    shape = shape_of(x, Bm, chunk_size)
+    shape = _shape_from(x, Bm, chunk_size)
+    check_tensors(shape, x=x, dt=dt, A=A, Bm=Bm, Cm=Cm, D=D, init_state=init_state, y=y, final_state=final_state)
+    if y is None:
+        raise SSDError(1, "y is required")
     code = lib.ssd_fwd_static_scratch(ctypes.byref(shape), _ptr(x), _ptr(dt), _ptr(A), _ptr(Bm), _ptr(Cm),
                                       _ptr(D), _ptr(init_state), _ptr(y), _ptr(final_state), _stream(stream))
     _check(code, "ssd_fwd_static_scratch")

@@ -216,9 +216,9 @@ bool use_fused(const ssd_shape& s) {
   return s.batch * (s.nheads / 2) >= sm_count();
 }
 
-ssd_status fwd_impl(int path, const ssd_shape* shape, const void* x, const float* dt, const float* A, const void* Bm,
-                    const void* Cm, const float* D, const float* init_state, void* y, float* final_state,
-                    void* workspace, size_t workspace_bytes, ssd_stream_t stream);
+ssd_status fwd_impl(int path, int first, int end, const ssd_shape* shape, const void* x, const float* dt,
+                    const float* A, const void* Bm, const void* Cm, const float* D, const float* init_state, void* y,
+                    float* final_state, void* workspace, size_t workspace_bytes, ssd_stream_t stream);
 
 bool build_fused_maps(const ssd_shape& s, const void* x, const void* Bm, const void* Cm, const void* y,
                       FusedMaps* m) {
@@ -364,7 +364,18 @@ ssd_status ssd_fwd(const ssd_shape* shape, const void* x, const float* dt, const
                    const void* Cm, const float* D, const float* init_state, void* y, float* final_state,
                    void* workspace, size_t workspace_bytes, ssd_stream_t stream) {
   const int path = shape && ssd_validate_shape(shape) == SSD_OK && use_fused(*shape) ? 1 : 0;
-  return fwd_impl(path, shape, x, dt, A, Bm, Cm, D, init_state, y, final_state, workspace, workspace_bytes, stream);
+  return fwd_impl(path, 0, 1 << 30, shape, x, dt, A, Bm, Cm, D, init_state, y, final_state, workspace,
+                  workspace_bytes, stream);
+}
+
+ssd_status ssd_fwd_range(const ssd_shape* shape, const void* x, const float* dt, const float* A, const void* Bm,
+                         const void* Cm, const float* D, const float* init_state, void* y, float* final_state,
+                         void* workspace, size_t workspace_bytes, int first_launch, int end_launch,
+                         ssd_stream_t stream) {
+  if (first_launch < 0 || end_launch < first_launch) return SSD_ERR_INVALID_ARG;
+  const int path = shape && ssd_validate_shape(shape) == SSD_OK && use_fused(*shape) ? 1 : 0;
+  return fwd_impl(path, first_launch, end_launch, shape, x, dt, A, Bm, Cm, D, init_state, y, final_state, workspace,
+                  workspace_bytes, stream);
 }
 
 ssd_status ssd_fused_pass(const ssd_shape* shape, const void* x, const void* Bm, const void* Cm, const float* D,
@@ -391,7 +402,8 @@ ssd_status ssd_fwd_fused(const ssd_shape* shape, const void* x, const float* dt,
                          const void* Cm, const float* D, const float* init_state, void* y, float* final_state,
                          void* workspace, size_t workspace_bytes, ssd_stream_t stream) {
   if (shape && ssd_validate_shape(shape) == SSD_OK && shape->dtype != SSD_BF16) return SSD_ERR_UNSUPPORTED;
-  return fwd_impl(1, shape, x, dt, A, Bm, Cm, D, init_state, y, final_state, workspace, workspace_bytes, stream);
+  return fwd_impl(1, 0, 1 << 30, shape, x, dt, A, Bm, Cm, D, init_state, y, final_state, workspace, workspace_bytes,
+                  stream);
 }
 
 }  // extern "C"
@@ -399,10 +411,12 @@ ssd_status ssd_fwd_fused(const ssd_shape* shape, const void* x, const float* dt,
 namespace ssd {
 namespace {
 
-// path: 0 staged, 1 one-pass
-ssd_status fwd_impl(int path, const ssd_shape* shape, const void* x, const float* dt, const float* A, const void* Bm,
-                    const void* Cm, const float* D, const float* init_state, void* y, float* final_state,
-                    void* workspace, size_t workspace_bytes, ssd_stream_t stream) {
+// path: 0 staged, 1 one-pass.  Enqueues the schedule's launches with index in
+// [first, end); a launch is a programmatic dependent only of a launch of the
+// same call (the first one enqueued here is an ordinary stream-ordered launch).
+ssd_status fwd_impl(int path, int first, int end, const ssd_shape* shape, const void* x, const float* dt,
+                    const float* A, const void* Bm, const void* Cm, const float* D, const float* init_state, void* y,
+                    float* final_state, void* workspace, size_t workspace_bytes, ssd_stream_t stream) {
   ssd_workspace_layout L;
   ssd_status st = check_workspace(shape, workspace, workspace_bytes, &L);
   if (st != SSD_OK) return st;
@@ -414,18 +428,27 @@ ssd_status fwd_impl(int path, const ssd_shape* shape, const void* x, const float
   }
   if ((init_state && !aligned16(init_state)) || (final_state && !aligned16(final_state)))
     return SSD_ERR_INVALID_ARG;
-  if (empty_problem(*shape)) return ssd_state_passing(shape, init_state, final_state, workspace, workspace_bytes, stream);
+  if (empty_problem(*shape))
+    return first == 0 && end > 0 ? ssd_state_passing(shape, init_state, final_state, workspace, workspace_bytes, stream)
+                                 : SSD_OK;
   // build every tensor map before the first launch, so an encoding failure enqueues nothing
   const bool bf16 = shape->dtype == SSD_BF16;
   Work w = carve(workspace, L, bf16);
+  const Dims d = make_dims(*shape);
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaSuccess;
+  int k = 0;  // index of the next launch of the schedule
+  auto step = [&](auto&& launch) {
+    if (e == cudaSuccess && k >= first && k < end) e = launch(k > first);
+    ++k;
+  };
   if (path == 1) {
     FusedMaps fmaps;
     if (!build_fused_maps(*shape, x, Bm, Cm, y, &fmaps)) return SSD_ERR_CUDA;
-    const Dims d = make_dims(*shape);
-    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-    cudaError_t e = launch_chunk_cumsum(d, dt, A, w, cs);
-    if (e == cudaSuccess)
-      e = launch_fused(d, fmaps, D, x, init_state, final_state, w, spin_limit_ns(), cs, true);
+    step([&](bool) { return launch_chunk_cumsum(d, dt, A, w, cs); });
+    step([&](bool dep) {
+      return launch_fused(d, fmaps, D, x, init_state, final_state, w, spin_limit_ns(), cs, dep);
+    });
     return from_cuda(e);
   }
   ChunkStateMaps smaps;
@@ -433,20 +456,18 @@ ssd_status fwd_impl(int path, const ssd_shape* shape, const void* x, const float
   const void* hp = bf16 ? static_cast<const void*>(w.states_bf16) : static_cast<const void*>(w.states);
   if (!build_state_maps(*shape, x, Bm, w.states, &smaps) || !build_out_maps(*shape, x, Bm, Cm, hp, y, &omaps))
     return SSD_ERR_CUDA;
-  const Dims d = make_dims(*shape);
-  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   const uint64_t spin = spin_limit_ns();
   // fp32: the chunk_cumsum launch also transposes Bm once for every head of its group
-  cudaError_t e = launch_chunk_cumsum(d, dt, A, w, cs, bf16 ? nullptr : Bm);
+  step([&](bool) { return launch_chunk_cumsum(d, dt, A, w, cs, bf16 ? nullptr : Bm); });
   // chunk_state and compute_out are programmatic dependents of the kernel before them (their
   // launch and prologue overlap its tail).  state_passing is one only while chunk_state runs
   // in a single wave (two CTAs per SM): launched early beside a later wave, its blocks slowed
   // long sequences (16k tokens x dstate 256: 0.397 against 0.381 ms), while on a one-wave
   // problem the early launch saves about 1 us (370M layer: 0.0897 against 0.0908 ms).
   const bool one_wave = static_cast<int64_t>(d.B) * d.nc * (d.H / 2) <= 2 * static_cast<int64_t>(sm_count());
-  if (e == cudaSuccess) e = launch_chunk_state(d, bf16, smaps, w, spin, cs, true);
-  if (e == cudaSuccess) e = launch_state_passing(d, bf16, init_state, final_state, w, cs, one_wave);
-  if (e == cudaSuccess) e = launch_compute_out(d, bf16, omaps, D, x, y, w, spin, cs, true);
+  step([&](bool dep) { return launch_chunk_state(d, bf16, smaps, w, spin, cs, dep); });
+  step([&](bool dep) { return launch_state_passing(d, bf16, init_state, final_state, w, cs, one_wave && dep); });
+  step([&](bool dep) { return launch_compute_out(d, bf16, omaps, D, x, y, w, spin, cs, dep); });
   return from_cuda(e);
 }
 

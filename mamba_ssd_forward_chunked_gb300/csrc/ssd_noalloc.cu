@@ -57,12 +57,8 @@ extern "C" ssd_status ssd_fwd_static_scratch(const ssd_shape* shape, const void*
   void* scratch = nullptr;
   st = scratch_on_current_device(&scratch);
   if (st != SSD_OK) return st;
-  // The array keeps the previous call's contents: start from a clean status word.
-  ssd_workspace_layout L;
-  st = ssd_fwd_workspace_layout(shape, &L);
-  if (st != SSD_OK) return st;
-  if (cudaMemsetAsync(static_cast<unsigned char*>(scratch) + L.status, 0, sizeof(int),
-                      reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
-    return SSD_ERR_CUDA;
+  // Nothing is enqueued here: ssd_fwd checks every pointer first, and for a
+  // non-empty problem its first kernel clears the status word and the one-pass
+  // counters, so the previous call's contents of the array never leak into this one.
   return ssd_fwd(shape, x, dt, A, Bm, Cm, D, init_state, y, final_state, scratch, kSsdStaticScratchBytes, stream);
 }

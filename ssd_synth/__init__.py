@@ -70,16 +70,54 @@ def uniform01(seed: int, stream: int, count: int, offset: int = 0) -> np.ndarray
     return ((z >> np.uint64(11)).astype(np.float64) + 0.5) * (1.0 / 9007199254740992.0)
 
 
+def _box_muller(u: np.ndarray) -> np.ndarray:
+    """Normals from consecutive uniform pairs (u1, u2): sqrt(-2 ln u1) times cos / sin of 2 pi u2."""
+    u1, u2 = u[0::2], u[1::2]
+    r = np.sqrt(-2.0 * np.log(u1))
+    out = np.empty(u.shape[0], dtype=np.float64)
+    out[0::2] = r * np.cos(2.0 * math.pi * u2)
+    out[1::2] = r * np.sin(2.0 * math.pi * u2)
+    return out
+
+
 def normal(seed: int, stream: int, count: int) -> np.ndarray:
     """``count`` standard normals (float64) by Box-Muller on uniform pairs."""
     npairs = (count + 1) // 2
-    u = uniform01(seed, stream, 2 * npairs)
-    u1, u2 = u[0::2], u[1::2]
-    r = np.sqrt(-2.0 * np.log(u1))
-    out = np.empty(2 * npairs, dtype=np.float64)
-    out[0::2] = r * np.cos(2.0 * math.pi * u2)
-    out[1::2] = r * np.sin(2.0 * math.pi * u2)
-    return out[:count]
+    return _box_muller(uniform01(seed, stream, 2 * npairs))[:count]
+
+
+_CHUNK_PAIRS = 1 << 20
+
+
+def normal_f32(seed: int, stream: int, count: int, scale: float = 1.0, bf16: bool = False) -> np.ndarray:
+    """``(normal(seed, stream, count) * scale)`` as float32 (rounded on to bf16
+    values when ``bf16``), computed in independent slices of the stream on a
+    few threads.  Element i depends only on i (the generator is counter-based
+    and each Box-Muller pair is whole inside a slice), so this is the same
+    function of the index as ``normal``; the slices only keep large tensors
+    fast to draw."""
+    import concurrent.futures as cf
+    out = np.empty(count, dtype=np.float32)
+    npairs = (count + 1) // 2
+
+    def fill(p0: int) -> None:
+        p1 = min(npairs, p0 + _CHUNK_PAIRS)
+        v = _box_muller(uniform01(seed, stream, 2 * (p1 - p0), offset=2 * p0))
+        if scale != 1.0:
+            v *= scale
+        lo, hi = 2 * p0, min(count, 2 * p1)
+        f = v[: hi - lo].astype(np.float32)
+        out[lo:hi] = round_to_bf16(f) if bf16 else f
+
+    starts = range(0, npairs, _CHUNK_PAIRS)
+    if npairs <= _CHUNK_PAIRS:
+        for p0 in starts:
+            fill(p0)
+    else:
+        import os
+        with cf.ThreadPoolExecutor(max_workers=min(16, os.cpu_count() or 4)) as ex:
+            list(ex.map(fill, starts))
+    return out
 
 
 def round_to_bf16(a: np.ndarray) -> np.ndarray:
@@ -147,8 +185,11 @@ def make_inputs(w: Workload, seed: Optional[int] = None) -> Dict[str, np.ndarray
     """
     s = w.seed if seed is None else seed
     B, L, H, P, N, G = w.batch, w.seqlen, w.nheads, w.headdim, w.dstate, w.ngroups
+    if w.dtype not in ("bf16", "f32"):
+        raise ValueError(f"unknown dtype {w.dtype!r}")
+    low = w.dtype == "bf16"  # x, Bm and Cm stored as bf16 values
     out: Dict[str, np.ndarray] = {}
-    out["x"] = normal(s, STREAM_IDS["x"], B * L * H * P).astype(np.float32).reshape(B, L, H, P)
+    out["x"] = normal_f32(s, STREAM_IDS["x"], B * L * H * P, bf16=low).reshape(B, L, H, P)
     z = normal(s, STREAM_IDS["dt"], B * L * H)
     v = z - 4.6
     softplus = np.where(v > 20.0, v, np.log1p(np.exp(np.minimum(v, 20.0))))
@@ -156,16 +197,11 @@ def make_inputs(w: Workload, seed: Optional[int] = None) -> Dict[str, np.ndarray
     u = uniform01(s, STREAM_IDS["A"], H)
     out["A"] = (-np.exp(u * math.log(16.0))).astype(np.float32)
     scale = 1.0 / math.sqrt(N)
-    out["Bm"] = (normal(s, STREAM_IDS["Bm"], B * L * G * N) * scale).astype(np.float32).reshape(B, L, G, N)
-    out["Cm"] = (normal(s, STREAM_IDS["Cm"], B * L * G * N) * scale).astype(np.float32).reshape(B, L, G, N)
+    out["Bm"] = normal_f32(s, STREAM_IDS["Bm"], B * L * G * N, scale, bf16=low).reshape(B, L, G, N)
+    out["Cm"] = normal_f32(s, STREAM_IDS["Cm"], B * L * G * N, scale, bf16=low).reshape(B, L, G, N)
     out["D"] = normal(s, STREAM_IDS["D"], H).astype(np.float32)
     if w.init_state:
-        out["init"] = (normal(s, STREAM_IDS["init"], B * H * P * N) * 0.1).astype(np.float32).reshape(B, H, P, N)
-    if w.dtype == "bf16":
-        for k in ("x", "Bm", "Cm"):
-            out[k] = round_to_bf16(out[k])
-    elif w.dtype != "f32":
-        raise ValueError(f"unknown dtype {w.dtype!r}")
+        out["init"] = normal_f32(s, STREAM_IDS["init"], B * H * P * N, 0.1).reshape(B, H, P, N)
     return out
 
 

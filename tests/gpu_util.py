@@ -42,6 +42,40 @@ def run_gpu(inp: Dict[str, np.ndarray], dtype: str, Q: int, with_init: Optional[
     return y.float().cpu().numpy().astype(np.float64), fin.cpu().numpy().astype(np.float64)
 
 
+def run_gpu_schedule(d: Dict[str, torch.Tensor], Q: int, schedule: str):
+    """One forward pass on device tensors ``d`` through the C ABI.  schedule:
+    "auto" (ssd_fwd picks), "fused" (the one-pass kernel, ssd_fwd_fused) or
+    "staged" (the four step entry points in order: the staged schedule for
+    any shape).  Returns (y, final_state) on the device."""
+    import mamba_ssd_forward_chunked_gb300 as ssd
+    init = d.get("init")
+    if schedule in ("auto", "fused"):
+        return ssd.ssd_fwd(d["x"], d["dt"], d["A"], d["Bm"], d["Cm"], d["D"], Q, init_state=init,
+                           schedule=schedule)
+    assert schedule == "staged", schedule
+    shape = ssd.shape_of(d["x"], d["Bm"], Q)
+    ws = ssd.new_workspace(shape)
+    B, L, H, P = d["x"].shape
+    y = torch.empty_like(d["x"])
+    fin = torch.empty(B, H, P, d["Bm"].shape[3], dtype=torch.float32, device=d["x"].device)
+    ssd.ssd_chunk_cumsum(shape, d["dt"], d["A"], ws)
+    ssd.ssd_chunk_state(shape, d["x"], d["Bm"], ws)
+    ssd.ssd_state_passing(shape, init, fin, ws)
+    ssd.ssd_compute_out(shape, d["x"], d["Bm"], d["Cm"], d["D"], y, ws)
+    assert ssd.ssd_fwd_check(ws) == 0
+    return y, fin
+
+
+def pair_rows(y: torch.Tensor, fin: torch.Tensor, pairs: np.ndarray):
+    """The sampled (b, h) pairs' outputs, gathered on the device: y[b, :, h]
+    stacked as [k, L, P] and final_state[b, h] as [k, P, N], in fp64 on the host."""
+    bi = torch.as_tensor(pairs[:, 0], device=y.device)
+    hi = torch.as_tensor(pairs[:, 1], device=y.device)
+    ys = y[bi, :, hi].float().cpu().numpy().astype(np.float64)
+    fs = fin[bi, hi].cpu().numpy().astype(np.float64)
+    return ys, fs
+
+
 def sampled_pairs(B: int, H: int, k: int, seed: int = 0) -> np.ndarray:
     """k (b, h) pairs spread over the batch and heads, always with the first
     and last head and batch."""

@@ -103,6 +103,14 @@ def test_argument_errors_before_any_launch(ext):
     bad = shape(ext, dstate=96)
     assert lib.ssd_fwd(by(bad), fake, fake, fake, fake, fake, fake, None, fake, None, fake, need, None) == 2
     assert lib.ssd_fwd_check(None) == 1
+    # launch ranges: a negative start or an inverted range, then the same checks as ssd_fwd
+    for a, b in ((-1, 1), (2, 1)):
+        assert lib.ssd_fwd_range(by(s), fake, fake, fake, fake, fake, fake, None, fake, None, fake, need, a, b,
+                                 None) == 1
+    assert lib.ssd_fwd_range(by(s), None, fake, fake, fake, fake, fake, None, fake, None, fake, need, 0, 1,
+                             None) == 1
+    assert lib.ssd_fwd_range(by(s), fake, fake, fake, fake, fake, fake, None, fake, None, fake, need - 1, 0, 1,
+                             None) == 3
     assert lib.ssd_debug_timeout_probe(None, 10, None) == 1
     assert lib.ssd_debug_timeout_probe(fake, 0, None) == 1
 
@@ -189,3 +197,41 @@ def test_binding_refuses_host_tensors(ext):
     with pytest.raises(ext.SSDError) as e:
         ext.ssd_fwd(x, dt, A, Bm, Cm, D, 64)
     assert e.value.code == 1 and "CUDA" in str(e.value)
+
+
+def test_binding_checks_every_tensor_argument(ext):
+    """Every tensor a call passes is checked against the shape before the C
+    library sees it: device (host tensors and mixed devices), dtype, exact
+    shape, contiguity and the workspace's size.  A host output, a short Cm or
+    an undersized buffer would otherwise reach the kernels as a bad pointer."""
+    import torch
+    s = ext.make_shape(2, 64, 4, 64, 1, 64, 64, ext.SSD_F32)
+    lay = ext.expected_layouts(s)
+    good = {k: torch.zeros(dims, dtype=dts[0]) for k, (dims, dts) in lay.items()}
+    ws = torch.zeros(ext.ssd_fwd_workspace_size(s), dtype=torch.uint8)
+    # the full argument set passes (no GPU: the CUDA requirement is lifted for the test)
+    ext.check_tensors(s, require_cuda=False, workspace=ws, **good)
+
+    def rejects(code, **bad):
+        args = dict(good, workspace=ws)
+        args.update(bad)
+        with pytest.raises(ext.SSDError) as e:
+            ext.check_tensors(s, require_cuda=False, **args)
+        assert e.value.code == code, (bad.keys(), e.value)
+
+    rejects(1, Cm=torch.zeros(2, 63, 1, 64))                      # short Cm
+    rejects(1, dt=torch.zeros(2, 64, 3))                          # dt for fewer heads
+    rejects(1, D=torch.zeros(5))                                  # D for more heads
+    rejects(1, final_state=torch.zeros(2, 4, 64, 32))             # undersized final state
+    rejects(1, init_state=torch.zeros(2, 4, 64, 64, dtype=torch.float64))
+    rejects(2, y=torch.zeros(2, 64, 4, 64, dtype=torch.bfloat16))  # y in another dtype than x
+    rejects(1, y=torch.zeros(2, 64, 64, 4).transpose(2, 3))       # right shape, not contiguous
+    rejects(3, workspace=ws[:-1])                                 # workspace one byte short
+    rejects(1, workspace=torch.zeros(ws.numel() // 4, dtype=torch.int32))
+    rejects(1, y=torch.zeros(2, 64, 4, 64, device="meta"))        # another device than the rest
+    # with the CUDA requirement (the default), any host tensor is refused, outputs included
+    for name in ("y", "final_state", "init_state", "workspace"):
+        t = ws if name == "workspace" else good[name]
+        with pytest.raises(ext.SSDError) as e:
+            ext.check_tensors(s, **{name: t})
+        assert e.value.code == 1 and "CUDA" in str(e.value)

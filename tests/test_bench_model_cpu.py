@@ -1,6 +1,6 @@
 """bench.py's host-side arithmetic, on CPU: the per-kernel byte and flop model
-adds up to the step's algorithmic totals, the TF32 peak follows the nominal
-TF32/bf16 ratio, the clock summary reads nvidia-smi's CSV lines, and a DRAM
+adds up to the step's algorithmic totals, the TF32 peak is the bf16 peak times
+the measured (else the nominal) TF32/bf16 ratio, the clock summary reads nvidia-smi's CSV lines, and a DRAM
 traffic record is used only while its kernel's source file is unchanged."""
 import hashlib
 import json
@@ -30,10 +30,12 @@ def test_kernel_model_adds_up(name):
     assert by["init"] == (by["final"] if w.init_state else 0)
 
 
-def test_tf32_peak_is_the_nominal_fraction_of_bf16():
+def test_tf32_peak_is_the_measured_or_nominal_fraction_of_bf16():
     pk = {"bf16_tflops": 1930.0}
     assert bench.tensor_peak(pk, "bf16") == 1930.0
+    assert bench.tensor_peak(pk, "bf16", 0.3) == 1930.0  # the ratio applies to TF32 problems only
     assert bench.tensor_peak(pk, "f32") == pytest.approx(1930.0 * 1.1 / 2.25)
+    assert bench.tensor_peak(pk, "f32", 0.5) == pytest.approx(965.0)
 
 
 def test_clock_summary_parses_nvidia_smi_lines():

@@ -120,3 +120,27 @@ def test_full_forward_equals_the_four_steps(name, over):
     assert torch.equal(f1, f2)
     if w.dtype == "f32":
         assert torch.equal(ssd.workspace_views(shape, ws)["bT"], ssd.workspace_views(shape, ws2)["bT"])
+
+
+@pytest.mark.parametrize("over", [CASES[1][1], CASES[3][1], CASES[4][1],
+                                  dict(batch=16, seqlen=384, nheads=20, dstate=128, chunk_size=128, dtype="bf16",
+                                       init_state=True)],
+                         ids=["f32-N128", "f32-N256-ragged", "bf16-staged-G2", "bf16-one-pass"])
+def test_launch_ranges_equal_the_full_forward(over):
+    """ssd_fwd_range over each single launch in turn (how the bench times the
+    schedule's kernels) gives bit for bit what one ssd_fwd call gives, on
+    both schedules."""
+    ssd, w, inp, d, shape, ws = _setup(over)
+    n = ssd.ssd_fwd_kernel_count(shape)
+    B, L, H = inp["dt"].shape
+    y1, f1 = ssd.ssd_fwd(d["x"], d["dt"], d["A"], d["Bm"], d["Cm"], d["D"], w.chunk_size,
+                         init_state=d.get("init"), workspace=ws)
+    ws2 = torch.zeros_like(ws)
+    y2 = torch.empty_like(d["x"])
+    f2 = torch.empty(B, H, 64, w.dstate, device="cuda")
+    for i in range(n):
+        ssd.ssd_fwd_range(d["x"], d["dt"], d["A"], d["Bm"], d["Cm"], d["D"], w.chunk_size, i, i + 1,
+                          init_state=d.get("init"), y=y2, final_state=f2, workspace=ws2)
+    torch.cuda.synchronize()
+    assert torch.equal(y1, y2) and torch.equal(f1, f2)
+    assert ssd.ssd_fwd_check(ws2) == 0

@@ -15,7 +15,7 @@ import torch
 
 import oracle
 import ssd_synth
-from gpu_util import TOL, compare_with_oracle, rel_err, run_gpu, sampled_pairs, to_device
+from gpu_util import TOL, compare_with_oracle, pair_rows, rel_err, run_gpu, run_gpu_schedule, sampled_pairs, to_device
 
 pytestmark = pytest.mark.gpu
 W = ssd_synth.WORKLOADS
@@ -38,13 +38,38 @@ def test_full_size_sampled(name, k):
     assert ey <= TOL[w.dtype] and ef <= TOL[w.dtype], (ey, ef)
 
 
-@pytest.mark.parametrize("name", ["sweep-L512-N64-Q128", "sweep-L2048-N128-Q256", "sweep-L32768-N256-Q256",
-                                  "sweep-L8192-N256-Q128"])
+SWEEP = sorted(n for n in W if n.startswith("sweep-"))
+
+
+@pytest.mark.parametrize("name", SWEEP)
 def test_sweep_points_sampled(name):
+    """Every point of the 65,536-token shape sweep (bf16, 64 heads in 8 groups),
+    at full size, against the oracle on sampled (batch, head) pairs: the
+    schedule ssd_fwd picks, and the other one too (the one-pass kernel, or the
+    staged kernels through the four step calls).  The staged bf16 path stores
+    chunk and entering states in bf16; L 32768 at chunk 128 is its longest
+    chain (256 chunks)."""
+    import mamba_ssd_forward_chunked_gb300 as ssd
     w = W[name]
+    assert len(SWEEP) == 24
+    inp = ssd_synth.make_inputs(w)
     pairs = sampled_pairs(w.batch, w.nheads, 6)
-    ey, ef, _, _ = compare_with_oracle(w, pairs=pairs)
-    assert ey <= TOL[w.dtype] and ef <= TOL[w.dtype], (ey, ef)
+    yr, fr, _ = oracle.recurrence(inp, pairs=pairs)
+    yrs = np.stack([yr[b, :, h] for b, h in pairs])
+    frs = np.stack([fr[b, h] for b, h in pairs])
+    del yr, fr
+    d = to_device(inp, w.dtype)
+    del inp
+    shape = ssd.shape_of(d["x"], d["Bm"], w.chunk_size)
+    picked = "fused" if ssd.ssd_fwd_kernel_count(shape) == 2 else "staged"
+    for schedule in ("auto", "staged" if picked == "fused" else "fused"):
+        y, f = run_gpu_schedule(d, w.chunk_size, schedule)
+        torch.cuda.synchronize()
+        ys, fs = pair_rows(y, f, pairs)
+        del y, f
+        assert np.all(np.isfinite(ys))
+        ey, ef = rel_err(ys, yrs), rel_err(fs, frs)
+        assert ey <= TOL[w.dtype] and ef <= TOL[w.dtype], (schedule, picked, ey, ef)
 
 
 SMALL = [

@@ -28,17 +28,25 @@ def _static_call(ssd, d, Q, y, fin, init):
                                           torch.cuda.current_stream().cuda_stream)
 
 
-@pytest.mark.parametrize("over", [
-    dict(seqlen=300, nheads=4, dstate=128, chunk_size=128, dtype="f32", init_state=True),
-    dict(batch=2, seqlen=640, nheads=8, ngroups=2, dstate=64, chunk_size=256, dtype="bf16"),
-], ids=["f32", "bf16"])
-def test_static_scratch_matches_ssd_fwd_twice(over):
+@pytest.mark.parametrize("over,kernels", [
+    (dict(seqlen=300, nheads=4, dstate=128, chunk_size=128, dtype="f32", init_state=True), 4),
+    (dict(batch=2, seqlen=640, nheads=8, ngroups=2, dstate=64, chunk_size=256, dtype="bf16"), 4),
+    # enough (batch, head pair) sequences for the one-pass schedule, whose window
+    # counter and flags live in the shared array and are reused call after call
+    (dict(batch=16, seqlen=256, nheads=32, dstate=64, chunk_size=128, dtype="bf16", init_state=True), 2),
+], ids=["f32", "bf16", "bf16-one-pass"])
+def test_static_scratch_matches_ssd_fwd_twice(over, kernels):
     import mamba_ssd_forward_chunked_gb300 as ssd
     results = []
     for seed in (1, 2):  # two calls in a row on different inputs
         w = ssd_synth.custom("noalloc", seed=seed, **over)
         inp = ssd_synth.make_inputs(w)
         d = to_device(inp, w.dtype)
+        shape = ssd.shape_of(d["x"], d["Bm"], w.chunk_size)
+        assert ssd.ssd_fwd_workspace_size(shape) <= ssd.SSD_STATIC_SCRATCH_BYTES
+        if kernels == 2 and torch.cuda.get_device_properties(0).multi_processor_count > w.batch * w.nheads // 2:
+            pytest.skip("fewer (batch, head pair) sequences than multiprocessors: ssd_fwd stays staged")
+        assert ssd.ssd_fwd_kernel_count(shape) == kernels
         init = d.get("init")
         y_ref, f_ref = ssd.ssd_fwd(d["x"], d["dt"], d["A"], d["Bm"], d["Cm"], d["D"], w.chunk_size,
                                    init_state=init)
@@ -63,3 +71,20 @@ def test_static_scratch_rejects_problems_beyond_its_size():
     code = ssd.lib.ssd_fwd_static_scratch(ctypes.byref(shape), fake, fake, fake, fake, fake, fake, None, fake, None,
                                           None)
     assert code == 3  # SSD_ERR_WORKSPACE
+
+
+def test_static_scratch_refuses_bad_pointers():
+    """A null or misaligned pointer is refused with SSD_ERR_INVALID_ARG (the entry
+    point enqueues nothing of its own before ssd_fwd's pointer checks)."""
+    import mamba_ssd_forward_chunked_gb300 as ssd
+    w = ssd_synth.custom("noalloc", seqlen=128, nheads=4, dstate=64, chunk_size=64, dtype="f32")
+    d = to_device(ssd_synth.make_inputs(w), w.dtype)
+    y = torch.empty_like(d["x"])
+    shape = ssd.shape_of(d["x"], d["Bm"], w.chunk_size)
+    p = lambda t: None if t is None else t.data_ptr()  # noqa: E731
+    st = torch.cuda.current_stream().cuda_stream
+    assert ssd.lib.ssd_fwd_static_scratch(ctypes.byref(shape), None, p(d["dt"]), p(d["A"]), p(d["Bm"]), p(d["Cm"]),
+                                          p(d["D"]), None, p(y), None, st) == 1
+    assert ssd.lib.ssd_fwd_static_scratch(ctypes.byref(shape), p(d["x"]), p(d["dt"]), p(d["A"]), p(d["Bm"]),
+                                          p(d["Cm"]), p(d["D"]), None, p(y) + 4, None, st) == 1
+    torch.cuda.synchronize()
