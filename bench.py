@@ -47,7 +47,7 @@ PRE_STEP_SLEEP_CYCLES = 200_000
 # when the live measurement below cannot run.
 NOMINAL_TF32_OVER_BF16 = 1.1 / 2.25
 KERNELS = ("chunk_cumsum", "chunk_state", "state_passing", "compute_out")  # staged schedule
-FUSED_KERNELS = ("chunk_cumsum", "ssd_fused")                                # one-pass schedule
+FUSED_KERNELS = ("causal_cb", "ssd_onepass")                                 # one-pass schedule
 
 
 # ------------------------------------------------------------------ model of the work
@@ -76,17 +76,18 @@ def kernel_model(w: ssd_synth.Workload):
     touch and its share of the algorithmic flops (intermediate workspace
     traffic is overhead and not counted)."""
     flops, by = algorithmic(w)
-    B, L, H, P, N, Q = w.batch, w.seqlen, w.nheads, w.headdim, w.dstate, w.chunk_size
+    B, L, H, P, N, G, Q = w.batch, w.seqlen, w.nheads, w.headdim, w.dstate, w.ngroups, w.chunk_size
     nc = -(-L // Q)
     f_state = B * nc * H * 2 * Q * N * P
+    f_cb = B * nc * G * N * Q * (Q + 1)
     return {
         "chunk_cumsum": {"bytes": by["dt"] + by["AD"] // 2, "flops": 0},
         "chunk_state": {"bytes": by["x"] + by["BmCm"] // 2, "flops": f_state},
         "state_passing": {"bytes": by["final"] + by["init"], "flops": 0},
         "compute_out": {"bytes": by["x"] + by["y"] + by["BmCm"] + by["AD"] // 2, "flops": flops - f_state},
-        # one-pass kernel: everything but dt (read by chunk_cumsum) and A
-        "ssd_fused": {"bytes": by["x"] + by["y"] + by["BmCm"] + by["AD"] // 2 + by["final"] + by["init"],
-                      "flops": flops},
+        # one-pass schedule: the causal C B^T blocks (Bm, Cm read), then everything of the step
+        "causal_cb": {"bytes": by["BmCm"], "flops": f_cb},
+        "ssd_onepass": {"bytes": sum(by.values()), "flops": flops - f_cb},
     }
 
 

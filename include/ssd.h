@@ -92,6 +92,10 @@ typedef struct {
  *               one run of windows to the next, per head pair in a layout of
  *               its own ([N/32][8][2*P rows][4]: a warp's 16-byte accesses are
  *               consecutive)
+ *   cbm         (SSD_BF16 only) bf16 [B][nw][G][128][128], nw = ceil(seqlen/128):
+ *               for every 128-token window and group the causal select of
+ *               C B^T, M[i][j] = c_i . b_j for j <= i and 0 above the
+ *               diagonal (one-pass schedule, written by its first step)
  *   bT          (SSD_F32 only) fp32, B*G*Lp*N values: Bm in 4 KB boxes of 32
  *               tokens x 32 dstate, transposed (a row is one dstate index),
  *               rounded to TF32 and 128-byte swizzled -- the K-major operand
@@ -108,6 +112,7 @@ typedef struct {
   size_t chain;
   size_t hslot;
   size_t bT;
+  size_t cbm;
   size_t total;
 } ssd_workspace_layout;
 
@@ -126,10 +131,13 @@ size_t ssd_fwd_workspace_size(const ssd_shape* shape);
 
 /* The whole forward pass, enqueued on `stream`.  Two schedules give the
  * recurrence's result (see the steps below for the formulas):
- *  - one-pass (ssd_fwd_fused): chunk_cumsum, then one persistent kernel that
- *    computes each window's state on the tensor core, chains the states
- *    between windows through the workspace (or final_state), and writes y;
- *    x, Bm and Cm are read once.  SSD_BF16 only.
+ *  - one-pass (ssd_fwd_fused; SSD_BF16 only): ssd_causal_cb, then one
+ *    persistent kernel (ssd_fused_pass) that runs every 128-token window of a
+ *    (batch, head pair): the window's cumulative decay, its state product on
+ *    the tensor core accumulated onto the running state, the carried-state
+ *    and intra-window products and y; the state moves between windows in
+ *    tensor memory and between runs of windows through the workspace (or
+ *    final_state).  x is read once and the states never reach HBM.
  *  - staged: chunk_cumsum, chunk_state, state_passing and compute_out
  *    (SSD_F32: the chunk_cumsum launch also transposes Bm into the workspace,
  *    once for every head of a group; ssd_chunk_state called alone does that
@@ -137,7 +145,9 @@ size_t ssd_fwd_workspace_size(const ssd_shape* shape);
  * ssd_fwd takes the one-pass schedule for SSD_BF16 when dstate <= 128 and
  * there are at least as many (batch, head pair) sequences as multiprocessors
  * (below that the chain of windows, not bandwidth, bounds the one-pass kernel);
- * otherwise the staged one.  init_state may be NULL (zero initial state); final_state
+ * otherwise the staged one.  The one-pass schedule works in windows of 128
+ * tokens whatever chunk_size is; the result is the recurrence's either way.
+ * init_state may be NULL (zero initial state); final_state
  * may be NULL (not written; the workspace holds the running state instead).
  * When given, final_state is also the running state's storage during the
  * call, so it must not overlap the inputs (it may equal init_state).  The
@@ -152,16 +162,23 @@ ssd_status ssd_fwd_fused(const ssd_shape* shape, const void* x, const float* dt,
                          const void* Bm, const void* Cm, const float* D, const float* init_state, void* y,
                          float* final_state, void* workspace, size_t workspace_bytes, ssd_stream_t stream);
 
-/* The one-pass schedule's second step alone (ssd_fwd_fused is
- * ssd_chunk_cumsum followed by this call): for every window of
- * min(chunk_size, 128) tokens of every (batch, head pair), the window state on
- * the tensor core, the state carried from the previous window (through the
- * workspace slot, or final_state, and a per-pair flag), and y.  Needs step 1
- * (chunk_cumsum), which also clears the flags.  SSD_BF16 only
- * (SSD_ERR_UNSUPPORTED otherwise); arguments as for ssd_fwd. */
-ssd_status ssd_fused_pass(const ssd_shape* shape, const void* x, const void* Bm, const void* Cm, const float* D,
-                          const float* init_state, void* y, float* final_state, void* workspace,
-                          size_t workspace_bytes, ssd_stream_t stream);
+/* Step 1 of the one-pass schedule alone ("Jane Street ML Engineers Map Mamba-2
+ * Recurrent State Computation to Tensor Cores with cuTile", compute_out
+ * paragraph: C B^T by one matrix product, causal mask made in registers):
+ * writes the workspace's cbm region, the causal select of C B^T in bf16 for
+ * every (batch, 128-token window, group), shared by every head of the group;
+ * also clears the status word and the one-pass run counter and flags.
+ * SSD_BF16 only (SSD_ERR_UNSUPPORTED otherwise). */
+ssd_status ssd_causal_cb(const ssd_shape* shape, const void* Bm, const void* Cm, void* workspace,
+                         size_t workspace_bytes, ssd_stream_t stream);
+
+/* Step 2 of the one-pass schedule alone (ssd_fwd_fused is ssd_causal_cb
+ * followed by this call): the persistent kernel described under ssd_fwd.
+ * Needs step 1.  SSD_BF16 only (SSD_ERR_UNSUPPORTED otherwise); arguments as
+ * for ssd_fwd. */
+ssd_status ssd_fused_pass(const ssd_shape* shape, const void* x, const float* dt, const float* A, const void* Bm,
+                          const void* Cm, const float* D, const float* init_state, void* y, float* final_state,
+                          void* workspace, size_t workspace_bytes, ssd_stream_t stream);
 
 /* The launches ssd_fwd makes for `shape`, numbered 0 .. ssd_fwd_kernel_count()-1
  * in the order ssd_fwd enqueues them, restricted to those with index in

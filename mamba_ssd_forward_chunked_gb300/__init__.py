@@ -26,7 +26,7 @@ STATUS = {0: "SSD_OK", 1: "SSD_ERR_INVALID_ARG", 2: "SSD_ERR_UNSUPPORTED", 3: "S
 EXPORTS = ("ssd_status_string", "ssd_validate_shape", "ssd_fwd_workspace_layout", "ssd_fwd_workspace_size",
            "ssd_fwd", "ssd_fwd_check", "ssd_chunk_cumsum", "ssd_chunk_state", "ssd_state_passing",
            "ssd_compute_out", "ssd_debug_timeout_probe", "ssd_fwd_kernel_count", "ssd_fwd_static_scratch",
-           "ssd_fwd_fused", "ssd_fused_pass", "ssd_fwd_range")
+           "ssd_fwd_fused", "ssd_fused_pass", "ssd_fwd_range", "ssd_causal_cb")
 
 # Size of the library's own workspace array used by ssd_fwd_static_scratch.
 SSD_STATIC_SCRATCH_BYTES = 32 << 20
@@ -46,7 +46,8 @@ class ssd_shape(ctypes.Structure):
 class ssd_workspace_layout(ctypes.Structure):
     _fields_ = [("status", ctypes.c_size_t), ("cumsum", ctypes.c_size_t), ("dt_t", ctypes.c_size_t),
                 ("states", ctypes.c_size_t), ("states_bf16", ctypes.c_size_t), ("chain", ctypes.c_size_t),
-                ("hslot", ctypes.c_size_t), ("bT", ctypes.c_size_t), ("total", ctypes.c_size_t)]
+                ("hslot", ctypes.c_size_t), ("bT", ctypes.c_size_t), ("cbm", ctypes.c_size_t),
+                ("total", ctypes.c_size_t)]
 
 
 class SSDError(RuntimeError):
@@ -80,7 +81,9 @@ def _load() -> ctypes.CDLL:
     lib.ssd_fwd_range.restype = c_int
     lib.ssd_fwd_range.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, c_int, c_int, vp]
     lib.ssd_fused_pass.restype = c_int
-    lib.ssd_fused_pass.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    lib.ssd_fused_pass.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    lib.ssd_causal_cb.restype = c_int
+    lib.ssd_causal_cb.argtypes = [sp, vp, vp, vp, sz, vp]
     lib.ssd_fwd_check.restype = c_int
     lib.ssd_fwd_check.argtypes = [vp]
     lib.ssd_chunk_cumsum.restype = c_int
@@ -187,9 +190,12 @@ def workspace_views(shape: ssd_shape, ws: torch.Tensor) -> Dict[str, torch.Tenso
         out["states_bf16"] = view(L["states_bf16"], B * nc * H * P * N, torch.bfloat16, (B, nc, H, P, N))
     out["chain"] = view(L["chain"], 1 + B * (H // 2), torch.int32, (1 + B * (H // 2),))
     out["hslot"] = view(L["hslot"], B * H * P * N, torch.float32, (B * H * P * N,))
+    G = shape.ngroups
     if shape.dtype != SSD_BF16:  # Bm in 4 KB TF32 boxes, [B][G][Lp/32][N/32][box]
-        G = shape.ngroups
         out["bT"] = view(L["bT"], B * G * Lp * N, torch.float32, (B * G * Lp * N,))
+    else:  # causal C B^T per (batch, 128-token window, group)
+        nw = -(-shape.seqlen // 128)
+        out["cbm"] = view(L["cbm"], B * nw * G * 128 * 128, torch.bfloat16, (B, nw, G, 128, 128))
     return out
 
 
@@ -308,15 +314,22 @@ def ssd_fwd_check(workspace: torch.Tensor) -> int:
     return lib.ssd_fwd_check(_ptr(workspace))
 
 
-def ssd_fused_pass(shape: ssd_shape, x: torch.Tensor, Bm: torch.Tensor, Cm: torch.Tensor, D: torch.Tensor,
-                   init_state: Optional[torch.Tensor], y: torch.Tensor, final_state: Optional[torch.Tensor],
-                   workspace: torch.Tensor, stream=None) -> None:
-    """The one-pass kernel alone, after ssd_chunk_cumsum (C: ssd_fused_pass)."""
-    check_tensors(shape, x=x, Bm=Bm, Cm=Cm, D=D, init_state=init_state, y=y, final_state=final_state,
+def ssd_causal_cb(shape: ssd_shape, Bm: torch.Tensor, Cm: torch.Tensor, workspace: torch.Tensor, stream=None) -> None:
+    """Step 1 of the one-pass schedule: the causal C B^T blocks (C: ssd_causal_cb)."""
+    check_tensors(shape, Bm=Bm, Cm=Cm, workspace=workspace)
+    _check(lib.ssd_causal_cb(ctypes.byref(shape), _ptr(Bm), _ptr(Cm), _ptr(workspace), workspace.numel(),
+                             _stream(stream)), "ssd_causal_cb")
+
+
+def ssd_fused_pass(shape: ssd_shape, x: torch.Tensor, dt: torch.Tensor, A: torch.Tensor, Bm: torch.Tensor,
+                   Cm: torch.Tensor, D: torch.Tensor, init_state: Optional[torch.Tensor], y: torch.Tensor,
+                   final_state: Optional[torch.Tensor], workspace: torch.Tensor, stream=None) -> None:
+    """Step 2 of the one-pass schedule, after ssd_causal_cb (C: ssd_fused_pass)."""
+    check_tensors(shape, x=x, dt=dt, A=A, Bm=Bm, Cm=Cm, D=D, init_state=init_state, y=y, final_state=final_state,
                   workspace=workspace)
-    _check(lib.ssd_fused_pass(ctypes.byref(shape), _ptr(x), _ptr(Bm), _ptr(Cm), _ptr(D), _ptr(init_state), _ptr(y),
-                              _ptr(final_state), _ptr(workspace), workspace.numel(), _stream(stream)),
-           "ssd_fused_pass")
+    _check(lib.ssd_fused_pass(ctypes.byref(shape), _ptr(x), _ptr(dt), _ptr(A), _ptr(Bm), _ptr(Cm), _ptr(D),
+                              _ptr(init_state), _ptr(y), _ptr(final_state), _ptr(workspace), workspace.numel(),
+                              _stream(stream)), "ssd_fused_pass")
 
 
 def ssd_chunk_cumsum(shape: ssd_shape, dt: torch.Tensor, A: torch.Tensor, workspace: torch.Tensor,

@@ -102,6 +102,11 @@ ssd_status layout_of(const ssd_shape* shape, ssd_workspace_layout* out) {
   off = align_up(off + heads * s.headdim * s.dstate * sizeof(float));
   L.bT = off;
   if (s.dtype == SSD_F32) off = align_up(off + static_cast<size_t>(s.batch) * s.ngroups * lp * s.dstate * sizeof(float));
+  L.cbm = off;
+  if (s.dtype == SSD_BF16) {
+    const size_t nwin = static_cast<size_t>((s.seqlen + 127) / 128);
+    off = align_up(off + static_cast<size_t>(s.batch) * nwin * s.ngroups * 128 * 128 * sizeof(__nv_bfloat16));
+  }
   L.total = off;
   *out = L;
   return SSD_OK;
@@ -118,6 +123,7 @@ Work carve(void* ws, const ssd_workspace_layout& L, bool bf16) {
   w.counter = reinterpret_cast<int*>(p + L.chain);
   w.flags = w.counter + 1;
   w.hslot = reinterpret_cast<float*>(p + L.hslot);
+  w.cbm = bf16 ? static_cast<void*>(p + L.cbm) : nullptr;
   w.bT = bf16 ? nullptr : reinterpret_cast<float*>(p + L.bT);
   return w;
 }
@@ -220,24 +226,27 @@ ssd_status fwd_impl(int path, int first, int end, const ssd_shape* shape, const 
                     const float* A, const void* Bm, const void* Cm, const float* D, const float* init_state, void* y,
                     float* final_state, void* workspace, size_t workspace_bytes, ssd_stream_t stream);
 
-bool build_fused_maps(const ssd_shape& s, const void* x, const void* Bm, const void* Cm, const void* y,
-                      FusedMaps* m) {
-  const uint32_t S = static_cast<uint32_t>(s.chunk_size < 128 ? s.chunk_size : 128);
+bool build_onepass_maps(const ssd_shape& s, const void* x, const void* Bm, const void* Cm, const void* y,
+                        const void* cbm, OnePassMaps* m) {
   const uint64_t es = 2;
   const uint64_t gn = static_cast<uint64_t>(s.ngroups) * s.dstate;
   const uint64_t dims4[4] = {static_cast<uint64_t>(s.dstate), static_cast<uint64_t>(s.ngroups),
                              static_cast<uint64_t>(s.seqlen), static_cast<uint64_t>(s.batch)};
   const uint64_t str4[3] = {s.dstate * es, gn * es, gn * es * s.seqlen};
-  const uint32_t box4[4] = {64, 1, S, 1};
+  const uint32_t box4[4] = {64, 1, 128, 1};
   if (!encode(&m->cm, true, 4, Cm, dims4, str4, box4)) return false;
   if (!encode(&m->bm, true, 4, Bm, dims4, str4, box4)) return false;
   const uint64_t hp = static_cast<uint64_t>(s.nheads) * s.headdim;
   const uint64_t dims[3] = {hp, static_cast<uint64_t>(s.seqlen), static_cast<uint64_t>(s.batch)};
   const uint64_t str[2] = {hp * es, hp * es * s.seqlen};
-  const uint32_t box[3] = {64, S, 1};
+  const uint32_t box[3] = {64, 128, 1};
   if (!encode(&m->x, true, 3, x, dims, str, box)) return false;
   if (!encode(&m->y, true, 3, y, dims, str, box)) return false;
-  return true;
+  const uint64_t nwin = static_cast<uint64_t>((s.seqlen + 127) / 128);
+  const uint64_t mdims[2] = {128, static_cast<uint64_t>(s.batch) * nwin * s.ngroups * 128};
+  const uint64_t mstr[1] = {128 * es};
+  const uint32_t mbox[2] = {64, 128};
+  return encode(&m->m, true, 2, cbm, mdims, mstr, mbox);
 }
 
 }  // namespace
@@ -378,9 +387,24 @@ ssd_status ssd_fwd_range(const ssd_shape* shape, const void* x, const float* dt,
                   workspace_bytes, stream);
 }
 
-ssd_status ssd_fused_pass(const ssd_shape* shape, const void* x, const void* Bm, const void* Cm, const float* D,
-                          const float* init_state, void* y, float* final_state, void* workspace,
-                          size_t workspace_bytes, ssd_stream_t stream) {
+ssd_status ssd_causal_cb(const ssd_shape* shape, const void* Bm, const void* Cm, void* workspace,
+                         size_t workspace_bytes, ssd_stream_t stream) {
+  ssd_workspace_layout L;
+  ssd_status st = check_workspace(shape, workspace, workspace_bytes, &L);
+  if (st != SSD_OK) return st;
+  if (shape->dtype != SSD_BF16) return SSD_ERR_UNSUPPORTED;
+  if (empty_problem(*shape)) return SSD_OK;
+  if (!Bm || !Cm || !aligned16(Bm) || !aligned16(Cm)) return SSD_ERR_INVALID_ARG;
+  Work w = carve(workspace, L, true);
+  OnePassMaps maps;
+  // x and y are not read by this step: Cm stands in as a valid base for their (unused) maps
+  if (!build_onepass_maps(*shape, Cm, Bm, Cm, Cm, w.cbm, &maps)) return SSD_ERR_CUDA;
+  return from_cuda(launch_causal_cb(make_dims(*shape), maps, w, spin_limit_ns(), reinterpret_cast<cudaStream_t>(stream)));
+}
+
+ssd_status ssd_fused_pass(const ssd_shape* shape, const void* x, const float* dt, const float* A, const void* Bm,
+                          const void* Cm, const float* D, const float* init_state, void* y, float* final_state,
+                          void* workspace, size_t workspace_bytes, ssd_stream_t stream) {
   ssd_workspace_layout L;
   ssd_status st = check_workspace(shape, workspace, workspace_bytes, &L);
   if (st != SSD_OK) return st;
@@ -388,14 +412,14 @@ ssd_status ssd_fused_pass(const ssd_shape* shape, const void* x, const void* Bm,
   if ((init_state && !aligned16(init_state)) || (final_state && !aligned16(final_state)))
     return SSD_ERR_INVALID_ARG;
   if (empty_problem(*shape)) return SSD_OK;
-  if (!x || !Bm || !Cm || !D || !y || !aligned16(x) || !aligned16(Bm) || !aligned16(Cm) || !aligned16(y) ||
-      !aligned4(D))
+  if (!x || !dt || !A || !Bm || !Cm || !D || !y || !aligned16(x) || !aligned16(Bm) || !aligned16(Cm) ||
+      !aligned16(y) || !aligned4(dt) || !aligned4(A) || !aligned4(D))
     return SSD_ERR_INVALID_ARG;
   Work w = carve(workspace, L, true);
-  FusedMaps fmaps;
-  if (!build_fused_maps(*shape, x, Bm, Cm, y, &fmaps)) return SSD_ERR_CUDA;
-  return from_cuda(launch_fused(make_dims(*shape), fmaps, D, x, init_state, final_state, w,
-                                spin_limit_ns(), reinterpret_cast<cudaStream_t>(stream)));
+  OnePassMaps maps;
+  if (!build_onepass_maps(*shape, x, Bm, Cm, y, w.cbm, &maps)) return SSD_ERR_CUDA;
+  return from_cuda(launch_onepass(make_dims(*shape), maps, dt, A, D, x, init_state, final_state, w, spin_limit_ns(),
+                                  reinterpret_cast<cudaStream_t>(stream)));
 }
 
 ssd_status ssd_fwd_fused(const ssd_shape* shape, const void* x, const float* dt, const float* A, const void* Bm,
@@ -443,11 +467,12 @@ ssd_status fwd_impl(int path, int first, int end, const ssd_shape* shape, const 
     ++k;
   };
   if (path == 1) {
-    FusedMaps fmaps;
-    if (!build_fused_maps(*shape, x, Bm, Cm, y, &fmaps)) return SSD_ERR_CUDA;
-    step([&](bool) { return launch_chunk_cumsum(d, dt, A, w, cs); });
+    OnePassMaps omaps;
+    if (!build_onepass_maps(*shape, x, Bm, Cm, y, w.cbm, &omaps)) return SSD_ERR_CUDA;
+    const uint64_t spin = spin_limit_ns();
+    step([&](bool) { return launch_causal_cb(d, omaps, w, spin, cs); });
     step([&](bool dep) {
-      return launch_fused(d, fmaps, D, x, init_state, final_state, w, spin_limit_ns(), cs, dep);
+      return launch_onepass(d, omaps, dt, A, D, x, init_state, final_state, w, spin, cs, dep);
     });
     return from_cuda(e);
   }

@@ -30,6 +30,7 @@ struct Work {
   int* flags;                  // one-pass kernel: [B][H/2] windows published
   float* hslot;                // one-pass kernel: states at run boundaries (its own layout)
   float* bT;                   // fp32 problems: Bm as K-major TF32 boxes for chunk_state, or null
+  void* cbm;                   // bf16 problems: causal C B^T per (batch, 128-token window, group), or null
 };
 
 // Tensor maps built on the host for one call.
@@ -46,12 +47,13 @@ struct ComputeOutMaps {
   CUtensorMap y;   // y [B][L][H*P], box {128 B of p, 32 tokens, 1} (TMA stores)
 };
 
-// Tensor maps of the one-pass kernel (bf16), window of S = min(Q, 128) tokens.
-struct FusedMaps {
-  CUtensorMap x;   // x [B][L][H*P], box {64 p, S tokens, 1}
-  CUtensorMap cm;  // Cm [B][L][G][N], box {64 n, 1, S tokens, 1}
+// Tensor maps of the one-pass schedule (bf16), windows of 128 tokens.
+struct OnePassMaps {
+  CUtensorMap x;   // x [B][L][H*P], box {64 p, 128 tokens, 1}
+  CUtensorMap cm;  // Cm [B][L][G][N], box {64 n, 1, 128 tokens, 1}
   CUtensorMap bm;  // Bm, same box
-  CUtensorMap y;   // y [B][L][H*P], box {64 p, S tokens, 1} (TMA stores)
+  CUtensorMap m;   // causal C B^T rows [(B*nw*G*128)][128], box {64 j, 128 rows} (stores and loads)
+  CUtensorMap y;   // y [B][L][H*P], box {64 p, 128 tokens, 1} (TMA stores)
 };
 
 // Launches `kernel`; as a programmatic dependent of the preceding kernel in the
@@ -86,10 +88,11 @@ cudaError_t launch_state_passing(const Dims& d, bool bf16, const float* init, fl
 cudaError_t launch_compute_out(const Dims& d, bool bf16, const ComputeOutMaps& maps, const float* D,
                                const void* x, void* y, const Work& w, uint64_t spin_ns, cudaStream_t stream,
                                bool dependent = false);
-size_t fused_smem_bytes(const Dims& d);
-cudaError_t launch_fused(const Dims& d, const FusedMaps& maps, const float* D, const void* x, const float* init,
-                         float* final_state, const Work& w, uint64_t spin_ns, cudaStream_t stream,
-                         bool dependent = false);
+cudaError_t launch_causal_cb(const Dims& d, const OnePassMaps& maps, const Work& w, uint64_t spin_ns,
+                             cudaStream_t stream);
+cudaError_t launch_onepass(const Dims& d, const OnePassMaps& maps, const float* dt, const float* A, const float* D,
+                           const void* x, const float* init, float* final_state, const Work& w, uint64_t spin_ns,
+                           cudaStream_t stream, bool dependent = false);
 cudaError_t launch_timeout_probe(int* status, uint64_t limit_ns, cudaStream_t stream);
 
 }  // namespace ssd

@@ -1,0 +1,859 @@
+// Step 2 of the one-pass schedule: chunk state, state passing and output in
+// one persistent kernel (bf16 inputs, fp32 accumulation), every window of 128
+// tokens of a (batch, head pair) in flight behind the one before it.
+//
+// What it computes ("Jane Street ML Engineers Map Mamba-2 Recurrent State
+// Computation to Tensor Cores with cuTile", jump-formula, three-kernel and
+// compute_out paragraphs).  For a window of S = 128 tokens of head h, with G
+// the cumulative sum of dt*A from the window start (G_i includes token i) and
+// h_in the state entering the window:
+//
+//     y_i   = sum_{j<=i} (c_i . b_j) e^{G_i - G_j} dt_j x_j + e^{G_i} c_i h_in^T + D x_i
+//     h_out = e^{G_S} h_in + sum_j e^{G_S - G_j} dt_j x_j b_j^T
+//
+// i.e. the jump formula with decay applied window by window; any split into
+// windows gives the recurrence's result.
+//
+// Rescaled form (window start as reference).  With r_i = e^{G_i} (<= 1) and
+// X^_j = e^{-G_j} dt_j x_j:
+//
+//     y_i   = r_i [ sum_{j<=i} M_ij X^_j + c_i h_in^T ] + D x_i,   M_ij = (c_i . b_j) [j <= i]
+//     h_out = e^{G_S} (h_in + X^^T B)
+//
+// M is the causal select of C B^T alone: the same for every head of a group,
+// so the causal_cb kernel computes it once per (batch, window, group) and this
+// kernel loads it.  The intra product and the carried-state product share one
+// fp32 accumulator, and y_i at token i reads G only up to token i (the masked
+// entries of M are exact zeros), so y is causal to the last bit.  The form
+// needs e^{-G_S} within fp32 range: it is used while the window's decay -G_S
+// stays below 2^100 on both heads of the pair.  Otherwise the window takes an
+// exact path: X is scaled against the window END instead
+// (X~_j = e^{G_S - G_j} dt_j x_j <= dt_j x_j), the intra product is not run,
+// and the epilogue sums (c_i . b_j) e^{G_i - G_j} dt_j x_j on CUDA cores with
+// one exponential per element (exponent <= 0).
+//
+// The state on the tensor core.  The running state of the pair lives in tensor
+// memory as an fp32 accumulator with lane = (head, p) and columns = dstate.
+// Before a window's state product it holds pi * h_in (pi = 1 on the rescaled
+// form, e^{G_S} on the exact one), the product X^^T B (resp. X~^T B) is
+// accumulated onto it, and the state pass that follows reads it back, scales
+// it by mu (e^{G_S}, resp. 1) to get h_out, and writes pi' * h_out for the
+// next window plus the bf16 copy of h_out the next window's carried-state
+// product reads.  So the serial chain between windows is one state product and
+// one pass over the state; everything else of a window overlaps it.
+//
+// Runs and chaining.  A claim is a run of up to R consecutive windows of one
+// (batch, head pair); runs are claimed from a global counter in run-major order
+// (all first runs, then all second runs, ...), so a run's predecessor was
+// claimed earlier by a running CTA.  A run's last window publishes its state
+// (fp32, L2-resident workspace slot) and a per-pair flag; the next run's first
+// window waits for the flag (bounded) and loads it.  A sequence's first window
+// reads init_state (or zero) and its last writes final_state.
+//
+// GB300 mapping, per CTA (one per SM, 512 threads, persistent):
+//   warp 2       claims runs and publishes their windows in an 8-deep ring.
+//   warp 0       TMA: a ring of 32 KB stages holding, per window in the order
+//                the tensor core uses them, M (the causal operand), C and B.
+//   warp 1       owns tensor memory and issues every tcgen05.mma from one
+//                thread, per window n: the carried product C O(n)^T, the state
+//                product S(n), then the next window's intra product M X^.
+//   warp 3       TMA for the head pair's X window (three buffers; two at
+//                dstate 256): stores window n - 3's y out of a buffer, then
+//                loads window n's X into it.
+//   warps 4-7    the state pass: thread = state row (head, p).
+//   warps 8-15   one warpgroup per head, thread = token row: the window's
+//                cumsum (warp-shuffle scan of dt*A), the X scaling (in place),
+//                and the epilogue of the window before (y written over X).
+// Tensor memory: two output accumulators (columns [0, 256)) and the state
+// (columns [256, 256 + dstate)).  Every wait is bounded; on expiry the CTA
+// records SSD_ERR_DEVICE_TIMEOUT, waits for its own copies and exits.
+#include "ptx.cuh"
+#include "ssd_internal.cuh"
+
+namespace ssd {
+namespace {
+
+constexpr int kThreads = 512;
+constexpr int kWin = 128;
+constexpr int kInfoRing = 8;
+constexpr float kSpan = 100.f;  // log2 bound of the window decay for the rescaled form
+constexpr uint32_t kStage = 32768, kAtom = 16384, kXBytes = 32768;
+constexpr uint32_t kColY = 0, kColH = 256, kTmemCols = 512;
+
+struct WinInfo {
+  int b, pair, w;  // batch, head pair, window index in the sequence
+  int flags;       // bit 0: first window of its run, bit 1: last, bit 2: no more windows
+};
+// Per-window scalars the head warpgroups publish (slot n % 2, with the X buffer).
+struct Scal {
+  float alpha[2];  // e^{G_S} per head
+  int fast[2];     // rescaled form valid for the head
+};
+
+struct OPSmem {
+  uint32_t ring, xbuf, obuf, info, scal, scan, bars, holder, total;
+  int stages, nob, nxb;
+};
+
+// Shared memory: three stages of 32 KB (M; B and C in ceil(N/128) stages each),
+// X buffers of 32 KB (three up to dstate 128, two at 256), the carried-state
+// operand O (bf16 [2*P rows][N] in 64-column atoms), and the small control data.
+__host__ __device__ inline OPSmem op_layout(int N) {
+  OPSmem s{};
+  const uint32_t obytes = static_cast<uint32_t>(N / 64) * kAtom;
+  s.nob = 1;
+  s.nxb = N <= 128 ? 3 : 2;
+  s.stages = 3;
+  s.ring = 0;
+  s.xbuf = s.ring + s.stages * kStage;
+  s.obuf = s.xbuf + s.nxb * kXBytes;
+  s.info = s.obuf + s.nob * obytes;
+  s.scal = s.info + kInfoRing * sizeof(WinInfo);
+  s.scan = s.scal + 3 * sizeof(Scal);
+  s.bars = s.scan + 2 * 2 * 4 * sizeof(float);
+  s.holder = s.bars + 48 * 8;
+  s.total = s.holder + 16;
+  return s;
+}
+
+// Scaled pair, clamped below bf16's largest finite value: an overflowing
+// product must not become inf, which the causal select's zeros would turn
+// into NaN in rows that never see that token.
+__device__ __forceinline__ uint32_t scale_bf16x2(uint32_t v, float s) {
+  constexpr float kMax = 3.38e38f;
+  return pack_bf16x2(fminf(fmaxf(bf16_lo(v) * s, -kMax), kMax), fminf(fmaxf(bf16_hi(v) * s, -kMax), kMax));
+}
+
+// Inclusive sum over the 128 threads of a warpgroup in token order; each
+// result adds only values of threads at or before it.  `total` is the sum of
+// all 128, formed the same way by every thread (and equal to thread 127's
+// result).  `ws` holds four floats of the warpgroup.
+__device__ __forceinline__ float wg_scan(float v, float* ws, uint32_t bar, int lane, int wq, float& total) {
+  float incl = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const float u = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += u;
+  }
+  if (lane == 31) ws[wq] = incl;
+  named_bar_sync(bar, 128);
+  float pre = 0.f, tot = 0.f;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    if (k < wq) pre += ws[k];
+    tot += ws[k];
+  }
+  total = tot;
+  return wq == 0 ? incl : pre + incl;
+}
+
+// Exact epilogue of a window off the rescaled form, for token row i of head h:
+// the accumulator at `tacc` (64 columns) holds c_i h_in^T (carried state,
+// unscaled), and
+//   y_i = e^{G_i} acc + sum_{j<=i} M_ij e^{G_i - G_j} dt_j x_j + D x_i
+// with M read from the causal_cb output, x and dt from global memory and G
+// summed again along the row.  Rare (a window decaying by more than 2^100)
+// and slow; done in two halves of 32 columns to keep its registers few (it is
+// inlined: a call would make the compiler keep the hot loop's values in local
+// memory around it).
+__device__ __forceinline__ void exact_epilogue(const Dims& d, int b, int h, int t0, int i, float gi, float Ah,
+                                               float Dh, const __nv_bfloat16* __restrict__ Mrow,
+                                               const __nv_bfloat16* __restrict__ xg, const float* __restrict__ dtg,
+                                               uint32_t tacc, uint8_t* xr) {
+  const float ei = fast_exp2(gi);
+  const bool in_seq = t0 + i < d.L;
+  const uint4* xi = reinterpret_cast<const uint4*>(xg + ((static_cast<int64_t>(b) * d.L + t0 + i) * d.H + h) * d.P);
+#pragma unroll 1
+  for (int half = 0; half < 2; ++half) {
+    uint32_t ya[32];
+    tmem_ld32(tacc + 32 * half, ya);
+    tmem_ld_wait();
+    float acc[32];
+#pragma unroll
+    for (int q = 0; q < 32; ++q) acc[q] = 0.f;
+    float G = 0.f;
+    for (int j = 0; j <= i && t0 + j < d.L; ++j) {
+      const float dtj = dtg[(static_cast<int64_t>(b) * d.L + t0 + j) * d.H + h];
+      G += dtj * Ah;
+      const float coef = __bfloat162float(Mrow[j]) * fast_exp2(fminf(gi - G * kLog2e, 0.f)) * dtj;
+      const uint4* xj =
+          reinterpret_cast<const uint4*>(xg + ((static_cast<int64_t>(b) * d.L + t0 + j) * d.H + h) * d.P) + 4 * half;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const uint4 xv = __ldg(xj + c);
+        const uint32_t* xw = reinterpret_cast<const uint32_t*>(&xv);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          acc[8 * c + 2 * e] = fmaf(coef, bf16_lo(xw[e]), acc[8 * c + 2 * e]);
+          acc[8 * c + 2 * e + 1] = fmaf(coef, bf16_hi(xw[e]), acc[8 * c + 2 * e + 1]);
+        }
+      }
+    }
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const uint4 xv = in_seq ? __ldg(xi + 4 * half + c) : make_uint4(0, 0, 0, 0);
+      const uint32_t* xw = reinterpret_cast<const uint32_t*>(&xv);
+      uint4 v;
+      uint32_t* vw = reinterpret_cast<uint32_t*>(&v);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int pi = 8 * c + 2 * e;
+        vw[e] = pack_bf16x2(fmaf(Dh, bf16_lo(xw[e]), fmaf(ei, __uint_as_float(ya[pi]), acc[pi])),
+                            fmaf(Dh, bf16_hi(xw[e]), fmaf(ei, __uint_as_float(ya[pi + 1]), acc[pi + 1])));
+      }
+      const int cc = 4 * half + c;
+      *reinterpret_cast<uint4*>(xr + ((cc ^ (i & 7)) << 4)) = v;
+    }
+  }
+}
+
+// A head-warpgroup thread's view of one window.
+struct Ctx {
+  int b, pair, w, flags;
+  float g;   // log2 cumsum at this token (window start = 0)
+  float gS;  // log2 cumsum at the window end
+  float dt;  // dt at this token (0 past the sequence)
+  int fastH; // rescaled form valid for this head
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+    ssd_onepass_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap cmap,
+                       const __grid_constant__ CUtensorMap bmap, const __grid_constant__ CUtensorMap mmap,
+                       const __grid_constant__ CUtensorMap ymap, Dims d, int R, const float* __restrict__ dtg,
+                       const float* __restrict__ Avec, const float* __restrict__ Dvec,
+                       const __nv_bfloat16* __restrict__ Mg, const float* init, float* final_state, float* hslot,
+                       int* flags, int* counter, const __nv_bfloat16* __restrict__ xg, int* status,
+                       uint64_t spin_ns) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const OPSmem Ls = op_layout(d.N);
+  const int natom = d.N / 64;           // 64-column atoms of dstate
+  const int nhalf = (d.N + 127) / 128;  // 128-column halves (stages) of B and C
+  const int nxb = Ls.nxb;
+  const uint32_t obytes = static_cast<uint32_t>(natom) * kAtom;
+  const int hp = d.H / 2;
+  const int nw = (d.L + kWin - 1) / kWin;
+  const int runs_per_seq = (nw + R - 1) / R;
+  const int nruns = runs_per_seq * d.B * hp;
+  // Window n of this CTA uses X buffer (and scalar slot) n % nxb and output accumulator n % 2.
+  auto xs = [&](int n) { return n % nxb; };
+  auto xph = [&](int n) { return static_cast<uint32_t>((n / nxb) & 1); };
+  auto yph = [](int n) { return static_cast<uint32_t>((n >> 1) & 1); };
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Ls.bars);
+  uint64_t* full = bars;          // [3] ring stage landed
+  uint64_t* empty = bars + 3;     // [3] ring stage consumed (MMA commit)
+  uint64_t* xfull = bars + 6;     // [3] X window landed
+  uint64_t* xready = bars + 9;    // [3] X scaled and window scalars published (256)
+  uint64_t* ystaged = bars + 12;  // [3] y written into the X buffer (256: both head warpgroups)
+  uint64_t* tfull = bars + 15;    // [8] window ring
+  uint64_t* tempty = bars + 23;   // [8] (15 warps read each entry)
+  uint64_t* hready = bars + 31;   // [2] state (pi h_in) and O of the window in place (128)
+  uint64_t* dfull = bars + 33;    // [2] state product done (X^ of the window read)
+  uint64_t* cdone = bars + 35;    // [2] carried-state product done: O free, output complete
+  uint64_t* yfree = bars + 37;    // [2] output accumulator drained (256)
+  WinInfo* info = reinterpret_cast<WinInfo*>(smem + Ls.info);
+  Scal* scal = reinterpret_cast<Scal*>(smem + Ls.scal);
+  float* scanws = reinterpret_cast<float*>(smem + Ls.scan);  // [2 heads][2 windows][4]
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + Ls.holder);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < 3; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+      mbar_init(&xfull[s], 1);
+      mbar_init(&xready[s], 256);
+      mbar_init(&ystaged[s], 256);
+    }
+    for (int s = 0; s < kInfoRing; ++s) {
+      mbar_init(&tfull[s], 1);
+      mbar_init(&tempty[s], 15);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&hready[s], 128);
+      mbar_init(&dfull[s], 1);
+      mbar_init(&cdone[s], 1);
+      mbar_init(&yfree[s], 256);
+    }
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&xmap);
+    tma_prefetch_desc(&cmap);
+    tma_prefetch_desc(&bmap);
+    tma_prefetch_desc(&mmap);
+    tma_prefetch_desc(&ymap);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_holder, kTmemCols);
+    tmem_relinquish();
+  }
+  grid_dep_wait();  // causal_cb's operand, cleared counter and flags are visible from here on
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  bool ok = true;
+
+  // the window ring entry n, read by a whole warp; lane 0 frees the entry
+  auto read_info = [&](int n, WinInfo& I) -> bool {
+    const int ts = n % kInfoRing;
+    bool good = true;
+    if (lane == 0) good = mbar_wait(&tfull[ts], (n / kInfoRing) & 1, spin_ns);
+    good = __shfl_sync(0xffffffffu, good ? 1 : 0, 0) != 0;
+    if (!good) return false;
+    I = info[ts];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&tempty[ts]);
+    return true;
+  };
+  // the same, for a warp of which only lane 0 runs
+  auto read_info1 = [&](int n, WinInfo& I) -> bool {
+    const int ts = n % kInfoRing;
+    if (!mbar_wait(&tfull[ts], (n / kInfoRing) & 1, spin_ns)) return false;
+    I = info[ts];
+    mbar_arrive(&tempty[ts]);
+    return true;
+  };
+
+  if (warp == 2) {
+    // ------------------------------------------------------------ run scheduler
+    if (lane == 0) {
+      int n = 0;
+      for (bool more = true; more && ok;) {
+        const int run = atomicAdd(counter, 1);
+        int b = 0, pair = 0, w0 = 0, w1 = 1;
+        if (run < nruns) {
+          pair = run % hp;
+          b = (run / hp) % d.B;
+          const int k = run / hp / d.B;
+          w0 = k * R;
+          w1 = min(nw, w0 + R);
+        } else {
+          more = false;  // one end marker
+        }
+        for (int w = w0; w < w1 && ok; ++w, ++n) {
+          const int ts = n % kInfoRing;
+          if (n >= kInfoRing && !mbar_wait(&tempty[ts], ((n / kInfoRing) - 1) & 1, spin_ns)) {
+            ok = false;
+            break;
+          }
+          WinInfo I;
+          I.b = b;
+          I.pair = pair;
+          I.w = w;
+          I.flags = more ? ((w == w0 ? 1 : 0) | (w == w1 - 1 ? 2 : 0)) : 4;
+          info[ts] = I;
+          mbar_arrive(&tfull[ts]);
+        }
+      }
+    }
+  } else if (warp == 3) {
+    // ------------------------------------------------------------ X loads and y stores
+    // Window n's X goes into buffer n % nxb once window n - nxb's y has left it.
+    if (lane == 0) {
+      int hb[3] = {0, 0, 0}, ht[3] = {0, 0, 0}, hh0[3] = {0, 0, 0};  // batch, t0, h0 of each buffer's window
+      auto store = [&](int k) -> bool {  // window k's y, written over its X
+        const int sb = xs(k);
+        if (!mbar_wait(&ystaged[sb], xph(k), spin_ns)) return false;
+        uint8_t* xb = smem + Ls.xbuf + sb * kXBytes;
+        tma_store_3d(&ymap, xb, hh0[sb] * d.P, ht[sb], hb[sb]);
+        tma_store_3d(&ymap, xb + kWin * 128, (hh0[sb] + 1) * d.P, ht[sb], hb[sb]);
+        tma_store_commit();
+        return true;
+      };
+      int n = 0;
+      for (; ok; ++n) {
+        WinInfo I;
+        if (!read_info1(n, I)) {
+          ok = false;
+          break;
+        }
+        if (I.flags & 4) break;
+        const int sb = xs(n);
+        if (n >= nxb) {
+          if (!store(n - nxb)) {
+            ok = false;
+            break;
+          }
+          tma_store_wait_read();
+        }
+        hb[sb] = I.b;
+        ht[sb] = I.w * kWin;
+        hh0[sb] = 2 * I.pair;
+        uint8_t* xb = smem + Ls.xbuf + sb * kXBytes;
+        mbar_arrive_expect_tx(&xfull[sb], kXBytes);
+        tma_load_3d(xb, &xmap, &xfull[sb], hh0[sb] * d.P, ht[sb], I.b);
+        tma_load_3d(xb + kWin * 128, &xmap, &xfull[sb], (hh0[sb] + 1) * d.P, ht[sb], I.b);
+      }
+      // the last windows' y
+      for (int k = max(0, n - nxb); ok && k < n; ++k)
+        if (!store(k)) ok = false;
+      tma_store_wait_all();
+      // on a timeout: wait (bounded) for the X copies still in flight before the CTA exits
+      if (!ok)
+        for (int k = max(0, n - nxb); k <= n; ++k) mbar_wait(&xfull[xs(k)], xph(k), spin_ns);
+    }
+  } else if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer: the ring
+    // Per window, in the order the tensor core consumes them: M (intra product, issued one
+    // window ahead), then C (carried-state product) and B (state product) by 128-column halves.
+    if (lane == 0) {
+      int it = 0;
+      for (int n = 0; ok; ++n) {
+        WinInfo I;
+        if (!read_info1(n, I)) {
+          ok = false;
+          break;
+        }
+        if (I.flags & 4) break;
+        const int h0 = 2 * I.pair, g = h0 / (d.H / d.G), t0 = I.w * kWin;
+        const int nitems = 1 + 2 * nhalf;
+        for (int q = 0; q < nitems && ok; ++q, ++it) {
+          const int s = it % Ls.stages, rnd = it / Ls.stages;
+          if (rnd > 0 && !mbar_wait(&empty[s], (rnd - 1) & 1, spin_ns)) {
+            ok = false;
+            break;
+          }
+          uint8_t* st = smem + Ls.ring + s * kStage;
+          if (q == 0) {
+            mbar_arrive_expect_tx(&full[s], 2 * kAtom);
+            const int row = ((I.b * nw + I.w) * d.G + g) * kWin;
+            tma_load_2d(st, &mmap, &full[s], 0, row);
+            tma_load_2d(st + kAtom, &mmap, &full[s], 64, row);
+          } else {
+            const bool isC = q <= nhalf;
+            const int hf = isC ? q - 1 : q - 1 - nhalf;
+            const int na = min(2, natom - 2 * hf);
+            mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(na) * kAtom);
+            for (int a = 0; a < na; ++a)
+              tma_load_4d(st + a * kAtom, isC ? &cmap : &bmap, &full[s], hf * 128 + a * 64, g, t0, I.b);
+          }
+        }
+      }
+      // on a timeout: wait (bounded) for the copies still in flight before the CTA exits
+      if (!ok)
+        for (int k = max(0, it - Ls.stages); k < it; ++k) mbar_wait(&full[k % Ls.stages], (k / Ls.stages) & 1, spin_ns);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    // Per window n: the carried-state product C O(n)^T (so that O is free when the state
+    // product completes), the state product S(n), then the next window's intra product.
+    if (lane == 0) {
+      const uint32_t id_st = idesc_f32acc(1, 128, d.N < 128 ? d.N : 128, 1, 1);  // X^ pair^T x B (MN / MN)
+      const uint32_t id_in = idesc_f32acc(1, 128, 128, 0, 1);  // M (K-major) x X^ pair (MN-major)
+      const uint32_t id_yo = idesc_f32acc(1, 128, 128, 0, 0);  // C x O (both K-major)
+      const uint32_t xlbo = kWin * 128;                         // head stride in the X buffer
+      const uint32_t ob = smem_u32(smem + Ls.obuf);
+      int it = 0;
+      auto stage = [&](int i) -> uint32_t {
+        const int s = i % Ls.stages;
+        if (!mbar_wait(&full[s], (i / Ls.stages) & 1, spin_ns)) return 0u;
+        return smem_u32(smem + Ls.ring + s * kStage);
+      };
+      auto release = [&](int i) { mma_commit(&empty[i % Ls.stages]); };
+      // intra product of window n (its M is ring item `it`): false on a timeout
+      auto intra = [&](int n) -> bool {
+        if (!mbar_wait(&xready[xs(n)], xph(n), spin_ns)) return false;
+        if (n >= 2 && !mbar_wait(&yfree[n & 1], yph(n - 2), spin_ns)) return false;
+        const uint32_t sm = stage(it);
+        if (!sm) return false;
+        tc_fence_after();
+        if (scal[xs(n)].fast[0] && scal[xs(n)].fast[1]) {
+          const uint32_t xb = smem_u32(smem + Ls.xbuf + xs(n) * kXBytes);
+          for (int k = 0; k < kWin / 16; ++k)
+            mma_ss<false>(tmem + kColY + 128 * (n & 1), sdesc_sw128(sm + (k >> 2) * kAtom + (k & 3) * 32, 16, 1024),
+                          sdesc_sw128(xb + k * 2048, xlbo, 1024), id_in, k != 0 ? 1u : 0u);
+        }
+        release(it++);
+        return true;
+      };
+      WinInfo cur;
+      if (!read_info1(0, cur)) ok = false;
+      if (ok && !(cur.flags & 4) && !intra(0)) ok = false;
+      for (int n = 0; ok && !(cur.flags & 4); ++n) {
+        const int yb = n & 1;
+        const bool fast = scal[xs(n)].fast[0] && scal[xs(n)].fast[1];
+        if (!mbar_wait(&hready[yb], yph(n), spin_ns)) {  // pi h_in and O(n) in place
+          ok = false;
+          break;
+        }
+        // carried state: output += C O(n)^T over dstate
+        for (int hf = 0; hf < nhalf && ok; ++hf) {
+          const uint32_t sc = stage(it);
+          if (!sc) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const int na = min(2, natom - 2 * hf);
+          for (int k = 0; k < 4 * na; ++k)
+            mma_ss<false>(tmem + kColY + 128 * yb, sdesc_sw128(sc + (k >> 2) * kAtom + (k & 3) * 32, 16, 1024),
+                          sdesc_sw128(ob + (2 * hf + (k >> 2)) * kAtom + (k & 3) * 32, 16, 1024), id_yo,
+                          (fast || hf != 0 || k != 0) ? 1u : 0u);
+          release(it++);
+        }
+        if (!ok) break;
+        mma_commit(&cdone[yb]);
+        // S(n): accumulate X^^T B onto the state
+        const uint32_t xb = smem_u32(smem + Ls.xbuf + xs(n) * kXBytes);
+        for (int hf = 0; hf < nhalf && ok; ++hf) {
+          const uint32_t sb = stage(it);
+          if (!sb) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          for (int k = 0; k < kWin / 16; ++k)
+            mma_ss<false>(tmem + kColH + 128 * hf, sdesc_sw128(xb + k * 2048, xlbo, 1024),
+                          sdesc_sw128(sb + k * 2048, kAtom, 1024), id_st, 1u);
+          release(it++);
+        }
+        if (!ok) break;
+        mma_commit(&dfull[yb]);
+        // the next window's intra product
+        if (!read_info1(n + 1, cur)) {
+          ok = false;
+          break;
+        }
+        if (!(cur.flags & 4) && !intra(n + 1)) {
+          ok = false;
+          break;
+        }
+      }
+    }
+  } else if (warp < 8) {
+    // ------------------------------------------------------------ state pass
+    const int et = threadIdx.x - 128;  // TMEM lane = state row (head hd, p)
+    const int quad = warp & 3;
+    const int hd = et >> 6, p = et & 63;
+    const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+    const uint32_t tH = tmem + lane_base + kColH;
+    constexpr uint32_t bar_s = 1;
+    uint8_t* orow = smem + Ls.obuf + et * 128;  // this row of O in each 64-column atom
+    // O as bf16 chunks of one 32-column strip
+    auto put_o = [&](int n0, const uint32_t* hb) {
+      const float* h = reinterpret_cast<const float*>(hb);
+      uint8_t* oat = orow + (n0 >> 6) * kAtom;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint4 o;
+        o.x = pack_bf16x2(h[8 * c], h[8 * c + 1]);
+        o.y = pack_bf16x2(h[8 * c + 2], h[8 * c + 3]);
+        o.z = pack_bf16x2(h[8 * c + 4], h[8 * c + 5]);
+        o.w = pack_bf16x2(h[8 * c + 6], h[8 * c + 7]);
+        const int cc = ((n0 & 63) >> 3) + c;
+        *reinterpret_cast<uint4*>(oat + ((cc ^ (et & 7)) << 4)) = o;
+      }
+    };
+    // before writing O for window m: the carried product of window m - 1 is done
+    auto o_free = [&](int m) -> bool { return m < 1 || mbar_wait(&cdone[(m - 1) & 1], yph(m - 1), spin_ns); };
+    // the window's scalars: alpha = e^{G_S} and the rescaled-form flag of this head
+    float alpha = 1.f;
+    bool fastH = true;
+    for (int n = 0; ok; ++n) {
+      WinInfo I;
+      if (named_bar_or(bar_s, 128, !read_info(n, I))) {
+        ok = false;
+        break;
+      }
+      if (I.flags & 4) break;
+      const int yb = n & 1;
+      const bool first = I.flags & 1, last = I.flags & 2;
+      const int h = 2 * I.pair + hd;
+      const int64_t hrow = ((static_cast<int64_t>(I.b) * d.H + h) * d.P + p) * d.N;  // [B][H][P][N]
+      float4* slot = reinterpret_cast<float4*>(hslot + (static_cast<int64_t>(I.b) * hp + I.pair) * 128 * d.N) + et;
+      const bool seq_first = I.w == 0, seq_last = I.w == nw - 1;
+      if (first) {
+        // the state entering the run: predecessor's slot, init_state or zero, put in place
+        // as pi * h_in with O = h_in
+        bool bad = !mbar_wait(&xready[xs(n)], xph(n), spin_ns) || !o_free(n);
+        if (!seq_first && et == 0) bad = bad || !wait_flag_geq(flags + I.b * hp + I.pair, I.w, spin_ns);
+        if (named_bar_or(bar_s, 128, bad)) {
+          ok = false;
+          break;
+        }
+        alpha = scal[xs(n)].alpha[hd];
+        fastH = scal[xs(n)].fast[hd] != 0;
+        const float* hin = seq_first ? (init ? init + hrow : nullptr) : nullptr;
+        const float pre = fastH ? 1.f : alpha;
+#pragma unroll 1
+        for (int n0 = 0; n0 < d.N; n0 += 64) {  // two strips' loads in flight
+          float hv[64];
+#pragma unroll
+          for (int q = 0; q < 16; ++q) {
+            const float4 h4 = !seq_first ? __ldcg(slot + ((n0 >> 5) * 8 + q) * 128)
+                              : hin      ? __ldcg(reinterpret_cast<const float4*>(hin + n0) + q)
+                                         : make_float4(0.f, 0.f, 0.f, 0.f);
+            hv[4 * q] = h4.x;
+            hv[4 * q + 1] = h4.y;
+            hv[4 * q + 2] = h4.z;
+            hv[4 * q + 3] = h4.w;
+          }
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            uint32_t* hb = reinterpret_cast<uint32_t*>(hv + 32 * half);
+            put_o(n0 + 32 * half, hb);  // O = h_in
+#pragma unroll
+            for (int q = 0; q < 32; ++q) hv[32 * half + q] *= pre;
+            tmem_st32(tH + n0 + 32 * half, *reinterpret_cast<uint32_t(*)[32]>(hb));
+          }
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        fence_proxy_async_smem();
+        mbar_arrive(&hready[yb]);
+      }
+      // the pass over window n's state, h_out = mu * (pi h_in + X^T B), as soon as the state
+      // product is done (the carried product before it has released O)
+      {
+        if (named_bar_or(bar_s, 128, !mbar_wait(&dfull[yb], yph(n), spin_ns) || (!last && !o_free(n + 1)))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const float mu = fastH ? alpha : 1.f;
+        // one 32-column strip: h = mu * v, then the state and O for the next window, or the
+        // published state
+        auto strip = [&](int n0, uint32_t (&v)[32]) {
+#pragma unroll
+          for (int q = 0; q < 32; ++q) v[q] = __float_as_uint(mu * __uint_as_float(v[q]));
+          const float* hv = reinterpret_cast<const float*>(v);
+          if (!last) {
+            tmem_st32(tH + n0, v);
+            put_o(n0, v);
+          } else if (!seq_last) {  // publish for the run that continues this sequence
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              __stcg(slot + ((n0 >> 5) * 8 + q) * 128, make_float4(hv[4 * q], hv[4 * q + 1], hv[4 * q + 2], hv[4 * q + 3]));
+          } else if (final_state) {
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              reinterpret_cast<float4*>(final_state + hrow + n0)[q] =
+                  make_float4(hv[4 * q], hv[4 * q + 1], hv[4 * q + 2], hv[4 * q + 3]);
+          }
+        };
+        // strips in pairs, the next strip's load in flight while one is processed
+        uint32_t va[32], vb[32];
+        tmem_ld32(tH, va);
+#pragma unroll 1
+        for (int n0 = 0; n0 < d.N; n0 += 64) {
+          tmem_ld_wait();
+          tmem_ld32(tH + n0 + 32, vb);
+          strip(n0, va);
+          tmem_ld_wait();
+          if (n0 + 64 < d.N) tmem_ld32(tH + n0 + 64, va);
+          strip(n0 + 32, vb);
+        }
+        if (!last) {
+          tmem_st_wait();
+          // the next window's scalars (its X scaled); on the exact form the state it
+          // accumulates onto is e^{G_S} h_in, so rescale (rare)
+          if (named_bar_or(bar_s, 128, !mbar_wait(&xready[xs(n + 1)], xph(n + 1), spin_ns))) {
+            ok = false;
+            break;
+          }
+          alpha = scal[xs(n + 1)].alpha[hd];
+          fastH = scal[xs(n + 1)].fast[hd] != 0;
+          if (!fastH) {
+#pragma unroll 1
+            for (int n0 = 0; n0 < d.N; n0 += 32) {
+              uint32_t w32[32];
+              tmem_ld32(tH + n0, w32);
+              tmem_ld_wait();
+#pragma unroll
+              for (int q = 0; q < 32; ++q) w32[q] = __float_as_uint(alpha * __uint_as_float(w32[q]));
+              tmem_st32(tH + n0, w32);
+            }
+            tmem_st_wait();
+          }
+          tc_fence_before();
+          fence_proxy_async_smem();
+          mbar_arrive(&hready[(n + 1) & 1]);
+        } else {
+          tc_fence_before();
+          if (!seq_last) {
+            __threadfence();
+            named_bar_sync(bar_s, 128);
+            if (et == 0) st_release_gpu(flags + I.b * hp + I.pair, I.w + 1);
+          }
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ head warpgroups: cumsum, X scaling, epilogue
+    const int hh = (warp - 8) >> 2;  // head of the pair
+    const int et = threadIdx.x - 256 - 128 * hh;
+    const int quad = warp & 3;
+    const int r = quad * 32 + lane;  // token row = TMEM lane of the output
+    const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+    const uint32_t bar_h = 2 + hh;
+
+    // window n from the ring, and this token's dt load issued (used a window later).
+    // False at the end.
+    auto fetch = [&](int n, Ctx& c) -> bool {
+      WinInfo I;
+      if (named_bar_or(bar_h, 128, !read_info(n, I))) {
+        ok = false;
+        return false;
+      }
+      c.b = I.b;
+      c.pair = I.pair;
+      c.w = I.w;
+      c.flags = I.flags;
+      if (I.flags & 4) return false;
+      const int t = I.w * kWin + r;
+      c.dt = t < d.L ? __ldg(dtg + (static_cast<int64_t>(I.b) * d.L + t) * d.H + 2 * I.pair + hh) : 0.f;
+      return true;
+    };
+    // window n's cumsum, scalars and this head's X scaled in place
+    auto prepare = [&](int n, Ctx& c) -> bool {
+      const int h = 2 * c.pair + hh;
+      float total;
+      const float G = wg_scan(c.dt * Avec[h], scanws + (hh * 2 + (n & 1)) * 4, bar_h, lane, quad, total);
+      c.g = G * kLog2e;
+      c.gS = total * kLog2e;
+      c.fastH = -c.gS <= kSpan;  // G is non-increasing, so the window's decay bounds every exponent
+      const int sb = xs(n);
+      // the X buffer has landed, so window n - nxb (same buffer and scalar slot) has been
+      // stored: its readers of the slot are all done
+      if (named_bar_or(bar_h, 128, !mbar_wait(&xfull[sb], xph(n), spin_ns))) {
+        ok = false;
+        return false;
+      }
+      if (et == 0) {
+        scal[sb].alpha[hh] = fast_exp2(c.gS);
+        scal[sb].fast[hh] = c.fastH;
+      }
+      // X^ (window start as reference) or X~ (window end) for this head, in place; the
+      // row's eight 16-byte chunks are all loaded before any is written back
+      const float wfac = fast_exp2(c.fastH ? -c.g : c.gS - c.g) * c.dt;
+      uint4* row = reinterpret_cast<uint4*>(smem + Ls.xbuf + sb * kXBytes + hh * kWin * 128 + r * 128);
+      uint4 xv[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) xv[k] = row[k ^ (r & 7)];  // the warp's 32 rows spread over all banks
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        xv[k].x = scale_bf16x2(xv[k].x, wfac);
+        xv[k].y = scale_bf16x2(xv[k].y, wfac);
+        xv[k].z = scale_bf16x2(xv[k].z, wfac);
+        xv[k].w = scale_bf16x2(xv[k].w, wfac);
+        row[k ^ (r & 7)] = xv[k];
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(&xready[sb]);
+      return true;
+    };
+
+    Ctx cur, nxt, nn;
+    bool more = fetch(0, cur) && prepare(0, cur);
+    bool more1 = more && fetch(1, nxt);
+    for (int n = 0; ok && more; ++n) {
+      if (more1 && !prepare(n + 1, nxt)) break;
+      const bool more2 = more1 && fetch(n + 2, nn);
+      if (!ok) break;
+      const int yb = n & 1, sb = xs(n);
+      const int h = 2 * cur.pair + hh;
+      const int t0 = cur.w * kWin;
+      // y = r_i * acc + D x_i, written over X^ in the X buffer (once the state product,
+      // issued after the carried one, has read X^ too); warp 3 stores it
+      if (named_bar_or(bar_h, 128, !mbar_wait(&xready[sb], xph(n), spin_ns) ||
+                                       !mbar_wait(&cdone[yb], yph(n), spin_ns) ||
+                                       !mbar_wait(&dfull[yb], yph(n), spin_ns))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const bool fast = scal[sb].fast[0] && scal[sb].fast[1];
+      const float Dh = Dvec[h];
+      uint8_t* xr = smem + Ls.xbuf + sb * kXBytes + hh * kWin * 128 + r * 128;
+      const uint32_t tacc = tmem + lane_base + kColY + 128 * yb + 64 * hh;
+      if (fast) {
+        uint32_t ya[64];
+        tmem_ld32(tacc, *reinterpret_cast<uint32_t(*)[32]>(ya));
+        tmem_ld32(tacc + 32, *reinterpret_cast<uint32_t(*)[32]>(ya + 32));
+        tmem_ld_wait();
+        tc_fence_before();
+        mbar_arrive(&yfree[yb]);
+        const float ri = fast_exp2(cur.g);
+        const float wfac = fast_exp2(-cur.g) * cur.dt;
+        // D x_i = (r_i D / dt_i) X^_i while X^_i = wfac x_i is well inside the normal range;
+        // otherwise (rare) x_i itself is read back from global memory
+        float c = ri * Dh / cur.dt;
+        if (!(wfac >= 0x1p-80f)) {
+          c = Dh;
+          const bool in_seq = t0 + r < d.L;
+          const uint4* xi =
+              reinterpret_cast<const uint4*>(xg + ((static_cast<int64_t>(cur.b) * d.L + t0 + r) * d.H + h) * d.P);
+#pragma unroll 1
+          for (int k = 0; k < 8; ++k)
+            *reinterpret_cast<uint4*>(xr + ((k ^ (r & 7)) << 4)) = in_seq ? __ldg(xi + k) : make_uint4(0, 0, 0, 0);
+        }
+        uint4 xv[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) xv[k] = *reinterpret_cast<const uint4*>(xr + ((k ^ (r & 7)) << 4));
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          uint32_t* vw = reinterpret_cast<uint32_t*>(&xv[k]);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int pi = 8 * k + 2 * e;
+            vw[e] = pack_bf16x2(fmaf(c, bf16_lo(vw[e]), ri * __uint_as_float(ya[pi])),
+                                fmaf(c, bf16_hi(vw[e]), ri * __uint_as_float(ya[pi + 1])));
+          }
+          *reinterpret_cast<uint4*>(xr + ((k ^ (r & 7)) << 4)) = xv[k];
+        }
+      } else {
+        const int g = (2 * cur.pair) / (d.H / d.G);
+        const __nv_bfloat16* Mrow = Mg + ((static_cast<int64_t>(cur.b) * nw + cur.w) * d.G + g) * kWin * kWin +
+                                    static_cast<int64_t>(r) * kWin;
+        exact_epilogue(d, cur.b, h, t0, r, cur.g, Avec[h], Dh, Mrow, xg, dtg, tacc, xr);
+        tc_fence_before();
+        mbar_arrive(&yfree[yb]);
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(&ystaged[sb]);
+      cur = nxt;
+      nxt = nn;
+      more = more1;
+      more1 = more2;
+    }
+  }
+
+  if (!ok) atomicExch(status, static_cast<int>(SSD_ERR_DEVICE_TIMEOUT));
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace
+
+size_t onepass_smem_bytes(const Dims& d) { return op_layout(d.N).total + 1024; }
+
+int onepass_runs(const Dims& d, int R) {
+  const int nw = (d.L + kWin - 1) / kWin;
+  return ((nw + R - 1) / R) * d.B * (d.H / 2);
+}
+
+cudaError_t launch_onepass(const Dims& d, const OnePassMaps& maps, const float* dt, const float* A, const float* D,
+                           const void* x, const float* init, float* final_state, const Work& w, uint64_t spin_ns,
+                           cudaStream_t stream, bool dependent) {
+  const int R = 4;  // windows per run
+  const int nruns = onepass_runs(d, R);
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const size_t smem = onepass_smem_bytes(d);
+  e = cudaFuncSetAttribute(ssd_onepass_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  const int grid = nruns < sms ? nruns : sms;
+  return launch_k(ssd_onepass_kernel, dim3(grid), dim3(kThreads), smem, stream, dependent, maps.x, maps.cm, maps.bm,
+                  maps.m, maps.y, d, R, dt, A, D, static_cast<const __nv_bfloat16*>(w.cbm), init, final_state,
+                  w.hslot, w.flags, w.counter, static_cast<const __nv_bfloat16*>(x), w.status, spin_ns);
+}
+
+}  // namespace ssd

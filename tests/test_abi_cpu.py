@@ -78,7 +78,10 @@ def test_workspace_layout(ext):
             assert lay["total"] >= lay["states_bf16"] + extra
             # fp32: room for Bm as transposed TF32 boxes (B * G * Lp * N floats), bf16: none
             bT = 2 * 1 * Lp * 128 * 4 if dt == ext.SSD_F32 else 0
-            assert lay["total"] - lay["bT"] >= bT and lay["bT"] >= lay["hslot"] + 2 * 32 * 64 * 128 * 4
+            assert lay["cbm"] - lay["bT"] >= bT and lay["bT"] >= lay["hslot"] + 2 * 32 * 64 * 128 * 4
+            # bf16: the causal C B^T block of every (batch, 128-token window, group)
+            cbm = 2 * (-(-L // 128)) * 1 * 128 * 128 * 2 if dt == ext.SSD_BF16 else 0
+            assert lay["total"] - lay["cbm"] >= cbm
             assert ext.ssd_fwd_workspace_size(s) == lay["total"]
     assert ext.ssd_fwd_workspace_size(shape(ext, dstate=100)) == 0
 
@@ -144,6 +147,7 @@ def test_workspace_views_are_disjoint_and_inside(ext):
             for (a0, a1, na), (b0, b1, nb) in zip(spans, spans[1:]):
                 assert a1 <= b0, (na, nb)
             assert ("bT" in dict((n, 1) for _, _, n in spans)) == (dt == ext.SSD_F32)
+            assert ("cbm" in dict((n, 1) for _, _, n in spans)) == (dt == ext.SSD_BF16)
 
 
 def test_step_entry_points_reject_bad_arguments_before_any_launch(ext):
@@ -174,12 +178,21 @@ def test_step_entry_points_reject_bad_arguments_before_any_launch(ext):
         assert lib.ssd_compute_out(by(s), fake, fake, odd4, fake, fake, fake, need, None) == 1
         assert lib.ssd_compute_out(by(s), fake, fake, fake, odd2, fake, fake, need, None) == 1
         if dt == ext.SSD_F32:  # the one-pass schedule is bf16 only
-            assert lib.ssd_fused_pass(by(s), fake, fake, fake, fake, None, fake, None, fake, need, None) == 2
+            assert lib.ssd_fused_pass(by(s), fake, fake, fake, fake, fake, fake, None, fake, None, fake, need,
+                                      None) == 2
             assert lib.ssd_fwd_fused(by(s), fake, fake, fake, fake, fake, fake, None, fake, None, fake, need,
                                      None) == 2
+            assert lib.ssd_causal_cb(by(s), fake, fake, fake, need, None) == 2
         else:
-            assert lib.ssd_fused_pass(by(s), None, fake, fake, fake, None, fake, None, fake, need, None) == 1
-            assert lib.ssd_fused_pass(by(s), fake, fake, fake, fake, odd4, fake, None, fake, need, None) == 1
+            assert lib.ssd_fused_pass(by(s), None, fake, fake, fake, fake, fake, None, fake, None, fake, need,
+                                      None) == 1
+            assert lib.ssd_fused_pass(by(s), fake, fake, fake, fake, fake, fake, odd4, fake, None, fake, need,
+                                      None) == 1
+            assert lib.ssd_fused_pass(by(s), fake, odd2, fake, fake, fake, fake, None, fake, None, fake, need,
+                                      None) == 1
+            assert lib.ssd_causal_cb(by(s), None, fake, fake, need, None) == 1
+            assert lib.ssd_causal_cb(by(s), fake, odd4, fake, need, None) == 1
+            assert lib.ssd_causal_cb(by(s), fake, fake, fake, need - 1, None) == 3
     big = shape(ext, batch=4, seqlen=4096, nheads=80, dtype=ext.SSD_BF16)
     assert ext.ssd_fwd_workspace_size(big) > (32 << 20)
     assert lib.ssd_fwd_static_scratch(by(big), fake, fake, fake, fake, fake, fake, None, fake, None, None) == 3

@@ -22,9 +22,10 @@ def test_kernel_model_adds_up(name):
     km = bench.kernel_model(w)
     total = sum(by.values())
     assert km["chunk_state"]["flops"] + km["compute_out"]["flops"] == flops
-    assert km["ssd_fused"]["flops"] == flops and km["chunk_cumsum"]["flops"] == 0
-    # one pass: every byte of the step except dt and A, which chunk_cumsum reads
-    assert km["ssd_fused"]["bytes"] + km["chunk_cumsum"]["bytes"] == total
+    assert km["causal_cb"]["flops"] + km["ssd_onepass"]["flops"] == flops and km["chunk_cumsum"]["flops"] == 0
+    # one pass: the main kernel touches every byte of the step; the causal C B^T blocks read Bm and Cm once more
+    assert km["ssd_onepass"]["bytes"] == total
+    assert km["causal_cb"]["bytes"] == by["BmCm"]
     # staged: x and Bm are read twice (chunk_state, then compute_out)
     assert sum(km[k]["bytes"] for k in STAGED) == total + by["x"] + by["BmCm"] // 2
     assert by["init"] == (by["final"] if w.init_state else 0)

@@ -1,10 +1,11 @@
 """The one-pass schedule (C: ssd_fwd_fused) against the fp64 oracle
 recurrence, element by element, on bf16 shapes chosen to reach every branch
-of the kernel: window sizes 64 and 128 (chunk sizes 64, 128, 256), dstate 64,
-128 and 256 (runs of four windows with the state kept in tensor memory, or of
-one window), grouped heads, ragged and one-token sequences, initial states,
-windows that take the exact fallback next to windows that take the rescaled
-form, and the full-size workloads the benchmark times (sampled pairs).
+of the kernels: windows of 128 tokens whatever the chunk size (64, 128, 256),
+dstate 64, 128 and 256 (two carried-state operand buffers, or one), runs of
+windows chained through the workspace flags, grouped heads, ragged and
+one-token sequences, initial states, windows that take the exact path next
+to windows on the rescaled form, and the full-size workloads the benchmark
+times (sampled pairs).
 
 Tolerance: max|out - ref| / max|ref| <= 2e-2 for bf16 inputs, on y and on the
 final state."""

@@ -144,3 +144,37 @@ def test_launch_ranges_equal_the_full_forward(over):
     torch.cuda.synchronize()
     assert torch.equal(y1, y2) and torch.equal(f1, f2)
     assert ssd.ssd_fwd_check(ws2) == 0
+
+
+@pytest.mark.parametrize("over", [dict(batch=2, seqlen=300, nheads=4, ngroups=2, dstate=128, chunk_size=256),
+                                  dict(seqlen=128, nheads=2, dstate=64, chunk_size=64),
+                                  dict(seqlen=200, nheads=2, dstate=256, chunk_size=128)],
+                         ids=["N128-G2-ragged", "N64", "N256"])
+def test_causal_cb_blocks(over):
+    """Step 1 of the one-pass schedule alone: every (batch, 128-token window,
+    group) block equals C B^T of that window (fp64 product of the same bf16
+    inputs) up to bf16 rounding, with the upper triangle exactly zero and
+    rows and columns past the sequence zero."""
+    ssd, w, inp, d = None, None, None, None
+    ssd, w, inp, d, shape, ws = _setup(dict(over, dtype="bf16"))
+    ssd.ssd_causal_cb(shape, d["Bm"], d["Cm"], ws)
+    torch.cuda.synchronize()
+    M = ssd.workspace_views(shape, ws)["cbm"].float().cpu().numpy().astype(np.float64)
+    B, L, G, N = inp["Bm"].shape
+    nw = -(-L // 128)
+    assert M.shape == (B, nw, G, 128, 128)
+    Bp = np.zeros((B, nw * 128, G, N))
+    Cp = np.zeros((B, nw * 128, G, N))
+    Bp[:, :L] = inp["Bm"]
+    Cp[:, :L] = inp["Cm"]
+    tri = np.tril(np.ones((128, 128), dtype=bool))
+    for b in range(B):
+        for k in range(nw):
+            for g in range(G):
+                c = Cp[b, 128 * k:128 * (k + 1), g]
+                bb = Bp[b, 128 * k:128 * (k + 1), g]
+                ref = np.where(tri, c @ bb.T, 0.0)
+                got = M[b, k, g]
+                assert np.all(got[~tri] == 0.0)
+                assert np.all(np.abs(got - ref) <= 2.0 ** -8 * np.abs(ref) + 1e-5), (b, k, g)
+    assert int(ssd.workspace_views(shape, ws)["status"].item()) == 0
