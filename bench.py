@@ -220,17 +220,29 @@ def whole_job_tokens_per_s(tokens_per_rank: int, world: int, ms: float) -> float
 
 # ------------------------------------------------------------------ GPU arm
 
+SHARED_HEADERS = ("ptx.cuh", "ssd_internal.cuh", "tile_transpose.cuh")
+
+
+def kernel_source_digest(kernel: str, root: str = None) -> str:
+    """Digest of a kernel's source as compiled: its .cu file and the shared
+    device headers every kernel includes (a change to either can change what
+    the kernel does)."""
+    csrc = os.path.join(root or ROOT, "mamba_ssd_forward_chunked_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in (kernel + ".cu",) + SHARED_HEADERS:
+        h.update(open(os.path.join(csrc, name), "rb").read())
+    return h.hexdigest()[:16]
+
+
 def _profile_traffic(kernel: str, workload: str):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on
     the current source of that kernel (else None)."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.json")
-    src = os.path.join(ROOT, "mamba_ssd_forward_chunked_gb300", "csrc", kernel + ".cu")
     try:
         with open(path) as f:
             rec = json.load(f)
         e = rec[workload][kernel]
-        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-        if e.get("source_sha256_16") != digest:
+        if e.get("source_sha256_16") != kernel_source_digest(kernel):
             return None
         return float(e["dram_bytes_per_launch"])
     except Exception:

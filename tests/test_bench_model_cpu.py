@@ -2,7 +2,6 @@
 adds up to the step's algorithmic totals, the TF32 peak is the bf16 peak times
 the measured (else the nominal) TF32/bf16 ratio, the clock summary reads nvidia-smi's CSV lines, and a DRAM
 traffic record is used only while its kernel's source file is unchanged."""
-import hashlib
 import json
 import os
 import shutil
@@ -60,22 +59,21 @@ def test_traffic_record_is_used_only_for_the_source_it_was_taken_on(tmp_path, mo
         if workload.startswith("_"):
             continue
         for kernel, e in kernels.items():
-            src = os.path.join(bench.ROOT, "mamba_ssd_forward_chunked_gb300", "csrc", kernel + ".cu")
-            same = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16] == e["source_sha256_16"]
+            same = bench.kernel_source_digest(kernel) == e["source_sha256_16"]
             got = bench._profile_traffic(kernel, workload)
             assert got == (float(e["dram_bytes_per_launch"]) if same else None), (workload, kernel)
-    # a record taken on another source of the kernel is ignored
+    # a record taken on another source of the kernel, or of a header it includes, is ignored
     root = tmp_path / "repo"
     (root / "profiles").mkdir(parents=True)
     csrc = root / "mamba_ssd_forward_chunked_gb300" / "csrc"
     csrc.mkdir(parents=True)
-    shutil.copy(os.path.join(bench.ROOT, "mamba_ssd_forward_chunked_gb300", "csrc", "compute_out.cu"), csrc)
-    digest = hashlib.sha256(open(csrc / "compute_out.cu", "rb").read()).hexdigest()[:16]
+    for name in ("compute_out.cu",) + bench.SHARED_HEADERS:
+        shutil.copy(os.path.join(bench.ROOT, "mamba_ssd_forward_chunked_gb300", "csrc", name), csrc)
+    digest = bench.kernel_source_digest("compute_out", str(root))
     entry = {"dram_bytes_per_launch": 123.0, "source_sha256_16": digest}
     (root / "profiles" / "dram_traffic.json").write_text(json.dumps({"w": {"compute_out": entry}}))
     monkeypatch.setattr(bench, "ROOT", str(root))
     assert bench._profile_traffic("compute_out", "w") == 123.0
-    with open(csrc / "compute_out.cu", "a") as f:
+    with open(csrc / "ptx.cuh", "a") as f:
         f.write("\n")
     assert bench._profile_traffic("compute_out", "w") is None
-    assert bench._profile_traffic("compute_out", "other") is None
