@@ -12,8 +12,8 @@ published.  Value ``i`` of stream ``k`` is ``mix(key_k + (i + 1) * GAMMA)``,
 so any element can be regenerated on its own.  Uniforms take the top 53 bits;
 normals use the Box-Muller transform on consecutive uniform pairs.
 
-Value recipe (the Mamba-2 layer shapes named in the workload table of the
-SSD-forward write-up, with the distributions stated beside it):
+Value recipe (Mamba-2 layer shapes: the ~370M and ~2.7B layers, a long
+sequence with a large state, and a 65,536-token shape sweep; see WORKLOADS):
 
 * x ~ N(0, 1)
 * Bm, Cm ~ N(0, 1) / sqrt(N)
