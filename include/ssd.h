@@ -142,10 +142,10 @@ size_t ssd_fwd_workspace_size(const ssd_shape* shape);
  *    (SSD_F32: the chunk_cumsum launch also transposes Bm into the workspace,
  *    once for every head of a group; ssd_chunk_state called alone does that
  *    transpose itself).
- * ssd_fwd takes the one-pass schedule for SSD_BF16 when dstate <= 128 and
- * there are at least as many (batch, head pair) sequences as multiprocessors
- * (below that the chain of windows, not bandwidth, bounds the one-pass kernel);
- * otherwise the staged one.  The one-pass schedule works in windows of 128
+ * ssd_fwd takes the one-pass schedule for SSD_BF16 when there are at least as
+ * many (batch, head pair) sequences as multiprocessors (below that the chain
+ * of windows, not bandwidth, bounds the one-pass kernel); otherwise the staged
+ * one.  The one-pass schedule works in windows of 128
  * tokens whatever chunk_size is; the result is the recurrence's either way.
  * init_state may be NULL (zero initial state); final_state
  * may be NULL (not written; the workspace holds the running state instead).
