@@ -37,26 +37,32 @@
 // Before a window's state product it holds pi * h_in (pi = 1 on the rescaled
 // form, e^{G_S} on the exact one), the product X^^T B (resp. X~^T B) is
 // accumulated onto it, and the state pass that follows reads it back, scales
-// it by mu (e^{G_S}, resp. 1) to get h_out, and writes pi' * h_out for the
-// next window plus the bf16 copy of h_out the next window's carried-state
-// product reads.  So the serial chain between windows is one state product and
-// one pass over the state; everything else of a window overlaps it.
+// it by mu (e^{G_S}, resp. 1) to get h_out, writes pi' * h_out back for the
+// next window and hands it over; only then does it write the bf16 copy O of
+// h_out that the next window's carried-state product reads.  So the serial
+// chain between windows is one state product and the tensor-memory half of one
+// pass over the state; the intra and carried-state products, the O writes and
+// the rest of a window overlap it.
 //
-// Runs and chaining.  A claim is a run of up to R consecutive windows of one
-// (batch, head pair); runs are claimed from a global counter in run-major order
-// (all first runs, then all second runs, ...), so a run's predecessor was
-// claimed earlier by a running CTA.  A run's last window publishes its state
-// (fp32, L2-resident workspace slot) and a per-pair flag; the next run's first
-// window waits for the flag (bounded) and loads it.  A sequence's first window
-// reads init_state (or zero) and its last writes final_state.
+// Runs and chaining.  Windows go out in runs (consecutive windows of one
+// sequence, i.e. one (batch, head pair)), either claimed from a global counter
+// or split statically between the CTAs (see the schedule warp below).  A run's
+// last window publishes its state (fp32, L2-resident workspace slot) and a
+// per-pair flag; the next run's first window waits for the flag (bounded) and
+// loads it.  A sequence's first window reads init_state (or zero) and its last
+// writes final_state.
 //
 // GB300 mapping, per CTA (one per SM, 512 threads, persistent):
-//   warp 2       claims runs and publishes their windows in an 8-deep ring.
+//   warp 2       the schedule: publishes the CTA's windows in an 8-deep ring.
 //   warp 0       TMA: a ring of 32 KB stages holding, per window in the order
-//                the tensor core uses them, M (the causal operand), C and B.
+//                the tensor core uses them, B, M (the causal operand) and C
+//                (C before M at dstate 256).
 //   warp 1       owns tensor memory and issues every tcgen05.mma from one
-//                thread, per window n: the carried product C O(n)^T, the state
-//                product S(n), then the next window's intra product M X^.
+//                thread, per window n: the state product S(n) once the state
+//                is handed over, then the intra product M X^ and, once O(n) is
+//                written, the carried product C O(n)^T (at dstate 256 the
+//                carried product first, since the pass writes O for the first
+//                128 columns before the hand-off).
 //   warp 3       TMA for the head pair's X window (three buffers; two at
 //                dstate 256): stores window n - 3's y out of a buffer, then
 //                loads window n's X into it.
@@ -64,9 +70,10 @@
 //   warps 8-15   one warpgroup per head, thread = token row: the window's
 //                cumsum (warp-shuffle scan of dt*A), the X scaling (in place),
 //                and the epilogue of the window before (y written over X).
-// Tensor memory: two output accumulators (columns [0, 256)) and the state
-// (columns [256, 256 + dstate)).  Every wait is bounded; on expiry the CTA
-// records SSD_ERR_DEVICE_TIMEOUT, waits for its own copies and exits.
+// The control warps give registers to the state pass (setmaxnreg).  Tensor
+// memory: two output accumulators (columns [0, 256)) and the state (columns
+// [256, 256 + dstate)).  Every wait is bounded; on expiry the CTA records
+// SSD_ERR_DEVICE_TIMEOUT, waits for its own copies and exits.
 #include "ptx.cuh"
 #include "ssd_internal.cuh"
 
@@ -79,6 +86,25 @@ constexpr int kInfoRing = 8;
 constexpr float kSpan = 100.f;  // log2 bound of the window decay for the rescaled form
 constexpr uint32_t kStage = 32768, kAtom = 16384, kXBytes = 32768;
 constexpr uint32_t kColY = 0, kColH = 256, kTmemCols = 512;
+
+// Register split between the warpgroups (setmaxnreg): the CTA is launched with
+// kRegLaunch per thread; the control warpgroup (one active lane per warp) gives
+// registers up and the state warpgroup, which holds a window's bf16 state copy
+// across the hand-off, takes them; the head warpgroups keep the launch count.
+// The split must stay within the launch's pool (an increase that cannot be met
+// waits without end), which the host checks against the compiled register count
+// before every launch.
+constexpr uint32_t kRegLaunch = 128, kRegCtl = 56, kRegState = 200;
+static_assert(128 * (kRegCtl + kRegState + 2 * kRegLaunch) <= kThreads * kRegLaunch, "register split above the pool");
+
+template <uint32_t kRegs>
+__device__ __forceinline__ void regs_release() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
+template <uint32_t kRegs>
+__device__ __forceinline__ void regs_acquire() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
 
 struct WinInfo {
   int b, pair, w;  // batch, head pair, window index in the sequence
@@ -209,10 +235,11 @@ __device__ __forceinline__ void exact_epilogue(const Dims& d, int b, int h, int 
 
 // A head-warpgroup thread's view of one window.
 struct Ctx {
-  int b, pair, w, flags;
+  int b, pair, w;
   float g;   // log2 cumsum at this token (window start = 0)
-  float gS;  // log2 cumsum at the window end
   float dt;  // dt at this token (0 past the sequence)
+  float a;   // A_h
+  float dd;  // D_h
   int fastH; // rescaled form valid for this head
 };
 
@@ -230,11 +257,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int natom = d.N / 64;           // 64-column atoms of dstate
   const int nhalf = (d.N + 127) / 128;  // 128-column halves (stages) of B and C
   const int nxb = Ls.nxb;
-  const uint32_t obytes = static_cast<uint32_t>(natom) * kAtom;
   const int hp = d.H / 2;
   const int nw = (d.L + kWin - 1) / kWin;
-  const int runs_per_seq = (nw + R - 1) / R;
-  const int nruns = runs_per_seq * d.B * hp;
   // Window n of this CTA uses X buffer (and scalar slot) n % nxb and output accumulator n % 2.
   auto xs = [&](int n) { return n % nxb; };
   auto xph = [&](int n) { return static_cast<uint32_t>((n / nxb) & 1); };
@@ -247,10 +271,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* ystaged = bars + 12;  // [3] y written into the X buffer (256: both head warpgroups)
   uint64_t* tfull = bars + 15;    // [8] window ring
   uint64_t* tempty = bars + 23;   // [8] (15 warps read each entry)
-  uint64_t* hready = bars + 31;   // [2] state (pi h_in) and O of the window in place (128)
+  uint64_t* sready = bars + 31;   // [2] state (pi h_in) of the window in place (128)
   uint64_t* dfull = bars + 33;    // [2] state product done (X^ of the window read)
   uint64_t* cdone = bars + 35;    // [2] carried-state product done: O free, output complete
   uint64_t* yfree = bars + 37;    // [2] output accumulator drained (256)
+  uint64_t* oready = bars + 39;   // [2] O (bf16 h_in) of the window in place (128)
+  uint64_t* ydone = bars + 41;    // [2] output accumulator complete (intra and carried products done)
   WinInfo* info = reinterpret_cast<WinInfo*>(smem + Ls.info);
   Scal* scal = reinterpret_cast<Scal*>(smem + Ls.scal);
   float* scanws = reinterpret_cast<float*>(smem + Ls.scan);  // [2 heads][2 windows][4]
@@ -270,7 +296,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&tempty[s], 15);
     }
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&hready[s], 128);
+      mbar_init(&sready[s], 128);
+      mbar_init(&oready[s], 128);
+      mbar_init(&ydone[s], 1);
       mbar_init(&dfull[s], 1);
       mbar_init(&cdone[s], 1);
       mbar_init(&yfree[s], 256);
@@ -316,37 +344,73 @@ __global__ void __launch_bounds__(kThreads, 1)
     return true;
   };
 
+  if (warp < 4) {
+  regs_release<kRegCtl>();
   if (warp == 2) {
-    // ------------------------------------------------------------ run scheduler
+    // ------------------------------------------------------------ schedule
+    // Windows go out in runs: consecutive windows of one sequence (batch, head pair).  Two
+    // schedules (R = run length, 0 for the static one):
+    //  - claims: runs of R windows taken from a global counter in run-major order (all first
+    //    runs, then all second runs, ...), so a run's predecessor was claimed earlier by a
+    //    running CTA; a faster CTA takes more runs.
+    //  - static: the CTA's share of the list of all windows, sequence by sequence,
+    //    [c T / P, (c + 1) T / P) for T windows and P CTAs, as runs in this order: the first
+    //    windows of the sequence that crosses the share's end (published for the next CTA),
+    //    the whole sequences inside, and the rest of the sequence that crosses the share's
+    //    start (resumed from the previous CTA).  With P at most the number of sequences a share
+    //    holds at least one sequence's windows, so the previous CTA, which starts with that
+    //    sequence's first windows, has published them before this CTA gets to the rest.  Every
+    //    CTA gets the same number of windows (+-1), where claims of R windows may leave some
+    //    CTAs a whole run more than others.  The list orders sequences by (pair within its
+    //    group, batch, group), so the CTAs c + k P / Q run a group's Q pairs side by side.
     if (lane == 0) {
       int n = 0;
-      for (bool more = true; more && ok;) {
-        const int run = atomicAdd(counter, 1);
-        int b = 0, pair = 0, w0 = 0, w1 = 1;
-        if (run < nruns) {
-          pair = run % hp;
-          b = (run / hp) % d.B;
-          const int k = run / hp / d.B;
-          w0 = k * R;
-          w1 = min(nw, w0 + R);
-        } else {
-          more = false;  // one end marker
-        }
-        for (int w = w0; w < w1 && ok; ++w, ++n) {
+      bool good = true;
+      // windows [w0, w1) of sequence (b, pair) into the ring; flags bit 0 / 1 = first / last
+      // of the run, bit 2 = end marker
+      auto put = [&](int b, int pair, int w0, int w1, int fl) {
+        for (int w = w0; good && w < w1; ++w, ++n) {
           const int ts = n % kInfoRing;
           if (n >= kInfoRing && !mbar_wait(&tempty[ts], ((n / kInfoRing) - 1) & 1, spin_ns)) {
-            ok = false;
+            good = false;
             break;
           }
           WinInfo I;
           I.b = b;
           I.pair = pair;
           I.w = w;
-          I.flags = more ? ((w == w0 ? 1 : 0) | (w == w1 - 1 ? 2 : 0)) : 4;
+          I.flags = fl | (w == w0 ? 1 : 0) | (w == w1 - 1 ? 2 : 0);
           info[ts] = I;
           mbar_arrive(&tfull[ts]);
         }
+      };
+      if (R > 0) {
+        const int nruns = ((nw + R - 1) / R) * d.B * hp;
+        for (;;) {
+          const int run = atomicAdd(counter, 1);
+          if (run >= nruns || !good) break;
+          const int w0 = run / hp / d.B * R;
+          put((run / hp) % d.B, run % hp, w0, min(nw, w0 + R), 0);
+        }
+      } else {
+        const int64_t total = static_cast<int64_t>(d.B) * hp * nw;
+        const int64_t lo = static_cast<int64_t>(blockIdx.x) * total / gridDim.x;
+        const int64_t hi = static_cast<int64_t>(blockIdx.x + 1) * total / gridDim.x;
+        const int s_lo = static_cast<int>(lo / nw), w_lo = static_cast<int>(lo % nw);
+        const int s_hi = static_cast<int>(hi / nw), w_hi = static_cast<int>(hi % nw);
+        const int Q = hp / d.G, nbg = d.B * d.G;  // pairs per group; (batch, group) combinations
+        const int head = w_hi > 0 ? 1 : 0, tail = w_lo > 0 ? 1 : 0;
+        const int first_full = s_lo + tail, nfull = s_hi - first_full;
+        for (int k = 0; good && k < head + nfull + tail; ++k) {
+          // run k: windows [w0, w1) of list entry sq
+          const int sq = k < head ? s_hi : k < head + nfull ? first_full + k - head : s_lo;
+          const int w0 = k < head + nfull ? 0 : w_lo, w1 = k < head ? w_hi : nw;
+          const int q = sq / nbg, bg = sq % nbg;
+          put(bg / d.G, (bg % d.G) * Q + q, w0, w1, 0);
+        }
       }
+      put(0, 0, 0, 1, 4);  // the end marker
+      ok = good;
     }
   } else if (warp == 3) {
     // ------------------------------------------------------------ X loads and y stores
@@ -396,8 +460,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 0) {
     // ------------------------------------------------------------ TMA producer: the ring
-    // Per window, in the order the tensor core consumes them: M (intra product, issued one
-    // window ahead), then C (carried-state product) and B (state product) by 128-column halves.
+    // Per window, in the order the tensor core consumes them: B (state product) by 128-column
+    // halves, then M (intra product) and C (carried-state product, by halves); at dstate 256
+    // C comes before M.
     if (lane == 0) {
       int it = 0;
       for (int n = 0; ok; ++n) {
@@ -416,14 +481,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           uint8_t* st = smem + Ls.ring + s * kStage;
-          if (q == 0) {
+          const int qm = d.N > 128 ? 2 * nhalf : nhalf;  // M after C at dstate 256, before it otherwise
+          if (q == qm) {
             mbar_arrive_expect_tx(&full[s], 2 * kAtom);
             const int row = ((I.b * nw + I.w) * d.G + g) * kWin;
             tma_load_2d(st, &mmap, &full[s], 0, row);
             tma_load_2d(st + kAtom, &mmap, &full[s], 64, row);
           } else {
-            const bool isC = q <= nhalf;
-            const int hf = isC ? q - 1 : q - 1 - nhalf;
+            const bool isC = q >= nhalf && q != qm;
+            const int hf = !isC ? q : q - nhalf - (q > qm ? 1 : 0);
             const int na = min(2, natom - 2 * hf);
             mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(na) * kAtom);
             for (int a = 0; a < na; ++a)
@@ -437,14 +503,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    // Per window n: the carried-state product C O(n)^T (so that O is free when the state
-    // product completes), the state product S(n), then the next window's intra product.
+    // Per window n: the state product S(n) as soon as the state is in place (the serial chain
+    // between windows is S(n) and the pass over its result), then the intra product and,
+    // once O(n) is in place, the carried-state product C O(n)^T; both run during the pass.
     if (lane == 0) {
       const uint32_t id_st = idesc_f32acc(1, 128, d.N < 128 ? d.N : 128, 1, 1);  // X^ pair^T x B (MN / MN)
       const uint32_t id_in = idesc_f32acc(1, 128, 128, 0, 1);  // M (K-major) x X^ pair (MN-major)
       const uint32_t id_yo = idesc_f32acc(1, 128, 128, 0, 0);  // C x O (both K-major)
       const uint32_t xlbo = kWin * 128;                         // head stride in the X buffer
       const uint32_t ob = smem_u32(smem + Ls.obuf);
+      const bool c_first = d.N > 128;  // carried product before the intra product (see below)
       int it = 0;
       auto stage = [&](int i) -> uint32_t {
         const int s = i % Ls.stages;
@@ -452,50 +520,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         return smem_u32(smem + Ls.ring + s * kStage);
       };
       auto release = [&](int i) { mma_commit(&empty[i % Ls.stages]); };
-      // intra product of window n (its M is ring item `it`): false on a timeout
-      auto intra = [&](int n) -> bool {
-        if (!mbar_wait(&xready[xs(n)], xph(n), spin_ns)) return false;
-        if (n >= 2 && !mbar_wait(&yfree[n & 1], yph(n - 2), spin_ns)) return false;
-        const uint32_t sm = stage(it);
-        if (!sm) return false;
-        tc_fence_after();
-        if (scal[xs(n)].fast[0] && scal[xs(n)].fast[1]) {
-          const uint32_t xb = smem_u32(smem + Ls.xbuf + xs(n) * kXBytes);
-          for (int k = 0; k < kWin / 16; ++k)
-            mma_ss<false>(tmem + kColY + 128 * (n & 1), sdesc_sw128(sm + (k >> 2) * kAtom + (k & 3) * 32, 16, 1024),
-                          sdesc_sw128(xb + k * 2048, xlbo, 1024), id_in, k != 0 ? 1u : 0u);
-        }
-        release(it++);
-        return true;
-      };
       WinInfo cur;
       if (!read_info1(0, cur)) ok = false;
-      if (ok && !(cur.flags & 4) && !intra(0)) ok = false;
       for (int n = 0; ok && !(cur.flags & 4); ++n) {
         const int yb = n & 1;
-        const bool fast = scal[xs(n)].fast[0] && scal[xs(n)].fast[1];
-        if (!mbar_wait(&hready[yb], yph(n), spin_ns)) {  // pi h_in and O(n) in place
+        // S(n): accumulate X^^T B onto the state once pi h_in is in place and X^ is scaled
+        if (!mbar_wait(&sready[yb], yph(n), spin_ns) || !mbar_wait(&xready[xs(n)], xph(n), spin_ns)) {
           ok = false;
           break;
         }
-        // carried state: output += C O(n)^T over dstate
-        for (int hf = 0; hf < nhalf && ok; ++hf) {
-          const uint32_t sc = stage(it);
-          if (!sc) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const int na = min(2, natom - 2 * hf);
-          for (int k = 0; k < 4 * na; ++k)
-            mma_ss<false>(tmem + kColY + 128 * yb, sdesc_sw128(sc + (k >> 2) * kAtom + (k & 3) * 32, 16, 1024),
-                          sdesc_sw128(ob + (2 * hf + (k >> 2)) * kAtom + (k & 3) * 32, 16, 1024), id_yo,
-                          (fast || hf != 0 || k != 0) ? 1u : 0u);
-          release(it++);
-        }
-        if (!ok) break;
-        mma_commit(&cdone[yb]);
-        // S(n): accumulate X^^T B onto the state
+        const bool fast = scal[xs(n)].fast[0] && scal[xs(n)].fast[1];
         const uint32_t xb = smem_u32(smem + Ls.xbuf + xs(n) * kXBytes);
         for (int hf = 0; hf < nhalf && ok; ++hf) {
           const uint32_t sb = stage(it);
@@ -504,25 +538,75 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
+          // 16 tokens per MMA: both MN-major operands advance by 16 rows (2048 bytes)
+          const uint64_t da = sdesc_sw128(xb, xlbo, 1024), db = sdesc_sw128(sb, kAtom, 1024);
+#pragma unroll 1
           for (int k = 0; k < kWin / 16; ++k)
-            mma_ss<false>(tmem + kColH + 128 * hf, sdesc_sw128(xb + k * 2048, xlbo, 1024),
-                          sdesc_sw128(sb + k * 2048, kAtom, 1024), id_st, 1u);
+            mma_ss<false>(tmem + kColH + 128 * hf, da + k * (2048 >> 4), db + k * (2048 >> 4), id_st, 1u);
           release(it++);
         }
         if (!ok) break;
         mma_commit(&dfull[yb]);
-        // the next window's intra product
-        if (!read_info1(n + 1, cur)) {
+        // The intra and carried products into output accumulator n % 2, once window n - 2's
+        // output is drained.  Up to dstate 128 the intra product goes first; at dstate 256 the
+        // carried product does, so that O(n) is free early: the pass writes O for the first
+        // 128 columns before it hands the state over.
+        if (n >= 2 && !mbar_wait(&yfree[yb], yph(n - 2), spin_ns)) {
           ok = false;
           break;
         }
-        if (!(cur.flags & 4) && !intra(n + 1)) {
+        auto intra = [&]() -> bool {
+          const uint32_t sm = stage(it);
+          if (!sm) return false;
+          tc_fence_after();
+          if (fast) {
+            // 16 tokens j per MMA: M (K-major, 64-column atoms) advances 32 bytes within an atom,
+            // X^ (MN-major) by 16 rows
+            const uint64_t da = sdesc_sw128(sm, 16, 1024), db = sdesc_sw128(xb, xlbo, 1024);
+#pragma unroll 1
+            for (int k = 0; k < kWin / 16; ++k)
+              mma_ss<false>(tmem + kColY + 128 * yb, da + (k >> 2) * (kAtom >> 4) + (k & 3) * 2, db + k * (2048 >> 4),
+                            id_in, (c_first || k != 0) ? 1u : 0u);
+          }
+          release(it++);
+          return true;
+        };
+        // carried state: output += C O(n)^T over dstate, once O(n) is in place
+        auto carried = [&]() -> bool {
+          if (!mbar_wait(&oready[yb], yph(n), spin_ns)) return false;
+          for (int hf = 0; hf < nhalf; ++hf) {
+            const uint32_t sc = stage(it);
+            if (!sc) return false;
+            tc_fence_after();
+            // 16 dstate columns per MMA: C and O (both K-major, 64-column atoms) advance 32 bytes
+            // within an atom
+            const int na = min(2, natom - 2 * hf);
+            const uint64_t da = sdesc_sw128(sc, 16, 1024), db = sdesc_sw128(ob + 2 * hf * kAtom, 16, 1024);
+#pragma unroll 1
+            for (int k = 0; k < 4 * na; ++k) {
+              const uint32_t off = (k >> 2) * (kAtom >> 4) + (k & 3) * 2;
+              mma_ss<false>(tmem + kColY + 128 * yb, da + off, db + off, id_yo,
+                            ((fast && !c_first) || hf != 0 || k != 0) ? 1u : 0u);
+            }
+            release(it++);
+          }
+          mma_commit(&cdone[yb]);
+          return true;
+        };
+        if (c_first ? !(carried() && intra()) : !(intra() && carried())) {
+          ok = false;
+          break;
+        }
+        mma_commit(&ydone[yb]);
+        if (!read_info1(n + 1, cur)) {
           ok = false;
           break;
         }
       }
     }
+  }
   } else if (warp < 8) {
+    regs_acquire<kRegState>();
     // ------------------------------------------------------------ state pass
     const int et = threadIdx.x - 128;  // TMEM lane = state row (head hd, p)
     const int quad = warp & 3;
@@ -602,27 +686,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st_wait();
         tc_fence_before();
         fence_proxy_async_smem();
-        mbar_arrive(&hready[yb]);
+        mbar_arrive(&sready[yb]);
+        mbar_arrive(&oready[yb]);
       }
-      // the pass over window n's state, h_out = mu * (pi h_in + X^T B), as soon as the state
-      // product is done (the carried product before it has released O)
+      // The pass over window n's state, h_out = mu * (pi h_in + X^T B), as soon as the state
+      // product is done.  The state for the next window goes back into tensor memory first and
+      // is handed over (sready); the bf16 copy O of the last (up to 128) columns, which only
+      // the carried product reads, is kept in registers and written after the hand-off, once
+      // the carried product of window n has read O(n).  At dstate 256 the first 128 columns
+      // write O inside the loop.
       {
-        if (named_bar_or(bar_s, 128, !mbar_wait(&dfull[yb], yph(n), spin_ns) || (!last && !o_free(n + 1)))) {
+        if (named_bar_or(bar_s, 128, !mbar_wait(&dfull[yb], yph(n), spin_ns))) {
           ok = false;
           break;
         }
         tc_fence_after();
         const float mu = fastH ? alpha : 1.f;
-        // one 32-column strip: h = mu * v, then the state and O for the next window, or the
-        // published state
-        auto strip = [&](int n0, uint32_t (&v)[32]) {
+        const int ndef0 = d.N > 128 ? d.N - 128 : 0;  // first column of the deferred O block
+        bool ofree = last;                            // O(n + 1) may be written (no O after a run's last window)
+        // one 32-column strip scaled: h = mu * v; on a run's last window, publish it
+        auto scale_publish = [&](int n0, uint32_t (&v)[32]) {
 #pragma unroll
           for (int q = 0; q < 32; ++q) v[q] = __float_as_uint(mu * __uint_as_float(v[q]));
+          if (!last) return;
           const float* hv = reinterpret_cast<const float*>(v);
-          if (!last) {
-            tmem_st32(tH + n0, v);
-            put_o(n0, v);
-          } else if (!seq_last) {  // publish for the run that continues this sequence
+          if (!seq_last) {  // for the run that continues this sequence
 #pragma unroll
             for (int q = 0; q < 8; ++q)
               __stcg(slot + ((n0 >> 5) * 8 + q) * 128, make_float4(hv[4 * q], hv[4 * q + 1], hv[4 * q + 2], hv[4 * q + 3]));
@@ -638,12 +726,47 @@ __global__ void __launch_bounds__(kThreads, 1)
         // (65,536-token sweep point L2048-N128: 512 against 530 us for one load in flight)
         uint32_t va[32], vb[32];
 #pragma unroll 1
-        for (int n0 = 0; n0 < d.N; n0 += 64) {
+        for (int n0 = 0; n0 < ndef0; n0 += 64) {  // dstate 256: columns 0..127
           tmem_ld32(tH + n0, va);
           tmem_ld32(tH + n0 + 32, vb);
           tmem_ld_wait();
-          strip(n0, va);
-          strip(n0 + 32, vb);
+          scale_publish(n0, va);
+          scale_publish(n0 + 32, vb);
+          if (!last) {
+            tmem_st32(tH + n0, va);
+            tmem_st32(tH + n0 + 32, vb);
+            if (!ofree) {
+              if (named_bar_or(bar_s, 128, !o_free(n + 1))) {
+                ok = false;
+                break;
+              }
+              ofree = true;
+            }
+            put_o(n0, va);
+            put_o(n0 + 32, vb);
+          }
+        }
+        if (!ok) break;
+        uint32_t pk[64];  // bf16 pairs of the deferred columns ndef0 .. ndef0 + 127
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          const int n0 = ndef0 + 64 * k;
+          if (n0 < d.N) {
+            tmem_ld32(tH + n0, va);
+            tmem_ld32(tH + n0 + 32, vb);
+            tmem_ld_wait();
+            scale_publish(n0, va);
+            scale_publish(n0 + 32, vb);
+            if (!last) {
+              tmem_st32(tH + n0, va);
+              tmem_st32(tH + n0 + 32, vb);
+#pragma unroll
+              for (int q = 0; q < 16; ++q) {
+                pk[32 * k + q] = pack_bf16x2(__uint_as_float(va[2 * q]), __uint_as_float(va[2 * q + 1]));
+                pk[32 * k + 16 + q] = pack_bf16x2(__uint_as_float(vb[2 * q]), __uint_as_float(vb[2 * q + 1]));
+              }
+            }
+          }
         }
         if (!last) {
           tmem_st_wait();
@@ -658,18 +781,34 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!fastH) {
 #pragma unroll 1
             for (int n0 = 0; n0 < d.N; n0 += 32) {
-              uint32_t w32[32];
-              tmem_ld32(tH + n0, w32);
+              tmem_ld32(tH + n0, va);
               tmem_ld_wait();
 #pragma unroll
-              for (int q = 0; q < 32; ++q) w32[q] = __float_as_uint(alpha * __uint_as_float(w32[q]));
-              tmem_st32(tH + n0, w32);
+              for (int q = 0; q < 32; ++q) va[q] = __float_as_uint(alpha * __uint_as_float(va[q]));
+              tmem_st32(tH + n0, va);
             }
             tmem_st_wait();
           }
           tc_fence_before();
+          mbar_arrive(&sready[(n + 1) & 1]);
+          // O(n + 1) = h_out in bf16, once the carried product of window n has read O(n)
+          if (!ofree && named_bar_or(bar_s, 128, !o_free(n + 1))) {
+            ok = false;
+            break;
+          }
+#pragma unroll
+          for (int k = 0; k < 2; ++k) {
+            const int n0 = ndef0 + 64 * k;
+            if (n0 < d.N) {
+              uint8_t* oat = orow + (n0 >> 6) * kAtom;
+#pragma unroll
+              for (int c = 0; c < 8; ++c)
+                *reinterpret_cast<uint4*>(oat + ((c ^ (et & 7)) << 4)) =
+                    make_uint4(pk[32 * k + 4 * c], pk[32 * k + 4 * c + 1], pk[32 * k + 4 * c + 2], pk[32 * k + 4 * c + 3]);
+            }
+          }
           fence_proxy_async_smem();
-          mbar_arrive(&hready[(n + 1) & 1]);
+          mbar_arrive(&oready[(n + 1) & 1]);
         } else {
           tc_fence_before();
           if (!seq_last) {
@@ -700,20 +839,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       c.b = I.b;
       c.pair = I.pair;
       c.w = I.w;
-      c.flags = I.flags;
       if (I.flags & 4) return false;
       const int t = I.w * kWin + r;
       c.dt = t < d.L ? __ldg(dtg + (static_cast<int64_t>(I.b) * d.L + t) * d.H + 2 * I.pair + hh) : 0.f;
+      c.a = __ldg(Avec + 2 * I.pair + hh);
+      c.dd = __ldg(Dvec + 2 * I.pair + hh);
       return true;
     };
     // window n's cumsum, scalars and this head's X scaled in place
     auto prepare = [&](int n, Ctx& c) -> bool {
-      const int h = 2 * c.pair + hh;
       float total;
-      const float G = wg_scan(c.dt * Avec[h], scanws + (hh * 2 + (n & 1)) * 4, bar_h, lane, quad, total);
+      const float G = wg_scan(c.dt * c.a, scanws + (hh * 2 + (n & 1)) * 4, bar_h, lane, quad, total);
       c.g = G * kLog2e;
-      c.gS = total * kLog2e;
-      c.fastH = -c.gS <= kSpan;  // G is non-increasing, so the window's decay bounds every exponent
+      const float gS = total * kLog2e;
+      c.fastH = -gS <= kSpan;  // G is non-increasing, so the window's decay bounds every exponent
       const int sb = xs(n);
       // the X buffer has landed, so window n - nxb (same buffer and scalar slot) has been
       // stored: its readers of the slot are all done
@@ -722,12 +861,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         return false;
       }
       if (et == 0) {
-        scal[sb].alpha[hh] = fast_exp2(c.gS);
+        scal[sb].alpha[hh] = fast_exp2(gS);
         scal[sb].fast[hh] = c.fastH;
       }
       // X^ (window start as reference) or X~ (window end) for this head, in place; the
       // row's eight 16-byte chunks are all loaded before any is written back
-      const float wfac = fast_exp2(c.fastH ? -c.g : c.gS - c.g) * c.dt;
+      const float wfac = fast_exp2(c.fastH ? -c.g : gS - c.g) * c.dt;
       uint4* row = reinterpret_cast<uint4*>(smem + Ls.xbuf + sb * kXBytes + hh * kWin * 128 + r * 128);
       uint4 xv[8];
 #pragma unroll
@@ -758,14 +897,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       // y = r_i * acc + D x_i, written over X^ in the X buffer (once the state product,
       // issued after the carried one, has read X^ too); warp 3 stores it
       if (named_bar_or(bar_h, 128, !mbar_wait(&xready[sb], xph(n), spin_ns) ||
-                                       !mbar_wait(&cdone[yb], yph(n), spin_ns) ||
+                                       !mbar_wait(&ydone[yb], yph(n), spin_ns) ||
                                        !mbar_wait(&dfull[yb], yph(n), spin_ns))) {
         ok = false;
         break;
       }
       tc_fence_after();
       const bool fast = scal[sb].fast[0] && scal[sb].fast[1];
-      const float Dh = Dvec[h];
+      const float Dh = cur.dd;
       uint8_t* xr = smem + Ls.xbuf + sb * kXBytes + hh * kWin * 128 + r * 128;
       const uint32_t tacc = tmem + lane_base + kColY + 128 * yb + 64 * hh;
       if (fast) {
@@ -807,7 +946,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int g = (2 * cur.pair) / (d.H / d.G);
         const __nv_bfloat16* Mrow = Mg + ((static_cast<int64_t>(cur.b) * nw + cur.w) * d.G + g) * kWin * kWin +
                                     static_cast<int64_t>(r) * kWin;
-        exact_epilogue(d, cur.b, h, t0, r, cur.g, Avec[h], Dh, Mrow, xg, dtg, tacc, xr);
+        exact_epilogue(d, cur.b, h, t0, r, cur.g, cur.a, Dh, Mrow, xg, dtg, tacc, xr);
         tc_fence_before();
         mbar_arrive(&yfree[yb]);
       }
@@ -838,18 +977,34 @@ int onepass_runs(const Dims& d, int R) {
   return ((nw + R - 1) / R) * d.B * (d.H / 2);
 }
 
-// Windows per run (the claim unit), from the shape: the longest of 16, 8 and 4
-// windows that still gives every multiprocessor at least four runs.  Longer runs
-// hand the state between CTAs less often; enough runs per CTA keep the last
-// wave short.  Measured on GB300 (bf16, dstate 128 / 64): the 2.7B layer
-// (32 windows per sequence, 160 sequences) ran 0.261 / 0.207 / 0.197 / 0.205 ms
-// with R = 2 / 4 / 8 / 16; the 65,536-token sweep points L = 2048, N = 128 and
-// L = 8192, N = 64 (G = 8) ran 0.737 / 0.592 / 0.551 / 0.539 and
-// 0.694 / 0.514 / 0.504 / 0.506 ms.
+// The schedule from the shape: claims of R windows (the longest of 16, 8 and 4 that
+// still gives every multiprocessor at least four runs; longer runs hand the state
+// between CTAs less often), unless those runs spread unevenly -- the busiest CTA more
+// than 10 % above the mean -- in which case the static split (0) runs.  Measured on
+// GB300 (bf16):
+//  - 2.7B layer (160 sequences of 32 windows): claims of 2 / 4 / 8 / 16 windows ran
+//    0.259 / 0.203 / 0.192 / 0.199 ms, and 8 windows leave some CTAs 5 runs against a
+//    mean of 4.2; the static split ran 0.166 ms.
+//  - 65,536-token sweep points with many whole sequences per CTA (L2048 and L8192 at
+//    N64-256, L512): claims ran 0.49-0.83 ms, the static split 0.46-0.97 ms (slower
+//    on all but one: per-CTA speeds differ by about 10 %, which claims absorb).
 int onepass_run_length(const Dims& d, int sms) {
-  for (int R : {16, 8})
-    if (onepass_runs(d, R) >= 4 * sms) return R;
-  return 4;
+  int R = 4;
+  for (int r : {16, 8})
+    if (onepass_runs(d, r) >= 4 * sms) {
+      R = r;
+      break;
+    }
+  const int runs = onepass_runs(d, R);
+  const int per_cta = (runs + sms - 1) / sms;  // the busiest CTA's runs
+  return static_cast<double>(per_cta) * sms > 1.1 * runs ? 0 : R;
+}
+
+// One CTA per multiprocessor; the static split takes at most one per sequence (each
+// CTA's share must hold a whole sequence's windows), claims at most one per run.
+int onepass_grid(const Dims& d, int sms, int R) {
+  const int units = R > 0 ? onepass_runs(d, R) : d.B * (d.H / 2);
+  return units < sms ? units : sms;
 }
 
 cudaError_t launch_onepass(const Dims& d, const OnePassMaps& maps, const float* dt, const float* A, const float* D,
@@ -859,12 +1014,16 @@ cudaError_t launch_onepass(const Dims& d, const OnePassMaps& maps, const float* 
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
-  const int R = onepass_run_length(d, sms);
-  const int nruns = onepass_runs(d, R);
   const size_t smem = onepass_smem_bytes(d);
   e = cudaFuncSetAttribute(ssd_onepass_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  const int grid = nruns < sms ? nruns : sms;
+  // the register split assumes the compiled count; any other count is refused here
+  cudaFuncAttributes fa{};
+  e = cudaFuncGetAttributes(&fa, ssd_onepass_kernel);
+  if (e != cudaSuccess) return e;
+  if (fa.numRegs != static_cast<int>(kRegLaunch)) return cudaErrorInvalidConfiguration;
+  const int R = onepass_run_length(d, sms);
+  const int grid = onepass_grid(d, sms, R);
   return launch_k(ssd_onepass_kernel, dim3(grid), dim3(kThreads), smem, stream, dependent, maps.x, maps.cm, maps.bm,
                   maps.m, maps.y, d, R, dt, A, D, static_cast<const __nv_bfloat16*>(w.cbm), init, final_state,
                   w.hslot, w.flags, w.counter, static_cast<const __nv_bfloat16*>(x), w.status, spin_ns);
