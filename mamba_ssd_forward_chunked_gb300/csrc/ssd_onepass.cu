@@ -68,12 +68,14 @@
 //                loads window n's X into it.
 //   warps 4-7    the state pass: thread = state row (head, p).
 //   warps 8-15   one warpgroup per head, thread = token row: the window's
-//                cumsum (warp-shuffle scan of dt*A), the X scaling (in place),
-//                and the epilogue of the window before (y written over X).
-// The control warps give registers to the state pass (setmaxnreg).  Tensor
-// memory: two output accumulators (columns [0, 256)) and the state (columns
-// [256, 256 + dstate)).  Every wait is bounded; on expiry the CTA records
-// SSD_ERR_DEVICE_TIMEOUT, waits for its own copies and exits.
+//                cumsum (warp-shuffle scan of dt*A), the X scaling (in place)
+//                with D x_i / r_i put into the output accumulator as its
+//                starting value, and the epilogue of the window before
+//                (y = r_i acc written over X).
+// The control warps give registers to the state pass and the head warpgroups
+// (setmaxnreg).  Tensor memory: two output accumulators (columns [0, 256)) and
+// the state (columns [256, 256 + dstate)).  Every wait is bounded; on expiry the
+// CTA records SSD_ERR_DEVICE_TIMEOUT, waits for its own copies and exits.
 #include "ptx.cuh"
 #include "ssd_internal.cuh"
 
@@ -89,13 +91,13 @@ constexpr uint32_t kColY = 0, kColH = 256, kTmemCols = 512;
 
 // Register split between the warpgroups (setmaxnreg): the CTA is launched with
 // kRegLaunch per thread; the control warpgroup (one active lane per warp) gives
-// registers up and the state warpgroup, which holds a window's bf16 state copy
-// across the hand-off, takes them; the head warpgroups keep the launch count.
+// registers up, the state warpgroup, which holds a window's bf16 state copy
+// across the hand-off, and the two head warpgroups take them.
 // The split must stay within the launch's pool (an increase that cannot be met
 // waits without end), which the host checks against the compiled register count
 // before every launch.
-constexpr uint32_t kRegLaunch = 128, kRegCtl = 56, kRegState = 200;
-static_assert(128 * (kRegCtl + kRegState + 2 * kRegLaunch) <= kThreads * kRegLaunch, "register split above the pool");
+constexpr uint32_t kRegLaunch = 128, kRegCtl = 48, kRegState = 176, kRegHead = 144;
+static_assert(128 * (kRegCtl + kRegState + 2 * kRegHead) <= kThreads * kRegLaunch, "register split above the pool");
 
 template <uint32_t kRegs>
 __device__ __forceinline__ void regs_release() {
@@ -566,7 +568,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
             for (int k = 0; k < kWin / 16; ++k)
               mma_ss<false>(tmem + kColY + 128 * yb, da + (k >> 2) * (kAtom >> 4) + (k & 3) * 2, db + k * (2048 >> 4),
-                            id_in, (c_first || k != 0) ? 1u : 0u);
+                            id_in, 1u);
           }
           release(it++);
           return true;
@@ -585,8 +587,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
             for (int k = 0; k < 4 * na; ++k) {
               const uint32_t off = (k >> 2) * (kAtom >> 4) + (k & 3) * 2;
-              mma_ss<false>(tmem + kColY + 128 * yb, da + off, db + off, id_yo,
-                            ((fast && !c_first) || hf != 0 || k != 0) ? 1u : 0u);
+              mma_ss<false>(tmem + kColY + 128 * yb, da + off, db + off, id_yo, (fast || hf != 0 || k != 0) ? 1u : 0u);
             }
             release(it++);
           }
@@ -820,6 +821,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else {
+    regs_acquire<kRegHead>();
     // ------------------------------------------------------------ head warpgroups: cumsum, X scaling, epilogue
     const int hh = (warp - 8) >> 2;  // head of the pair
     const int et = threadIdx.x - 256 - 128 * hh;
@@ -871,6 +873,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint4 xv[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k) xv[k] = row[k ^ (r & 7)];  // the warp's 32 rows spread over all banks
+      // The output accumulator's starting value on the rescaled form: D x_i / r_i, so that the
+      // epilogue's r_i * acc already holds D x_i (window n - 2's output in these columns was
+      // drained by this warpgroup's epilogue).  On the exact form the carried product
+      // overwrites it, and the epilogue adds D x_i itself.
+      {
+        const float sx = c.fastH ? c.dd * fast_exp2(-c.g) : 0.f;
+        const uint32_t ty = tmem + lane_base + kColY + 128 * (n & 1) + 64 * hh;
+#pragma unroll
+        for (int qt = 0; qt < 4; ++qt) {  // 16 columns at a time
+          uint32_t v[16];
+#pragma unroll
+          for (int k = 0; k < 2; ++k) {
+            const uint32_t* xw = reinterpret_cast<const uint32_t*>(&xv[2 * qt + k]);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              v[8 * k + 2 * e] = __float_as_uint(sx * bf16_lo(xw[e]));
+              v[8 * k + 2 * e + 1] = __float_as_uint(sx * bf16_hi(xw[e]));
+            }
+          }
+          tmem_st16(ty + 16 * qt, v);
+        }
+      }
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
         xv[k].x = scale_bf16x2(xv[k].x, wfac);
@@ -879,6 +903,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         xv[k].w = scale_bf16x2(xv[k].w, wfac);
         row[k ^ (r & 7)] = xv[k];
       }
+      tmem_st_wait();
+      tc_fence_before();
       fence_proxy_async_smem();
       mbar_arrive(&xready[sb]);
       return true;
@@ -914,33 +940,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld_wait();
         tc_fence_before();
         mbar_arrive(&yfree[yb]);
+        // y_i = r_i * acc: the accumulator started at D x_i / r_i (see prepare)
         const float ri = fast_exp2(cur.g);
-        const float wfac = fast_exp2(-cur.g) * cur.dt;
-        // D x_i = (r_i D / dt_i) X^_i while X^_i = wfac x_i is well inside the normal range;
-        // otherwise (rare) x_i itself is read back from global memory
-        float c = ri * Dh / cur.dt;
-        if (!(wfac >= 0x1p-80f)) {
-          c = Dh;
-          const bool in_seq = t0 + r < d.L;
-          const uint4* xi =
-              reinterpret_cast<const uint4*>(xg + ((static_cast<int64_t>(cur.b) * d.L + t0 + r) * d.H + h) * d.P);
-#pragma unroll 1
-          for (int k = 0; k < 8; ++k)
-            *reinterpret_cast<uint4*>(xr + ((k ^ (r & 7)) << 4)) = in_seq ? __ldg(xi + k) : make_uint4(0, 0, 0, 0);
-        }
-        uint4 xv[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) xv[k] = *reinterpret_cast<const uint4*>(xr + ((k ^ (r & 7)) << 4));
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-          uint32_t* vw = reinterpret_cast<uint32_t*>(&xv[k]);
+          uint4 v;
+          uint32_t* vw = reinterpret_cast<uint32_t*>(&v);
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int pi = 8 * k + 2 * e;
-            vw[e] = pack_bf16x2(fmaf(c, bf16_lo(vw[e]), ri * __uint_as_float(ya[pi])),
-                                fmaf(c, bf16_hi(vw[e]), ri * __uint_as_float(ya[pi + 1])));
+            vw[e] = pack_bf16x2(ri * __uint_as_float(ya[pi]), ri * __uint_as_float(ya[pi + 1]));
           }
-          *reinterpret_cast<uint4*>(xr + ((k ^ (r & 7)) << 4)) = xv[k];
+          *reinterpret_cast<uint4*>(xr + ((k ^ (r & 7)) << 4)) = v;
         }
       } else {
         const int g = (2 * cur.pair) / (d.H / d.G);
