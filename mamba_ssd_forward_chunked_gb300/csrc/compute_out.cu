@@ -36,8 +36,11 @@
 // two rings, in the order the MMA warp consumes them: per column block, the
 // dstate slices of {C, B, the two entering states} (48 KB stages) and the two
 // heads' X blocks (a ring of its own, so X blocks are fetched up to two column
-// blocks ahead); the next tile's loads stream in while this one computes.  Warp 1 owns tensor memory and issues every MMA from one thread.
-// Warps 2-5 and 6-9 are two warpgroups, one per head of the pair: each scales
+// blocks ahead); the next tile's loads stream in while this one computes.  Warp 1
+// owns tensor memory and issues every MMA from one thread; warps 2-3 only fill
+// the control warpgroup, which gives its registers to the head warpgroups
+// (setmaxnreg: the TF32 head code spilled at the launch count).
+// Warps 4-7 and 8-11 are two warpgroups, one per head of the pair: each scales
 // its carried-state accumulator, builds its masked matrix from the shared CB,
 // and writes its head's output rows, so the two heads' elementwise work runs
 // side by side.  A warpgroup loads the next tile's per-column data into
@@ -67,12 +70,27 @@ struct OutCfg {
   static constexpr int kXBytes = kTF32 ? 32768 : 16384;                            // X stage: 128 tokens x 64 p
   static constexpr int kXStages = kTF32 ? 2 : 4;                                   // X ring
   static constexpr int kKStepX = kTF32 ? 8 : 16;                                   // tokens per intra MMA
-  static constexpr int kThreads = 320;
+  static constexpr int kThreads = 384;
   static constexpr uint32_t kColCB = 0, kColM0 = 128, kColY0 = 384, kTmemCols = 512;
   static constexpr int kWgFloats = 3 * 256;  // per warpgroup: cumsum, dt, strip factors for 256 columns
 };
 
 constexpr float kSpan = 100.f;  // rescaled form: log2 bound on the diagonal block's decay
+
+// Register split (setmaxnreg): 384 threads launch with kRegLaunch each (12 warps, three per
+// sub-partition); the control warpgroup (TMA and MMA warps, two idle) gives registers up and
+// the two head warpgroups take them.  The split must stay within the launch's pool (an
+// increase that cannot be met waits without end); the host checks the compiled count.
+constexpr uint32_t kRegLaunch = 168, kRegCtl = 88, kRegHead = 200;
+static_assert(128 * (kRegCtl + 2 * kRegHead) <= 384 * kRegLaunch, "register split above the pool");
+template <uint32_t kRegs>
+__device__ __forceinline__ void regs_release() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
+template <uint32_t kRegs>
+__device__ __forceinline__ void regs_acquire() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
 
 // Rescaled operands are clamped to finite values: an overflowing product must
 // not become inf, which the causal select's zeros would turn into NaN in rows
@@ -255,6 +273,8 @@ __global__ void __launch_bounds__(OutCfg<T>::kThreads, 1)
   const uint32_t tmem = *tmem_holder;
   bool ok = true;
 
+  if (warp < 4) {
+  regs_release<kRegCtl>();
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
@@ -368,10 +388,12 @@ __global__ void __launch_bounds__(OutCfg<T>::kThreads, 1)
         if (ok) mma_commit(yfull);
       }
     }
+  }
   } else {
+    regs_acquire<kRegHead>();
     // ------------------------------------------------------------ one warpgroup per head
-    const int hh = (warp - 2) >> 2;
-    const int et = threadIdx.x - 64 - 128 * hh;  // 0..127
+    const int hh = (warp - 4) >> 2;
+    const int et = threadIdx.x - 128 - 128 * hh;  // 0..127
     const uint32_t bar_id = 1 + hh;
     float* gs = reinterpret_cast<float*>(smem + L.wg) + hh * C::kWgFloats;  // cumsum in log2 units
     float* dts = gs + 256;
@@ -697,6 +719,11 @@ cudaError_t launch_impl(const Dims& d, const ComputeOutMaps& maps, const float* 
     cudaError_t e = cudaFuncSetAttribute(compute_out_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
+    // the register split assumes the compiled count; any other count is refused here
+    cudaFuncAttributes fa{};
+    e = cudaFuncGetAttributes(&fa, compute_out_kernel<T>);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs != static_cast<int>(kRegLaunch)) return cudaErrorInvalidConfiguration;
     configured = true;
   }
   const int ntile = d.Q >= 128 ? d.Q / 128 : 1;
