@@ -99,6 +99,12 @@ constexpr uint32_t kColY = 0, kColH = 256, kTmemCols = 512;
 constexpr uint32_t kRegLaunch = 128, kRegCtl = 48, kRegState = 176, kRegHead = 144;
 static_assert(128 * (kRegCtl + kRegState + 2 * kRegHead) <= kThreads * kRegLaunch, "register split above the pool");
 
+// Asynchronous prefetch of a contiguous global range into L2 (16-byte aligned, size a
+// multiple of 16).
+__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 template <uint32_t kRegs>
 __device__ __forceinline__ void regs_release() {
   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegs));
@@ -371,6 +377,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       // windows [w0, w1) of sequence (b, pair) into the ring; flags bit 0 / 1 = first / last
       // of the run, bit 2 = end marker
       auto put = [&](int b, int pair, int w0, int w1, int fl) {
+        // a sequence's first window starts from init_state: bring the pair's block into L2
+        // now, while the window waits in the ring behind the ones before it
+        if (w0 == 0 && fl == 0 && init)
+          prefetch_l2_bulk(init + (static_cast<int64_t>(b) * d.H + 2 * pair) * d.P * d.N,
+                           static_cast<uint32_t>(2 * d.P * d.N * sizeof(float)));
         for (int w = w0; good && w < w1; ++w, ++n) {
           const int ts = n % kInfoRing;
           if (n >= kInfoRing && !mbar_wait(&tempty[ts], ((n / kInfoRing) - 1) & 1, spin_ns)) {
@@ -662,26 +673,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         fastH = scal[xs(n)].fast[hd] != 0;
         const float* hin = seq_first ? (init ? init + hrow : nullptr) : nullptr;
         const float pre = fastH ? 1.f : alpha;
+        // The entering state: the predecessor's slot ([16-column group][row] float4s),
+        // init_state (the row's columns in order, prefetched into L2 when the schedule
+        // published the run) or zero.  A rolled loop over 64 columns: 16 loads in flight per
+        // L2 round trip, and little code, since this path runs once per run and its code is
+        // never in the instruction cache.
+        const bool zero = seq_first && !hin;
+        const float4* src0 = seq_first ? reinterpret_cast<const float4*>(hin) : slot;
+        const int step = seq_first ? 8 : 8 * 128, stride = seq_first ? 1 : 128;
 #pragma unroll 1
-        for (int n0 = 0; n0 < d.N; n0 += 64) {  // two strips' loads in flight
-          float hv[64];
+        for (int n0 = 0; n0 < d.N; n0 += 64) {
+          uint32_t hb[64];
+          if (zero) {
 #pragma unroll
-          for (int q = 0; q < 16; ++q) {
-            const float4 h4 = !seq_first ? __ldcg(slot + ((n0 >> 5) * 8 + q) * 128)
-                              : hin      ? __ldcg(reinterpret_cast<const float4*>(hin + n0) + q)
-                                         : make_float4(0.f, 0.f, 0.f, 0.f);
-            hv[4 * q] = h4.x;
-            hv[4 * q + 1] = h4.y;
-            hv[4 * q + 2] = h4.z;
-            hv[4 * q + 3] = h4.w;
+            for (int q = 0; q < 64; ++q) hb[q] = 0u;
+          } else {
+#pragma unroll
+            for (int q = 0; q < 16; ++q) {
+              const float4 h4 = __ldcg(src0 + (n0 >> 5) * step + (q >> 3) * step + (q & 7) * stride);
+              hb[4 * q] = __float_as_uint(h4.x);
+              hb[4 * q + 1] = __float_as_uint(h4.y);
+              hb[4 * q + 2] = __float_as_uint(h4.z);
+              hb[4 * q + 3] = __float_as_uint(h4.w);
+            }
           }
 #pragma unroll
           for (int half = 0; half < 2; ++half) {
-            uint32_t* hb = reinterpret_cast<uint32_t*>(hv + 32 * half);
-            put_o(n0 + 32 * half, hb);  // O = h_in
+            uint32_t* hh = hb + 32 * half;
+            put_o(n0 + 32 * half, hh);  // O = h_in
 #pragma unroll
-            for (int q = 0; q < 32; ++q) hv[32 * half + q] *= pre;
-            tmem_st32(tH + n0 + 32 * half, *reinterpret_cast<uint32_t(*)[32]>(hb));
+            for (int q = 0; q < 32; ++q) hh[q] = __float_as_uint(pre * __uint_as_float(hh[q]));
+            tmem_st32(tH + n0 + 32 * half, *reinterpret_cast<uint32_t(*)[32]>(hh));
           }
         }
         tmem_st_wait();
