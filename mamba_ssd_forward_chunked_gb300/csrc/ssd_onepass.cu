@@ -932,12 +932,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       return true;
     };
 
-    Ctx cur, nxt, nn;
+    // Per iteration: the epilogue of window n, then window n + 2's cumsum and X scaling (its
+    // output accumulator is the one the epilogue just drained), so that a window's scaled X and
+    // scalars are ready a window before the state pass of the window ahead of it asks for them.
+    Ctx cur, nxt, nn, n3;
     bool more = fetch(0, cur) && prepare(0, cur);
-    bool more1 = more && fetch(1, nxt);
+    bool more1 = more && fetch(1, nxt) && prepare(1, nxt);
+    bool more2 = more1 && fetch(2, nn);
     for (int n = 0; ok && more; ++n) {
-      if (more1 && !prepare(n + 1, nxt)) break;
-      const bool more2 = more1 && fetch(n + 2, nn);
       if (!ok) break;
       const int yb = n & 1, sb = xs(n);
       const int h = 2 * cur.pair + hh;
@@ -985,10 +987,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       fence_proxy_async_smem();
       mbar_arrive(&ystaged[sb]);
+      if (more2 && !prepare(n + 2, nn)) break;
+      const bool more3 = more2 && fetch(n + 3, n3);
+      if (!ok) break;
       cur = nxt;
       nxt = nn;
+      nn = n3;
       more = more1;
       more1 = more2;
+      more2 = more3;
     }
   }
 
