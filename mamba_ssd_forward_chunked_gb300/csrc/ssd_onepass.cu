@@ -324,7 +324,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(tmem_holder, kTmemCols);
     tmem_relinquish();
   }
-  grid_dep_wait();  // causal_cb's operand, cleared counter and flags are visible from here on
+  // No griddepcontrol.wait here: what the pre-pass writes (the causal blocks, the cleared
+  // status word, counter and flags) is waited for by each role just before its first use, so
+  // the first X windows and init_state prefetches go out while the pre-pass finishes.
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -398,6 +400,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       };
       if (R > 0) {
+        grid_dep_wait();  // the counter is cleared by the pre-pass
         const int nruns = ((nw + R - 1) / R) * d.B * hp;
         for (;;) {
           const int run = atomicAdd(counter, 1);
@@ -496,6 +499,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint8_t* st = smem + Ls.ring + s * kStage;
           const int qm = d.N > 128 ? 2 * nhalf : nhalf;  // M after C at dstate 256, before it otherwise
           if (q == qm) {
+            if (n == 0) grid_dep_wait();  // the causal blocks come from the pre-pass
             mbar_arrive_expect_tx(&full[s], 2 * kAtom);
             const int row = ((I.b * nw + I.w) * d.G + g) * kWin;
             tma_load_2d(st, &mmap, &full[s], 0, row);
@@ -619,6 +623,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   } else if (warp < 8) {
     regs_acquire<kRegState>();
+    grid_dep_wait();  // the flags are cleared by the pre-pass
     // ------------------------------------------------------------ state pass
     const int et = threadIdx.x - 128;  // TMEM lane = state row (head hd, p)
     const int quad = warp & 3;
@@ -981,6 +986,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int g = (2 * cur.pair) / (d.H / d.G);
         const __nv_bfloat16* Mrow = Mg + ((static_cast<int64_t>(cur.b) * nw + cur.w) * d.G + g) * kWin * kWin +
                                     static_cast<int64_t>(r) * kWin;
+        grid_dep_wait();  // the causal blocks come from the pre-pass
         exact_epilogue(d, cur.b, h, t0, r, cur.g, cur.a, Dh, Mrow, xg, dtg, tacc, xr);
         tc_fence_before();
         mbar_arrive(&yfree[yb]);
@@ -999,7 +1005,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
-  if (!ok) atomicExch(status, static_cast<int>(SSD_ERR_DEVICE_TIMEOUT));
+  if (!ok) {
+    grid_dep_wait();  // the status word is cleared by the pre-pass
+    atomicExch(status, static_cast<int>(SSD_ERR_DEVICE_TIMEOUT));
+  }
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
