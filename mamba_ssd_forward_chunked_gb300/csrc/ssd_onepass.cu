@@ -337,7 +337,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto read_info = [&](int n, WinInfo& I) -> bool {
     const int ts = n % kInfoRing;
     bool good = true;
-    if (lane == 0) good = mbar_wait(&tfull[ts], (n / kInfoRing) & 1, spin_ns);
+    if (lane == 0) good = mbar_wait_short(&tfull[ts], (n / kInfoRing) & 1, spin_ns);
     good = __shfl_sync(0xffffffffu, good ? 1 : 0, 0) != 0;
     if (!good) return false;
     I = info[ts];
@@ -348,7 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // the same, for a warp of which only lane 0 runs
   auto read_info1 = [&](int n, WinInfo& I) -> bool {
     const int ts = n % kInfoRing;
-    if (!mbar_wait(&tfull[ts], (n / kInfoRing) & 1, spin_ns)) return false;
+    if (!mbar_wait_short(&tfull[ts], (n / kInfoRing) & 1, spin_ns)) return false;
     I = info[ts];
     mbar_arrive(&tempty[ts]);
     return true;
@@ -386,7 +386,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                            static_cast<uint32_t>(2 * d.P * d.N * sizeof(float)));
         for (int w = w0; good && w < w1; ++w, ++n) {
           const int ts = n % kInfoRing;
-          if (n >= kInfoRing && !mbar_wait(&tempty[ts], ((n / kInfoRing) - 1) & 1, spin_ns)) {
+          if (n >= kInfoRing && !mbar_wait_short(&tempty[ts], ((n / kInfoRing) - 1) & 1, spin_ns)) {
             good = false;
             break;
           }
@@ -435,7 +435,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int hb[3] = {0, 0, 0}, ht[3] = {0, 0, 0}, hh0[3] = {0, 0, 0};  // batch, t0, h0 of each buffer's window
       auto store = [&](int k) -> bool {  // window k's y, written over its X
         const int sb = xs(k);
-        if (!mbar_wait(&ystaged[sb], xph(k), spin_ns)) return false;
+        if (!mbar_wait_short(&ystaged[sb], xph(k), spin_ns)) return false;
         uint8_t* xb = smem + Ls.xbuf + sb * kXBytes;
         tma_store_3d(&ymap, xb, hh0[sb] * d.P, ht[sb], hb[sb]);
         tma_store_3d(&ymap, xb + kWin * 128, (hh0[sb] + 1) * d.P, ht[sb], hb[sb]);
@@ -472,7 +472,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_store_wait_all();
       // on a timeout: wait (bounded) for the X copies still in flight before the CTA exits
       if (!ok)
-        for (int k = max(0, n - nxb); k <= n; ++k) mbar_wait(&xfull[xs(k)], xph(k), spin_ns);
+        for (int k = max(0, n - nxb); k <= n; ++k) mbar_wait_short(&xfull[xs(k)], xph(k), spin_ns);
     }
   } else if (warp == 0) {
     // ------------------------------------------------------------ TMA producer: the ring
@@ -492,7 +492,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int nitems = 1 + 2 * nhalf;
         for (int q = 0; q < nitems && ok; ++q, ++it) {
           const int s = it % Ls.stages, rnd = it / Ls.stages;
-          if (rnd > 0 && !mbar_wait(&empty[s], (rnd - 1) & 1, spin_ns)) {
+          if (rnd > 0 && !mbar_wait_short(&empty[s], (rnd - 1) & 1, spin_ns)) {
             ok = false;
             break;
           }
@@ -516,7 +516,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // on a timeout: wait (bounded) for the copies still in flight before the CTA exits
       if (!ok)
-        for (int k = max(0, it - Ls.stages); k < it; ++k) mbar_wait(&full[k % Ls.stages], (k / Ls.stages) & 1, spin_ns);
+        for (int k = max(0, it - Ls.stages); k < it; ++k) mbar_wait_short(&full[k % Ls.stages], (k / Ls.stages) & 1, spin_ns);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -533,7 +533,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int it = 0;
       auto stage = [&](int i) -> uint32_t {
         const int s = i % Ls.stages;
-        if (!mbar_wait(&full[s], (i / Ls.stages) & 1, spin_ns)) return 0u;
+        if (!mbar_wait_short(&full[s], (i / Ls.stages) & 1, spin_ns)) return 0u;
         return smem_u32(smem + Ls.ring + s * kStage);
       };
       auto release = [&](int i) { mma_commit(&empty[i % Ls.stages]); };
@@ -542,7 +542,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int n = 0; ok && !(cur.flags & 4); ++n) {
         const int yb = n & 1;
         // S(n): accumulate X^^T B onto the state once pi h_in is in place and X^ is scaled
-        if (!mbar_wait(&sready[yb], yph(n), spin_ns) || !mbar_wait(&xready[xs(n)], xph(n), spin_ns)) {
+        if (!mbar_wait_short(&sready[yb], yph(n), spin_ns) || !mbar_wait_short(&xready[xs(n)], xph(n), spin_ns)) {
           ok = false;
           break;
         }
@@ -568,7 +568,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // output is drained.  Up to dstate 128 the intra product goes first; at dstate 256 the
         // carried product does, so that O(n) is free early: the pass writes O for the first
         // 128 columns before it hands the state over.
-        if (n >= 2 && !mbar_wait(&yfree[yb], yph(n - 2), spin_ns)) {
+        if (n >= 2 && !mbar_wait_short(&yfree[yb], yph(n - 2), spin_ns)) {
           ok = false;
           break;
         }
@@ -590,7 +590,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         };
         // carried state: output += C O(n)^T over dstate, once O(n) is in place
         auto carried = [&]() -> bool {
-          if (!mbar_wait(&oready[yb], yph(n), spin_ns)) return false;
+          if (!mbar_wait_short(&oready[yb], yph(n), spin_ns)) return false;
           for (int hf = 0; hf < nhalf; ++hf) {
             const uint32_t sc = stage(it);
             if (!sc) return false;
@@ -648,7 +648,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     };
     // before writing O for window m: the carried product of window m - 1 is done
-    auto o_free = [&](int m) -> bool { return m < 1 || mbar_wait(&cdone[(m - 1) & 1], yph(m - 1), spin_ns); };
+    auto o_free = [&](int m) -> bool { return m < 1 || mbar_wait_short(&cdone[(m - 1) & 1], yph(m - 1), spin_ns); };
     // the window's scalars: alpha = e^{G_S} and the rescaled-form flag of this head
     float alpha = 1.f;
     bool fastH = true;
@@ -668,7 +668,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (first) {
         // the state entering the run: predecessor's slot, init_state or zero, put in place
         // as pi * h_in with O = h_in
-        bool bad = !mbar_wait(&xready[xs(n)], xph(n), spin_ns) || !o_free(n);
+        bool bad = !mbar_wait_short(&xready[xs(n)], xph(n), spin_ns) || !o_free(n);
         if (!seq_first && et == 0) bad = bad || !wait_flag_geq(flags + I.b * hp + I.pair, I.w, spin_ns);
         if (named_bar_or(bar_s, 128, bad)) {
           ok = false;
@@ -724,7 +724,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the carried product of window n has read O(n).  At dstate 256 the first 128 columns
       // write O inside the loop.
       {
-        if (named_bar_or(bar_s, 128, !mbar_wait(&dfull[yb], yph(n), spin_ns))) {
+        if (named_bar_or(bar_s, 128, !mbar_wait_short(&dfull[yb], yph(n), spin_ns))) {
           ok = false;
           break;
         }
@@ -800,7 +800,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_st_wait();
           // the next window's scalars (its X scaled); on the exact form the state it
           // accumulates onto is e^{G_S} h_in, so rescale (rare)
-          if (named_bar_or(bar_s, 128, !mbar_wait(&xready[xs(n + 1)], xph(n + 1), spin_ns))) {
+          if (named_bar_or(bar_s, 128, !mbar_wait_short(&xready[xs(n + 1)], xph(n + 1), spin_ns))) {
             ok = false;
             break;
           }
@@ -885,7 +885,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int sb = xs(n);
       // the X buffer has landed, so window n - nxb (same buffer and scalar slot) has been
       // stored: its readers of the slot are all done
-      if (named_bar_or(bar_h, 128, !mbar_wait(&xfull[sb], xph(n), spin_ns))) {
+      if (named_bar_or(bar_h, 128, !mbar_wait_short(&xfull[sb], xph(n), spin_ns))) {
         ok = false;
         return false;
       }
@@ -951,9 +951,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int t0 = cur.w * kWin;
       // y = r_i * acc + D x_i, written over X^ in the X buffer (once the state product,
       // issued after the carried one, has read X^ too); warp 3 stores it
-      if (named_bar_or(bar_h, 128, !mbar_wait(&xready[sb], xph(n), spin_ns) ||
-                                       !mbar_wait(&ydone[yb], yph(n), spin_ns) ||
-                                       !mbar_wait(&dfull[yb], yph(n), spin_ns))) {
+      if (named_bar_or(bar_h, 128, !mbar_wait_short(&xready[sb], xph(n), spin_ns) ||
+                                       !mbar_wait_short(&ydone[yb], yph(n), spin_ns) ||
+                                       !mbar_wait_short(&dfull[yb], yph(n), spin_ns))) {
         ok = false;
         break;
       }
