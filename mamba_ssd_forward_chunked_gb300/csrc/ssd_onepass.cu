@@ -32,17 +32,24 @@
 // and the epilogue sums (c_i . b_j) e^{G_i - G_j} dt_j x_j on CUDA cores with
 // one exponential per element (exponent <= 0).
 //
-// The state on the tensor core.  The running state of the pair lives in tensor
-// memory as an fp32 accumulator with lane = (head, p) and columns = dstate.
-// Before a window's state product it holds pi * h_in (pi = 1 on the rescaled
-// form, e^{G_S} on the exact one), the product X^^T B (resp. X~^T B) is
-// accumulated onto it, and the state pass that follows reads it back, scales
-// it by mu (e^{G_S}, resp. 1) to get h_out, writes pi' * h_out back for the
-// next window and hands it over; only then does it write the bf16 copy O of
-// h_out that the next window's carried-state product reads.  So the serial
-// chain between windows is one state product and the tensor-memory half of one
-// pass over the state; the intra and carried-state products, the O writes and
-// the rest of a window overlap it.
+// The state.  Thread (head, p) of the state pass owns row (head, p) of the
+// pair's running state, and the window's state product X^^T B (resp. X~^T B)
+// comes from the tensor core with lane = (head, p) and columns = dstate.
+//  - dstate <= 128 (product buffers): the row lives in the thread's registers
+//    (fp32).  S(n) writes the window's product fresh into tensor-memory buffer
+//    n % 2; the pass reads it, h_out = e^{G_S} (h_in + X^^T B) (resp.
+//    e^{G_S} h_in + X~^T B), frees the buffer and writes the bf16 copy O of
+//    h_out that the next window's carried-state product reads.  S(n + 1) waits
+//    for nothing of the pass of window n, so the only hand-off between windows
+//    is O.
+//  - dstate 256 (state in tensor memory): the row does not fit in registers,
+//    so the state is an fp32 accumulator in tensor memory.  Before a window's
+//    state product it holds pi * h_in (pi = 1 on the rescaled form, e^{G_S} on
+//    the exact one), the product is accumulated onto it, and the pass reads it
+//    back, scales it by mu (e^{G_S}, resp. 1) to get h_out, writes pi' * h_out
+//    back and hands it over; only then does it write O.  The serial chain
+//    between windows is one state product and the tensor-memory half of one
+//    pass.
 //
 // Runs and chaining.  Windows go out in runs (consecutive windows of one
 // sequence, i.e. one (batch, head pair)), either claimed from a global counter
@@ -58,11 +65,12 @@
 //                the tensor core uses them, B, M (the causal operand) and C
 //                (C before M at dstate 256).
 //   warp 1       owns tensor memory and issues every tcgen05.mma from one
-//                thread, per window n: the state product S(n) once the state
-//                is handed over, then the intra product M X^ and, once O(n) is
-//                written, the carried product C O(n)^T (at dstate 256 the
-//                carried product first, since the pass writes O for the first
-//                128 columns before the hand-off).
+//                thread, per window n: the state product S(n) once X^ is
+//                scaled (and its product buffer read, resp. the state handed
+//                over), then the intra product M X^ and, once O(n) is written,
+//                the carried product C O(n)^T (at dstate 256 the carried
+//                product first, since the pass writes O for the first 128
+//                columns before the hand-off).
 //   warp 3       TMA for the head pair's X window (three buffers; two at
 //                dstate 256): stores window n - 3's y out of a buffer, then
 //                loads window n's X into it.
@@ -74,7 +82,8 @@
 //                (y = r_i acc written over X).
 // The control warps give registers to the state pass and the head warpgroups
 // (setmaxnreg).  Tensor memory: two output accumulators (columns [0, 256)) and
-// the state (columns [256, 256 + dstate)).  Every wait is bounded; on expiry the
+// two product buffers of 128 columns, resp. the state (columns [256, 512)).
+// The kernel is compiled per dstate (64, 128, 256).  Every wait is bounded; on expiry the
 // CTA records SSD_ERR_DEVICE_TIMEOUT, waits for its own copies and exits.
 #include "ptx.cuh"
 #include "ssd_internal.cuh"
@@ -91,8 +100,9 @@ constexpr uint32_t kColY = 0, kColH = 256, kTmemCols = 512;
 
 // Register split between the warpgroups (setmaxnreg): the CTA is launched with
 // kRegLaunch per thread; the control warpgroup (one active lane per warp) gives
-// registers up, the state warpgroup, which holds a window's bf16 state copy
-// across the hand-off, and the two head warpgroups take them.
+// registers up, the state warpgroup, which holds the running state row (dstate
+// <= 128) or a window's bf16 state copy across the hand-off (dstate 256), and
+// the two head warpgroups take them.
 // The split must stay within the launch's pool (an increase that cannot be met
 // waits without end), which the host checks against the compiled register count
 // before every launch.
@@ -251,6 +261,7 @@ struct Ctx {
   int fastH; // rescaled form valid for this head
 };
 
+template <int kN>
 __global__ void __launch_bounds__(kThreads, 1)
     ssd_onepass_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap cmap,
                        const __grid_constant__ CUtensorMap bmap, const __grid_constant__ CUtensorMap mmap,
@@ -259,6 +270,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                        const __nv_bfloat16* __restrict__ Mg, const float* init, float* final_state, float* hslot,
                        int* flags, int* counter, const __nv_bfloat16* __restrict__ xg, int* status,
                        uint64_t spin_ns) {
+  constexpr bool kPB = kN <= 128;  // product buffers (else the state accumulated in tensor memory)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const OPSmem Ls = op_layout(d.N);
@@ -279,7 +291,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* ystaged = bars + 12;  // [3] y written into the X buffer (256: both head warpgroups)
   uint64_t* tfull = bars + 15;    // [8] window ring
   uint64_t* tempty = bars + 23;   // [8] (15 warps read each entry)
-  uint64_t* sready = bars + 31;   // [2] state (pi h_in) of the window in place (128)
+  // [2] state in tensor memory: pi h_in of the window in place; product buffers: the pass has
+  // read the window's product, so its buffer is free (128)
+  uint64_t* sready = bars + 31;
   uint64_t* dfull = bars + 33;    // [2] state product done (X^ of the window read)
   uint64_t* cdone = bars + 35;    // [2] carried-state product done: O free, output complete
   uint64_t* yfree = bars + 37;    // [2] output accumulator drained (256)
@@ -541,8 +555,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!read_info1(0, cur)) ok = false;
       for (int n = 0; ok && !(cur.flags & 4); ++n) {
         const int yb = n & 1;
-        // S(n): accumulate X^^T B onto the state once pi h_in is in place and X^ is scaled
-        if (!mbar_wait_short(&sready[yb], yph(n), spin_ns) || !mbar_wait_short(&xready[xs(n)], xph(n), spin_ns)) {
+        // S(n) once X^ is scaled: accumulated onto the state once pi h_in is in place (state in
+        // tensor memory), or into product buffer n % 2 once the pass has read window n - 2's
+        // product from it (product buffers)
+        if (!(kPB ? n < 2 || mbar_wait_short(&sready[yb], yph(n - 2), spin_ns)
+                  : mbar_wait_short(&sready[yb], yph(n), spin_ns)) ||
+            !mbar_wait_short(&xready[xs(n)], xph(n), spin_ns)) {
           ok = false;
           break;
         }
@@ -557,9 +575,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           // 16 tokens per MMA: both MN-major operands advance by 16 rows (2048 bytes)
           const uint64_t da = sdesc_sw128(xb, xlbo, 1024), db = sdesc_sw128(sb, kAtom, 1024);
+          const uint32_t dst = tmem + kColH + 128 * (kPB ? yb : hf);
 #pragma unroll 1
           for (int k = 0; k < kWin / 16; ++k)
-            mma_ss<false>(tmem + kColH + 128 * hf, da + k * (2048 >> 4), db + k * (2048 >> 4), id_st, 1u);
+            mma_ss<false>(dst, da + k * (2048 >> 4), db + k * (2048 >> 4), id_st, (kPB && k == 0) ? 0u : 1u);
           release(it++);
         }
         if (!ok) break;
@@ -652,6 +671,125 @@ __global__ void __launch_bounds__(kThreads, 1)
     // the window's scalars: alpha = e^{G_S} and the rescaled-form flag of this head
     float alpha = 1.f;
     bool fastH = true;
+    if constexpr (kPB) {
+    // Product buffers (dstate <= 128).  The running state row h (head, p) stays in registers;
+    // S(n) writes X^^T B (X~^T B) fresh into tensor-memory buffer n % 2, and the pass adds it:
+    //   h_out = e^{G_S} (h_in + X^^T B)   (rescaled form),   e^{G_S} h_in + X~^T B   (exact).
+    // The pass frees the buffer as soon as it has read it, so S(n + 1) never waits for the pass
+    // of window n: the only hand-off left between windows is O, the bf16 copy of h that the
+    // next window's carried product reads.
+    float hs[kN];
+    // O = h in bf16 for the columns [0, N)
+    auto put_all_o = [&]() {
+#pragma unroll
+      for (int c = 0; c < kN / 8; ++c) {  // 16-byte chunk c: columns 8c .. 8c + 7
+        uint4 o;
+        o.x = pack_bf16x2(hs[8 * c], hs[8 * c + 1]);
+        o.y = pack_bf16x2(hs[8 * c + 2], hs[8 * c + 3]);
+        o.z = pack_bf16x2(hs[8 * c + 4], hs[8 * c + 5]);
+        o.w = pack_bf16x2(hs[8 * c + 6], hs[8 * c + 7]);
+        *reinterpret_cast<uint4*>(orow + (c >> 3) * kAtom + (((c & 7) ^ (et & 7)) << 4)) = o;
+      }
+    };
+    for (int n = 0; ok; ++n) {
+      WinInfo I;
+      if (named_bar_or(bar_s, 128, !read_info(n, I))) {
+        ok = false;
+        break;
+      }
+      if (I.flags & 4) break;
+      const int yb = n & 1;
+      const bool first = I.flags & 1, last = I.flags & 2;
+      const int h = 2 * I.pair + hd;
+      const int64_t hrow = ((static_cast<int64_t>(I.b) * d.H + h) * d.P + p) * d.N;  // [B][H][P][N]
+      float4* slot = reinterpret_cast<float4*>(hslot + (static_cast<int64_t>(I.b) * hp + I.pair) * 128 * d.N) + et;
+      const bool seq_first = I.w == 0, seq_last = I.w == nw - 1;
+      if (first) {
+        // the state entering the run: the predecessor's slot (float4 k of the row at
+        // slot[k * 128]), init_state (prefetched into L2 when the run was published) or zero;
+        // O = h_in
+        bool bad = !mbar_wait_short(&xready[xs(n)], xph(n), spin_ns) || !o_free(n);
+        if (!seq_first && et == 0) bad = bad || !wait_flag_geq(flags + I.b * hp + I.pair, I.w, spin_ns);
+        if (named_bar_or(bar_s, 128, bad)) {
+          ok = false;
+          break;
+        }
+        alpha = scal[xs(n)].alpha[hd];
+        fastH = scal[xs(n)].fast[hd] != 0;
+        const float* hin = seq_first ? (init ? init + hrow : nullptr) : nullptr;
+        if (seq_first && !hin) {
+#pragma unroll
+          for (int q = 0; q < kN; ++q) hs[q] = 0.f;
+        } else {
+          const float4* src0 = seq_first ? reinterpret_cast<const float4*>(hin) : slot;
+          const int stride = seq_first ? 1 : 128;
+#pragma unroll
+          for (int k = 0; k < kN / 4; ++k) {
+            const float4 h4 = __ldcg(src0 + k * stride);
+            hs[4 * k] = h4.x;
+            hs[4 * k + 1] = h4.y;
+            hs[4 * k + 2] = h4.z;
+            hs[4 * k + 3] = h4.w;
+          }
+        }
+        put_all_o();
+        fence_proxy_async_smem();
+        mbar_arrive(&oready[yb]);
+      }
+      // the pass: h_out from h_in and window n's product, in 32-column strips
+      if (named_bar_or(bar_s, 128, !mbar_wait_short(&dfull[yb], yph(n), spin_ns))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      {
+        const float beta = fastH ? alpha : 1.f;
+        const uint32_t tP = tmem + lane_base + kColH + 128 * yb;
+#pragma unroll
+        for (int n0 = 0; n0 < kN; n0 += 32) {  // two 16-column loads in flight
+          uint32_t v[16], u[16];
+          tmem_ld16(tP + n0, v);
+          tmem_ld16(tP + n0 + 16, u);
+          tmem_ld_wait();
+#pragma unroll
+          for (int q = 0; q < 16; ++q) hs[n0 + q] = fmaf(alpha, hs[n0 + q], beta * __uint_as_float(v[q]));
+#pragma unroll
+          for (int q = 0; q < 16; ++q) hs[n0 + 16 + q] = fmaf(alpha, hs[n0 + 16 + q], beta * __uint_as_float(u[q]));
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&sready[yb]);
+      if (last) {
+        // publish: the slot for the run that continues this sequence, or final_state
+        if (!seq_last) {
+#pragma unroll
+          for (int k = 0; k < kN / 4; ++k)
+            __stcg(slot + k * 128, make_float4(hs[4 * k], hs[4 * k + 1], hs[4 * k + 2], hs[4 * k + 3]));
+          __threadfence();
+          named_bar_sync(bar_s, 128);
+          if (et == 0) st_release_gpu(flags + I.b * hp + I.pair, I.w + 1);
+        } else if (final_state) {
+#pragma unroll
+          for (int k = 0; k < kN / 4; ++k)
+            reinterpret_cast<float4*>(final_state + hrow)[k] =
+                make_float4(hs[4 * k], hs[4 * k + 1], hs[4 * k + 2], hs[4 * k + 3]);
+        }
+      } else {
+        // the next window's scalars, then O(n + 1) = h_out once the carried product of window
+        // n has read O(n)
+        if (named_bar_or(bar_s, 128,
+                         !mbar_wait_short(&xready[xs(n + 1)], xph(n + 1), spin_ns) || !o_free(n + 1))) {
+          ok = false;
+          break;
+        }
+        alpha = scal[xs(n + 1)].alpha[hd];
+        fastH = scal[xs(n + 1)].fast[hd] != 0;
+        put_all_o();
+        fence_proxy_async_smem();
+        mbar_arrive(&oready[(n + 1) & 1]);
+      }
+    }
+    } else {
     for (int n = 0; ok; ++n) {
       WinInfo I;
       if (named_bar_or(bar_s, 128, !read_info(n, I))) {
@@ -846,6 +984,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
+    }
     }
   } else {
     regs_acquire<kRegHead>();
@@ -1064,16 +1203,19 @@ cudaError_t launch_onepass(const Dims& d, const OnePassMaps& maps, const float* 
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
   const size_t smem = onepass_smem_bytes(d);
-  e = cudaFuncSetAttribute(ssd_onepass_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  // product buffers up to dstate 128 (two of them and two output accumulators fill tensor
+  // memory); the state accumulated in tensor memory at dstate 256
+  const auto kern = d.N == 64 ? ssd_onepass_kernel<64> : d.N == 128 ? ssd_onepass_kernel<128> : ssd_onepass_kernel<256>;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   // the register split assumes the compiled count; any other count is refused here
   cudaFuncAttributes fa{};
-  e = cudaFuncGetAttributes(&fa, ssd_onepass_kernel);
+  e = cudaFuncGetAttributes(&fa, kern);
   if (e != cudaSuccess) return e;
   if (fa.numRegs != static_cast<int>(kRegLaunch)) return cudaErrorInvalidConfiguration;
   const int R = onepass_run_length(d, sms);
   const int grid = onepass_grid(d, sms, R);
-  return launch_k(ssd_onepass_kernel, dim3(grid), dim3(kThreads), smem, stream, dependent, maps.x, maps.cm, maps.bm,
+  return launch_k(kern, dim3(grid), dim3(kThreads), smem, stream, dependent, maps.x, maps.cm, maps.bm,
                   maps.m, maps.y, d, R, dt, A, D, static_cast<const __nv_bfloat16*>(w.cbm), init, final_state,
                   w.hslot, w.flags, w.counter, static_cast<const __nv_bfloat16*>(x), w.status, spin_ns);
 }
