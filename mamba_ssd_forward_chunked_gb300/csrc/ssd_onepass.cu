@@ -287,18 +287,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* full = bars;          // [3] ring stage landed
   uint64_t* empty = bars + 3;     // [3] ring stage consumed (MMA commit)
   uint64_t* xfull = bars + 6;     // [3] X window landed
-  uint64_t* xready = bars + 9;    // [3] X scaled and window scalars published (256)
+  // [3] X scaled and window scalars published (256); with product buffers also the pass's read
+  // of the product two windows back (+128), so the state product's buffer is free
+  uint64_t* xready = bars + 9;
   uint64_t* ystaged = bars + 12;  // [3] y written into the X buffer (256: both head warpgroups)
   uint64_t* tfull = bars + 15;    // [8] window ring
   uint64_t* tempty = bars + 23;   // [8] (15 warps read each entry)
-  // [2] state in tensor memory: pi h_in of the window in place; product buffers: the pass has
-  // read the window's product, so its buffer is free (128)
-  uint64_t* sready = bars + 31;
+  uint64_t* sready = bars + 31;   // [2] state in tensor memory: pi h_in of the window in place (128)
   uint64_t* dfull = bars + 33;    // [2] state product done (X^ of the window read)
-  uint64_t* cdone = bars + 35;    // [2] carried-state product done: O free, output complete
-  uint64_t* yfree = bars + 37;    // [2] output accumulator drained (256)
+  // [2] carried-state product done: O free; with product buffers (carried product last) also
+  // the output accumulator complete
+  uint64_t* cdone = bars + 35;
   uint64_t* oready = bars + 39;   // [2] O (bf16 h_in) of the window in place (128)
-  uint64_t* ydone = bars + 41;    // [2] output accumulator complete (intra and carried products done)
+  uint64_t* ydone = bars + 41;    // [2] state in tensor memory: output accumulator complete
   WinInfo* info = reinterpret_cast<WinInfo*>(smem + Ls.info);
   Scal* scal = reinterpret_cast<Scal*>(smem + Ls.scal);
   float* scanws = reinterpret_cast<float*>(smem + Ls.scan);  // [2 heads][2 windows][4]
@@ -310,7 +311,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
       mbar_init(&xfull[s], 1);
-      mbar_init(&xready[s], 256);
+      mbar_init(&xready[s], kPB ? 384 : 256);
       mbar_init(&ystaged[s], 256);
     }
     for (int s = 0; s < kInfoRing; ++s) {
@@ -323,7 +324,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&ydone[s], 1);
       mbar_init(&dfull[s], 1);
       mbar_init(&cdone[s], 1);
-      mbar_init(&yfree[s], 256);
     }
     fence_mbar_init();
   }
@@ -506,7 +506,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int nitems = 1 + 2 * nhalf;
         for (int q = 0; q < nitems && ok; ++q, ++it) {
           const int s = it % Ls.stages, rnd = it / Ls.stages;
-          if (rnd > 0 && !mbar_wait_short(&empty[s], (rnd - 1) & 1, spin_ns)) {
+          // With product buffers each item has its own stage, and B's and C's are free once the
+          // state (resp. carried) product of the window before has completed, which dfull (cdone)
+          // already signals; M's stage, and every stage at dstate 256, has its own commit (empty).
+          bool free_stage = true;
+          if (rnd > 0) {
+            if (kPB && q == 0)
+              free_stage = mbar_wait_short(&dfull[(n - 1) & 1], yph(n - 1), spin_ns);
+            else if (kPB && q == 2)
+              free_stage = mbar_wait_short(&cdone[(n - 1) & 1], yph(n - 1), spin_ns);
+            else
+              free_stage = mbar_wait_short(&empty[s], (rnd - 1) & 1, spin_ns);
+          }
+          if (!free_stage) {
             ok = false;
             break;
           }
@@ -555,11 +567,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!read_info1(0, cur)) ok = false;
       for (int n = 0; ok && !(cur.flags & 4); ++n) {
         const int yb = n & 1;
-        // S(n) once X^ is scaled: accumulated onto the state once pi h_in is in place (state in
-        // tensor memory), or into product buffer n % 2 once the pass has read window n - 2's
-        // product from it (product buffers)
-        if (!(kPB ? n < 2 || mbar_wait_short(&sready[yb], yph(n - 2), spin_ns)
-                  : mbar_wait_short(&sready[yb], yph(n), spin_ns)) ||
+        // S(n) once X^ is scaled: into product buffer n % 2 (xready(n) also says that the pass
+        // has read window n - 2's product from it), or accumulated onto the state once pi h_in
+        // is in place (sready)
+        if ((!kPB && !mbar_wait_short(&sready[yb], yph(n), spin_ns)) ||
             !mbar_wait_short(&xready[xs(n)], xph(n), spin_ns)) {
           ok = false;
           break;
@@ -579,18 +590,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
           for (int k = 0; k < kWin / 16; ++k)
             mma_ss<false>(dst, da + k * (2048 >> 4), db + k * (2048 >> 4), id_st, (kPB && k == 0) ? 0u : 1u);
-          release(it++);
+          if constexpr (!kPB) release(it);  // product buffers: dfull frees B's stage
+          ++it;
         }
         if (!ok) break;
         mma_commit(&dfull[yb]);
-        // The intra and carried products into output accumulator n % 2, once window n - 2's
-        // output is drained.  Up to dstate 128 the intra product goes first; at dstate 256 the
-        // carried product does, so that O(n) is free early: the pass writes O for the first
-        // 128 columns before it hands the state over.
-        if (n >= 2 && !mbar_wait_short(&yfree[yb], yph(n - 2), spin_ns)) {
-          ok = false;
-          break;
-        }
+        // The intra and carried products into output accumulator n % 2.  Window n - 2's output
+        // has been drained from it: the head warpgroups' epilogue of window n - 2 comes before
+        // their X scaling of window n, which xready(n) waited for.  Up to dstate 128 the intra
+        // product goes first; at dstate 256 the carried product does, so that O(n) is free
+        // early: the pass writes O for the first 128 columns before it hands the state over.
         auto intra = [&]() -> bool {
           const uint32_t sm = stage(it);
           if (!sm) return false;
@@ -623,7 +632,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               const uint32_t off = (k >> 2) * (kAtom >> 4) + (k & 3) * 2;
               mma_ss<false>(tmem + kColY + 128 * yb, da + off, db + off, id_yo, (fast || hf != 0 || k != 0) ? 1u : 0u);
             }
-            release(it++);
+            if constexpr (!kPB) release(it);  // product buffers: cdone frees C's stage
+            ++it;
           }
           mma_commit(&cdone[yb]);
           return true;
@@ -632,7 +642,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
-        mma_commit(&ydone[yb]);
+        if constexpr (!kPB) mma_commit(&ydone[yb]);  // product buffers: cdone, the last commit
         if (!read_info1(n + 1, cur)) {
           ok = false;
           break;
@@ -642,6 +652,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   } else if (warp < 8) {
     regs_acquire<kRegState>();
+    if constexpr (kPB) {
+      // windows 0 and 1 have no product two windows back to read
+      mbar_arrive(&xready[xs(0)]);
+      mbar_arrive(&xready[xs(1)]);
+    }
     grid_dep_wait();  // the flags are cleared by the pre-pass
     // ------------------------------------------------------------ state pass
     const int et = threadIdx.x - 128;  // TMEM lane = state row (head hd, p)
@@ -758,7 +773,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       tc_fence_before();
-      mbar_arrive(&sready[yb]);
+      mbar_arrive(&xready[xs(n + 2)]);  // product buffer n % 2 is free for S(n + 2)
       if (last) {
         // publish: the slot for the run that continues this sequence, or final_state
         if (!seq_last) {
@@ -1091,7 +1106,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // y = r_i * acc + D x_i, written over X^ in the X buffer (once the state product,
       // issued after the carried one, has read X^ too); warp 3 stores it
       if (named_bar_or(bar_h, 128, !mbar_wait_short(&xready[sb], xph(n), spin_ns) ||
-                                       !mbar_wait_short(&ydone[yb], yph(n), spin_ns) ||
+                                       !mbar_wait_short(kPB ? &cdone[yb] : &ydone[yb], yph(n), spin_ns) ||
                                        !mbar_wait_short(&dfull[yb], yph(n), spin_ns))) {
         ok = false;
         break;
@@ -1107,7 +1122,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32(tacc + 32, *reinterpret_cast<uint32_t(*)[32]>(ya + 32));
         tmem_ld_wait();
         tc_fence_before();
-        mbar_arrive(&yfree[yb]);
         // y_i = r_i * acc: the accumulator started at D x_i / r_i (see prepare)
         const float ri = fast_exp2(cur.g);
 #pragma unroll
@@ -1128,7 +1142,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         grid_dep_wait();  // the causal blocks come from the pre-pass
         exact_epilogue(d, cur.b, h, t0, r, cur.g, cur.a, Dh, Mrow, xg, dtg, tacc, xr);
         tc_fence_before();
-        mbar_arrive(&yfree[yb]);
       }
       fence_proxy_async_smem();
       mbar_arrive(&ystaged[sb]);
