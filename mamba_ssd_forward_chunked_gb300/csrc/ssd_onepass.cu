@@ -292,7 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* xready = bars + 9;
   uint64_t* ystaged = bars + 12;  // [3] y written into the X buffer (256: both head warpgroups)
   uint64_t* tfull = bars + 15;    // [8] window ring
-  uint64_t* tempty = bars + 23;   // [8] (15 warps read each entry)
+  uint64_t* tempty = bars + 23;   // [8] (14 warps read each entry)
   uint64_t* sready = bars + 31;   // [2] state in tensor memory: pi h_in of the window in place (128)
   uint64_t* dfull = bars + 33;    // [2] state product done (X^ of the window read)
   // [2] carried-state product done: O free; with product buffers (carried product last) also
@@ -304,6 +304,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   Scal* scal = reinterpret_cast<Scal*>(smem + Ls.scal);
   float* scanws = reinterpret_cast<float*>(smem + Ls.scan);  // [2 heads][2 windows][4]
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + Ls.holder);
+  // The CTA's number of windows, once the schedule knows it (INT_MAX until then): the tensor-core
+  // thread reads it instead of the window ring.
+  volatile int* nwin_s = reinterpret_cast<volatile int*>(smem + Ls.holder + 4);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
@@ -316,7 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int s = 0; s < kInfoRing; ++s) {
       mbar_init(&tfull[s], 1);
-      mbar_init(&tempty[s], 15);
+      mbar_init(&tempty[s], 14);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&sready[s], 128);
@@ -325,6 +328,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&dfull[s], 1);
       mbar_init(&cdone[s], 1);
     }
+    *nwin_s = 0x7fffffff;
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
@@ -439,6 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           put(bg / d.G, (bg % d.G) * Q + q, w0, w1, 0);
         }
       }
+      *nwin_s = n;         // for the tensor-core thread
       put(0, 0, 0, 1, 4);  // the end marker
       ok = good;
     }
@@ -563,15 +568,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         return smem_u32(smem + Ls.ring + s * kStage);
       };
       auto release = [&](int i) { mma_commit(&empty[i % Ls.stages]); };
-      WinInfo cur;
-      if (!read_info1(0, cur)) ok = false;
-      for (int n = 0; ok && !(cur.flags & 4); ++n) {
+      for (int n = 0; ok; ++n) {
         const int yb = n & 1;
         // S(n) once X^ is scaled: into product buffer n % 2 (xready(n) also says that the pass
         // has read window n - 2's product from it), or accumulated onto the state once pi h_in
-        // is in place (sready)
-        if ((!kPB && !mbar_wait_short(&sready[yb], yph(n), spin_ns)) ||
-            !mbar_wait_short(&xready[xs(n)], xph(n), spin_ns)) {
+        // is in place (sready).  Window n exists unless the schedule has published fewer
+        // windows; that count is read only while xready(n) is still open.
+        bool have = true;
+        if (!mbar_try_wait_short(&xready[xs(n)], xph(n))) {
+          const uint64_t t0w = globaltimer_ns();
+          for (;;) {
+            if (mbar_try_wait_short(&xready[xs(n)], xph(n))) break;
+            if (n >= *nwin_s) {
+              have = false;
+              break;
+            }
+            if (globaltimer_ns() - t0w > spin_ns) {
+              ok = false;
+              break;
+            }
+          }
+        }
+        if (!ok || !have) break;
+        if (!kPB && !mbar_wait_short(&sready[yb], yph(n), spin_ns)) {
           ok = false;
           break;
         }
@@ -643,10 +662,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         if constexpr (!kPB) mma_commit(&ydone[yb]);  // product buffers: cdone, the last commit
-        if (!read_info1(n + 1, cur)) {
-          ok = false;
-          break;
-        }
       }
     }
   }
