@@ -1118,11 +1118,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int yb = n & 1, sb = xs(n);
       const int h = 2 * cur.pair + hh;
       const int t0 = cur.w * kWin;
-      // y = r_i * acc + D x_i, written over X^ in the X buffer (once the state product,
-      // issued after the carried one, has read X^ too); warp 3 stores it
+      // y = r_i * acc + D x_i, written over X^ in the X buffer once the window's last product
+      // is done (tcgen05 operations complete in order, so the state product, which reads X^
+      // too, is done as well); warp 3 stores it
       if (named_bar_or(bar_h, 128, !mbar_wait_short(&xready[sb], xph(n), spin_ns) ||
-                                       !mbar_wait_short(kPB ? &cdone[yb] : &ydone[yb], yph(n), spin_ns) ||
-                                       !mbar_wait_short(&dfull[yb], yph(n), spin_ns))) {
+                                       !mbar_wait_short(kPB ? &cdone[yb] : &ydone[yb], yph(n), spin_ns))) {
         ok = false;
         break;
       }
