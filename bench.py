@@ -48,6 +48,8 @@ PRE_STEP_SLEEP_CYCLES = 200_000
 NOMINAL_TF32_OVER_BF16 = 1.1 / 2.25
 KERNELS = ("chunk_cumsum", "chunk_state", "state_passing", "compute_out")  # staged schedule
 FUSED_KERNELS = ("causal_cb", "ssd_onepass")                                 # one-pass schedule
+# segmented one-pass schedule: the staged state kernels over segments, then the one-pass pair
+SEGMENTED_KERNELS = ("chunk_cumsum", "chunk_state", "state_passing", "causal_cb", "ssd_onepass")
 
 
 # ------------------------------------------------------------------ model of the work
@@ -276,8 +278,9 @@ def run_gpu(args, w: ssd_synth.Workload, rank: int, world: int, local_rank: int)
         ssd.ssd_fwd(d["x"], d["dt"], d["A"], d["Bm"], d["Cm"], d["D"], w.chunk_size, init_state=init, y=y,
                     final_state=fin, workspace=ws, stream=stream)
 
-    fused = ssd.ssd_fwd_kernel_count(shape) == 2  # the schedule ssd_fwd takes for this shape
-    names = FUSED_KERNELS if fused else KERNELS
+    nkern = ssd.ssd_fwd_kernel_count(shape)  # the schedule ssd_fwd takes for this shape
+    fused = nkern in (2, 5)
+    names = FUSED_KERNELS if nkern == 2 else SEGMENTED_KERNELS if nkern == 5 else KERNELS
 
     def staged(ev):
         # the same launches ssd_fwd makes, in its order, one ssd_fwd_range call each with events between them
@@ -423,7 +426,7 @@ def run_gpu(args, w: ssd_synth.Workload, rank: int, world: int, local_rank: int)
         "kernels_ms": per_kernel,
         "timing": "median over steps (CUDA events on the launching stream)",
         "gpu_launches": ssd.ssd_fwd_kernel_count(shape) * args.steps,
-        "schedule": "one-pass" if fused else "staged",
+        "schedule": "one-pass" if nkern == 2 else "segmented one-pass" if nkern == 5 else "staged",
         "e2e": {"value": whole_job_tokens_per_s(w.tokens, world, ms_e2e), "unit": "tokens/s", "ms_per_step": ms_e2e,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "wall_s_timed_region_1": wall,

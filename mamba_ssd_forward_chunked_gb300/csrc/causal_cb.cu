@@ -36,8 +36,8 @@ constexpr uint32_t kAtom = 16384;  // 64 bf16 columns x 128 rows
 __global__ void __launch_bounds__(kThreads) causal_cb_kernel(const __grid_constant__ CUtensorMap cmap,
                                                              const __grid_constant__ CUtensorMap bmap,
                                                              const __grid_constant__ CUtensorMap mmap, Dims d,
-                                                             int nwin, int* status, int* chain, int nchain,
-                                                             uint64_t spin_ns) {
+                                                             int nwin, int* status, int clear_status, int* chain,
+                                                             int nchain, uint64_t spin_ns) {
   grid_dep_launch();  // the one-pass kernel may start its prologue now
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -54,7 +54,7 @@ __global__ void __launch_bounds__(kThreads) causal_cb_kernel(const __grid_consta
   const int b = unit / (d.G * nwin);
 
   if (unit == 0) {
-    if (threadIdx.x == 0) *status = 0;
+    if (threadIdx.x == 0 && clear_status) *status = 0;
     for (int k = threadIdx.x; k < nchain; k += kThreads) chain[k] = 0;
   }
   if (threadIdx.x == 0) {
@@ -143,7 +143,7 @@ __global__ void __launch_bounds__(kThreads) causal_cb_kernel(const __grid_consta
 size_t causal_cb_smem_bytes(const Dims& d) { return 1024 + 2 * (d.N / 64) * kAtom + 2 * kAtom + 64; }
 
 cudaError_t launch_causal_cb(const Dims& d, const OnePassMaps& maps, const Work& w, uint64_t spin_ns,
-                             cudaStream_t stream) {
+                             cudaStream_t stream, bool first) {
   const int nwin = (d.L + kWin - 1) / kWin;
   const int64_t units = static_cast<int64_t>(d.B) * nwin * d.G;
   if (units <= 0 || units > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
@@ -152,7 +152,8 @@ cudaError_t launch_causal_cb(const Dims& d, const OnePassMaps& maps, const Work&
       cudaFuncSetAttribute(causal_cb_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   return launch_k(causal_cb_kernel, dim3(static_cast<unsigned>(units)), dim3(kThreads), smem, stream, false,
-                  maps.cm, maps.bm, maps.m, d, nwin, w.status, w.counter, 1 + d.B * (d.H / 2), spin_ns);
+                  maps.cm, maps.bm, maps.m, d, nwin, w.status, first ? 1 : 0, w.counter, first ? 1 + d.B * (d.H / 2) : 0,
+                  spin_ns);
 }
 
 }  // namespace ssd

@@ -45,7 +45,10 @@ __global__ void __launch_bounds__(kThreads) chunk_cumsum_kernel(Dims d, const fl
     return;
   }
   const int Q = d.Q;
-  const int ld = Q + 1;  // odd row stride: the transposing writes hit distinct banks
+  // a chunk longer than 256 tokens (the one-pass schedule's segments) goes in pieces of 256,
+  // the running sum carried from piece to piece
+  const int P0 = Q < 256 ? Q : 256;
+  const int ld = P0 + 1;  // odd row stride: the transposing writes hit distinct banks
   const int hslices = (d.H + kHeadsPerBlock - 1) / kHeadsPerBlock;
   const int c = blk % d.nc;
   const int h0 = (blk / d.nc) % hslices * kHeadsPerBlock;
@@ -55,57 +58,62 @@ __global__ void __launch_bounds__(kThreads) chunk_cumsum_kernel(Dims d, const fl
     for (int k = threadIdx.x; k < nchain; k += kThreads) chain[k] = 0;  // one-pass kernel's counter and flags
   }
 
-  // all of the block's loads first (Q * 8 / 256 <= 8 per thread), then the stores to shared memory
-  float v[8];
-#pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    const int idx = threadIdx.x + k * kThreads;
-    const int t = idx / kHeadsPerBlock, hh = idx % kHeadsPerBlock;
-    const int tok = c * Q + t, h = h0 + hh;
-    v[k] = (t < Q && tok < d.L && h < d.H) ? dt[(static_cast<int64_t>(b) * d.L + tok) * d.H + h] : 0.f;
-  }
-#pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    const int idx = threadIdx.x + k * kThreads;
-    const int t = idx / kHeadsPerBlock, hh = idx % kHeadsPerBlock;
-    if (t < Q) s_dt[hh * ld + t] = v[k];
-  }
-  __syncthreads();
-
   const int lane = threadIdx.x & 31, hh = threadIdx.x >> 5;  // one warp per head
   const int h = h0 + hh;
   const float a_h = h < d.H ? A[h] : 0.f;
-  const int per = Q / 32;  // 2, 4 or 8 tokens per lane
-  float run[8];
-  float acc = 0.f;
+  const int per = P0 / 32;  // 2, 4 or 8 tokens per lane
+  float carry = 0.f;        // sum of the chunk's earlier pieces
+  for (int t0 = c * Q; t0 < (c + 1) * Q; t0 += P0) {
+    // all of the block's loads first (P0 * 8 / 256 <= 8 per thread), then the stores to shared memory
+    float v[8];
 #pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    if (k < per) {
-      acc += s_dt[hh * ld + lane * per + k] * a_h;
-      run[k] = acc;
+    for (int k = 0; k < 8; ++k) {
+      const int idx = threadIdx.x + k * kThreads;
+      const int t = idx / kHeadsPerBlock, h2 = h0 + idx % kHeadsPerBlock;
+      const int tok = t0 + t;
+      v[k] = (t < P0 && tok < d.L && h2 < d.H) ? dt[(static_cast<int64_t>(b) * d.L + tok) * d.H + h2] : 0.f;
     }
-  }
-  float incl = acc;
+    __syncthreads();  // the previous piece's shared-memory reads are done
 #pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const float u = __shfl_up_sync(0xffffffffu, incl, off);
-    if (lane >= off) incl += u;
-  }
-  // exclusive prefix = the previous lane's inclusive one (not incl - acc): each G_t is then
-  // computed from tokens <= t only, so later tokens cannot change it even by rounding
-  float excl = __shfl_up_sync(0xffffffffu, incl, 1);
-  if (lane == 0) excl = 0.f;
-#pragma unroll
-  for (int k = 0; k < 8; ++k)
-    if (k < per) s_g[hh * ld + lane * per + k] = run[k] + excl;
-  __syncthreads();
+    for (int k = 0; k < 8; ++k) {
+      const int idx = threadIdx.x + k * kThreads;
+      const int t = idx / kHeadsPerBlock, hs = idx % kHeadsPerBlock;
+      if (t < P0) s_dt[hs * ld + t] = v[k];
+    }
+    __syncthreads();
 
-  for (int idx = threadIdx.x; idx < kHeadsPerBlock * Q; idx += kThreads) {
-    const int hq = idx / Q, t = idx % Q;
-    if (h0 + hq < d.H) {
-      const int64_t o = (static_cast<int64_t>(b) * d.H + h0 + hq) * d.Lp + static_cast<int64_t>(c) * Q + t;
-      cumsum[o] = s_g[hq * ld + t];
-      dt_t[o] = s_dt[hq * ld + t];
+    float run[8];
+    float acc = 0.f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      if (k < per) {
+        acc += s_dt[hh * ld + lane * per + k] * a_h;
+        run[k] = acc;
+      }
+    }
+    float incl = acc;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const float u = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += u;
+    }
+    // exclusive prefix = the previous lane's inclusive one (not incl - acc): each G_t is then
+    // computed from tokens <= t only, so later tokens cannot change it even by rounding
+    float excl = __shfl_up_sync(0xffffffffu, incl, 1);
+    if (lane == 0) excl = 0.f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      if (k < per) s_g[hh * ld + lane * per + k] = run[k] + excl + carry;
+    carry += __shfl_sync(0xffffffffu, incl, 31);
+    __syncthreads();
+
+    for (int idx = threadIdx.x; idx < kHeadsPerBlock * P0; idx += kThreads) {
+      const int hq = idx / P0, t = idx % P0;
+      if (h0 + hq < d.H) {
+        const int64_t o = (static_cast<int64_t>(b) * d.H + h0 + hq) * d.Lp + t0 + t;
+        cumsum[o] = s_g[hq * ld + t];
+        dt_t[o] = s_dt[hq * ld + t];
+      }
     }
   }
 }

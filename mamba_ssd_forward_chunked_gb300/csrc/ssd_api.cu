@@ -228,6 +228,28 @@ bool use_fused(const ssd_shape& s) {
   return sms > 0 && s.batch * (s.nheads / 2) >= sms;
 }
 
+// Windows per segment of the segmented one-pass schedule, or 0 where it does not apply.  With
+// fewer head-pair sequences than multiprocessors but long sequences (bf16), the staged kernels
+// first carry the state across segments of 2048 (or 1024) tokens -- chunk_cumsum, chunk_state
+// and state_passing with the segment as their chunk -- and the one-pass kernel then runs every
+// segment as an independent run from its entering state, so every multiprocessor has work.
+// It applies when the segments divide the sequence and give at least two runs per
+// multiprocessor.
+int segment_windows(const ssd_shape& s) {
+  if (s.dtype != SSD_BF16 || use_fused(s)) return 0;
+  const int sms = sm_count();
+  if (sms <= 0) return 0;
+  const int64_t pairs = static_cast<int64_t>(s.batch) * (s.nheads / 2);
+  for (int r : {16, 8}) {
+    const int64_t q = 128 * r;
+    if (s.seqlen % q == 0 && pairs * (s.seqlen / q) >= 2 * static_cast<int64_t>(sms)) return r;
+  }
+  return 0;
+}
+
+// 0 staged, 1 one-pass, 2 segmented one-pass
+int schedule_of(const ssd_shape& s) { return use_fused(s) ? 1 : segment_windows(s) > 0 ? 2 : 0; }
+
 ssd_status fwd_impl(int path, int first, int end, const ssd_shape* shape, const void* x, const float* dt,
                     const float* A, const void* Bm, const void* Cm, const float* D, const float* init_state, void* y,
                     float* final_state, void* workspace, size_t workspace_bytes, ssd_stream_t stream);
@@ -304,8 +326,8 @@ size_t ssd_fwd_workspace_size(const ssd_shape* shape) {
 
 int ssd_fwd_kernel_count(const ssd_shape* shape) {
   if (ssd_validate_shape(shape) != SSD_OK || empty_problem(*shape)) return 0;
-  if (use_fused(*shape)) return 2;
-  return 4;
+  const int sched = schedule_of(*shape);
+  return sched == 1 ? 2 : sched == 2 ? 5 : 4;
 }
 
 ssd_status ssd_chunk_cumsum(const ssd_shape* shape, const float* dt, const float* A, void* workspace,
@@ -378,7 +400,7 @@ ssd_status ssd_compute_out(const ssd_shape* shape, const void* x, const void* Bm
 ssd_status ssd_fwd(const ssd_shape* shape, const void* x, const float* dt, const float* A, const void* Bm,
                    const void* Cm, const float* D, const float* init_state, void* y, float* final_state,
                    void* workspace, size_t workspace_bytes, ssd_stream_t stream) {
-  const int path = shape && ssd_validate_shape(shape) == SSD_OK && use_fused(*shape) ? 1 : 0;
+  const int path = shape && ssd_validate_shape(shape) == SSD_OK ? schedule_of(*shape) : 0;
   return fwd_impl(path, 0, 1 << 30, shape, x, dt, A, Bm, Cm, D, init_state, y, final_state, workspace,
                   workspace_bytes, stream);
 }
@@ -388,7 +410,7 @@ ssd_status ssd_fwd_range(const ssd_shape* shape, const void* x, const float* dt,
                          void* workspace, size_t workspace_bytes, int first_launch, int end_launch,
                          ssd_stream_t stream) {
   if (first_launch < 0 || end_launch < first_launch) return SSD_ERR_INVALID_ARG;
-  const int path = shape && ssd_validate_shape(shape) == SSD_OK && use_fused(*shape) ? 1 : 0;
+  const int path = shape && ssd_validate_shape(shape) == SSD_OK ? schedule_of(*shape) : 0;
   return fwd_impl(path, first_launch, end_launch, shape, x, dt, A, Bm, Cm, D, init_state, y, final_state, workspace,
                   workspace_bytes, stream);
 }
@@ -441,7 +463,7 @@ ssd_status ssd_fwd_fused(const ssd_shape* shape, const void* x, const float* dt,
 namespace ssd {
 namespace {
 
-// path: 0 staged, 1 one-pass.  Enqueues the schedule's launches with index in
+// path: 0 staged, 1 one-pass, 2 segmented one-pass.  Enqueues the schedule's launches with index in
 // [first, end); a launch is a programmatic dependent only of a launch of the
 // same call (the first one enqueued here is an ordinary stream-ordered launch).
 ssd_status fwd_impl(int path, int first, int end, const ssd_shape* shape, const void* x, const float* dt,
@@ -479,6 +501,28 @@ ssd_status fwd_impl(int path, int first, int end, const ssd_shape* shape, const 
     step([&](bool) { return launch_causal_cb(d, omaps, w, spin, cs); });
     step([&](bool dep) {
       return launch_onepass(d, omaps, dt, A, D, x, init_state, final_state, w, spin, cs, dep);
+    });
+    return from_cuda(e);
+  }
+  if (path == 2) {
+    // the staged state kernels with the segment as their chunk (the workspace's chunk-sized
+    // regions hold it: the segment divides the sequence and is longer than the chunk), then
+    // the one-pass kernel from the segments' entering states
+    const int R = segment_windows(*shape);
+    ssd_shape ss = *shape;
+    ss.chunk_size = 128 * R;
+    const Dims ds = make_dims(ss);
+    ChunkStateMaps smaps;
+    OnePassMaps omaps;
+    if (!build_state_maps(ss, x, Bm, w.states, &smaps) || !build_onepass_maps(*shape, x, Bm, Cm, y, w.cbm, &omaps))
+      return SSD_ERR_CUDA;
+    const uint64_t spin = spin_limit_ns();
+    step([&](bool) { return launch_chunk_cumsum(ds, dt, A, w, cs, nullptr); });
+    step([&](bool dep) { return launch_chunk_state(ds, true, smaps, w, spin, cs, dep); });
+    step([&](bool) { return launch_state_passing(ds, true, init_state, nullptr, w, cs, false); });
+    step([&](bool) { return launch_causal_cb(d, omaps, w, spin, cs, false); });
+    step([&](bool dep) {
+      return launch_onepass(d, omaps, dt, A, D, x, init_state, final_state, w, spin, cs, dep, w.states_bf16, R);
     });
     return from_cuda(e);
   }

@@ -88,11 +88,16 @@ cudaError_t launch_state_passing(const Dims& d, bool bf16, const float* init, fl
 cudaError_t launch_compute_out(const Dims& d, bool bf16, const ComputeOutMaps& maps, const float* D,
                                const void* x, void* y, const Work& w, uint64_t spin_ns, cudaStream_t stream,
                                bool dependent = false);
+// first: the call's first launch, which clears the status word and the one-pass kernel's run
+// counter and flags (otherwise an earlier launch of the call has)
 cudaError_t launch_causal_cb(const Dims& d, const OnePassMaps& maps, const Work& w, uint64_t spin_ns,
-                             cudaStream_t stream);
+                             cudaStream_t stream, bool first = true);
+// With seg_h set, every run is one segment of seg_windows windows whose entering state is
+// read from seg_h (bf16 [B][segment][H][P][N]) instead of being chained between runs.
 cudaError_t launch_onepass(const Dims& d, const OnePassMaps& maps, const float* dt, const float* A, const float* D,
                            const void* x, const float* init, float* final_state, const Work& w, uint64_t spin_ns,
-                           cudaStream_t stream, bool dependent = false);
+                           cudaStream_t stream, bool dependent = false, const void* seg_h = nullptr,
+                           int seg_windows = 0);
 cudaError_t launch_timeout_probe(int* status, uint64_t limit_ns, cudaStream_t stream);
 
 }  // namespace ssd

@@ -45,10 +45,12 @@ SWEEP = sorted(n for n in W if n.startswith("sweep-"))
 def test_sweep_points_sampled(name):
     """Every point of the 65,536-token shape sweep (bf16, 64 heads in 8 groups),
     at full size, against the oracle on sampled (batch, head) pairs: the
-    schedule ssd_fwd picks, and the other one too (the one-pass kernel, or the
+    schedule ssd_fwd picks, and the others too (the one-pass kernel, and the
     staged kernels through the four step calls).  The staged bf16 path stores
     chunk and entering states in bf16; L 32768 at chunk 128 is its longest
-    chain (256 chunks)."""
+    chain (256 chunks).  At L 32768 ssd_fwd takes the segmented one-pass
+    schedule (entering states of 2048-token segments from the staged kernels,
+    in bf16)."""
     import mamba_ssd_forward_chunked_gb300 as ssd
     w = W[name]
     assert len(SWEEP) == 24
@@ -61,8 +63,9 @@ def test_sweep_points_sampled(name):
     d = to_device(inp, w.dtype)
     del inp
     shape = ssd.shape_of(d["x"], d["Bm"], w.chunk_size)
-    picked = "fused" if ssd.ssd_fwd_kernel_count(shape) == 2 else "staged"
-    for schedule in ("auto", "staged" if picked == "fused" else "fused"):
+    picked = {2: "fused", 5: "segmented"}.get(ssd.ssd_fwd_kernel_count(shape), "staged")
+    others = {"fused": ["staged"], "staged": ["fused"], "segmented": ["fused", "staged"]}[picked]
+    for schedule in ["auto"] + others:
         y, f = run_gpu_schedule(d, w.chunk_size, schedule)
         torch.cuda.synchronize()
         ys, fs = pair_rows(y, f, pairs)
