@@ -129,7 +129,7 @@ ssd_status ssd_fwd_workspace_layout(const ssd_shape* shape, ssd_workspace_layout
  * invalid or unsupported). */
 size_t ssd_fwd_workspace_size(const ssd_shape* shape);
 
-/* The whole forward pass, enqueued on `stream`.  Two schedules give the
+/* The whole forward pass, enqueued on `stream`.  Three schedules give the
  * recurrence's result (see the steps below for the formulas):
  *  - one-pass (ssd_fwd_fused; SSD_BF16 only): ssd_causal_cb, then one
  *    persistent kernel (ssd_fused_pass) that runs every 128-token window of a
@@ -142,10 +142,16 @@ size_t ssd_fwd_workspace_size(const ssd_shape* shape);
  *    (SSD_F32: the chunk_cumsum launch also transposes Bm into the workspace,
  *    once for every head of a group; ssd_chunk_state called alone does that
  *    transpose itself).
+ *  - segmented one-pass (SSD_BF16 only): chunk_cumsum, chunk_state and
+ *    state_passing with segments of 2048 (or 1024) tokens as their chunk,
+ *    which leaves every segment's entering state (bf16) in the workspace, then
+ *    the one-pass pair, which runs each segment as an independent run from it.
  * ssd_fwd takes the one-pass schedule for SSD_BF16 when there are at least as
  * many (batch, head pair) sequences as multiprocessors (below that the chain
- * of windows, not bandwidth, bounds the one-pass kernel); otherwise the staged
- * one.  The one-pass schedule works in windows of 128
+ * of windows, not bandwidth, bounds the one-pass kernel); below that, the
+ * segmented one when segments divide the sequence and give at least two per
+ * multiprocessor over all pairs; otherwise the staged one (always for
+ * SSD_F32).  The one-pass schedules work in windows of 128
  * tokens whatever chunk_size is; the result is the recurrence's either way.
  * init_state may be NULL (zero initial state); final_state
  * may be NULL (not written; the workspace holds the running state instead).
@@ -239,7 +245,8 @@ ssd_status ssd_compute_out(const ssd_shape* shape, const void* x, const void* Bm
  * hang).  The workspace needs at least 4 bytes. */
 ssd_status ssd_debug_timeout_probe(void* workspace, uint32_t limit_us, ssd_stream_t stream);
 
-/* Number of kernels ssd_fwd enqueues for `shape` (0 for an empty input). */
+/* Number of kernels ssd_fwd enqueues for `shape` (0 for an empty input): 2
+ * on the one-pass schedule, 5 on the segmented one and 4 on the staged one. */
 int ssd_fwd_kernel_count(const ssd_shape* shape);
 
 /* Bytes of the device array that ssd_fwd_static_scratch uses as its workspace. */
