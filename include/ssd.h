@@ -149,9 +149,9 @@ size_t ssd_fwd_workspace_size(const ssd_shape* shape);
  * ssd_fwd takes the one-pass schedule for SSD_BF16 when there are at least as
  * many (batch, head pair) sequences as multiprocessors (below that the chain
  * of windows, not bandwidth, bounds the one-pass kernel); below that, the
- * segmented one when segments divide the sequence and give at least two per
- * multiprocessor over all pairs; otherwise the staged one (always for
- * SSD_F32).  The one-pass schedules work in windows of 128
+ * segmented one when the segments give at least two per multiprocessor over
+ * all pairs (a sequence's last segment may be shorter); otherwise the staged
+ * one (always for SSD_F32).  The one-pass schedules work in windows of 128
  * tokens whatever chunk_size is; the result is the recurrence's either way.
  * init_state may be NULL (zero initial state); final_state
  * may be NULL (not written; the workspace holds the running state instead).

@@ -4,6 +4,7 @@
 // ssd_fwd_check, which reads the 4-byte status word).
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
@@ -81,7 +82,9 @@ ssd_status layout_of(const ssd_shape* shape, ssd_workspace_layout* out) {
   if (st != SSD_OK) return st;
   const ssd_shape& s = *shape;
   const int64_t nc = (s.seqlen + s.chunk_size - 1) / s.chunk_size;
-  const size_t lp = static_cast<size_t>(nc) * s.chunk_size;
+  // bf16: the cumsum rows also hold the segmented schedule's 2048-token segments
+  const size_t lp = std::max(static_cast<size_t>(nc) * s.chunk_size,
+                             s.dtype == SSD_BF16 ? (static_cast<size_t>(s.seqlen) + 2047) / 2048 * 2048 : 0);
   const size_t heads = static_cast<size_t>(s.batch) * s.nheads;
   const size_t nstate = static_cast<size_t>(s.batch) * nc * s.nheads * s.headdim * s.dstate;
   ssd_workspace_layout L{};
@@ -233,8 +236,9 @@ bool use_fused(const ssd_shape& s) {
 // first carry the state across segments of 2048 (or 1024) tokens -- chunk_cumsum, chunk_state
 // and state_passing with the segment as their chunk -- and the one-pass kernel then runs every
 // segment as an independent run from its entering state, so every multiprocessor has work.
-// It applies when the segments divide the sequence and give at least two runs per
-// multiprocessor.
+// It applies when the segments give at least two runs per multiprocessor (a sequence's last
+// segment may be shorter).  Measured on GB300 with 64 sequences of 32768 tokens: segments of
+// 1024, 2048 and 4096 tokens ran 0.61-1.12, 0.62-1.12 and 0.68-1.18 ms.
 int segment_windows(const ssd_shape& s) {
   if (s.dtype != SSD_BF16 || use_fused(s)) return 0;
   const int sms = sm_count();
@@ -242,7 +246,7 @@ int segment_windows(const ssd_shape& s) {
   const int64_t pairs = static_cast<int64_t>(s.batch) * (s.nheads / 2);
   for (int r : {16, 8}) {
     const int64_t q = 128 * r;
-    if (s.seqlen % q == 0 && pairs * (s.seqlen / q) >= 2 * static_cast<int64_t>(sms)) return r;
+    if (pairs * ((s.seqlen + q - 1) / q) >= 2 * static_cast<int64_t>(sms)) return r;
   }
   return 0;
 }
@@ -505,9 +509,9 @@ ssd_status fwd_impl(int path, int first, int end, const ssd_shape* shape, const 
     return from_cuda(e);
   }
   if (path == 2) {
-    // the staged state kernels with the segment as their chunk (the workspace's chunk-sized
-    // regions hold it: the segment divides the sequence and is longer than the chunk), then
-    // the one-pass kernel from the segments' entering states
+    // the staged state kernels with the segment as their chunk (the workspace's cumsum rows are
+    // padded for it, and there are no more segments than chunks), then the one-pass kernel from
+    // the segments' entering states
     const int R = segment_windows(*shape);
     ssd_shape ss = *shape;
     ss.chunk_size = 128 * R;

@@ -75,6 +75,30 @@ def test_sweep_points_sampled(name):
         assert ey <= TOL[w.dtype] and ef <= TOL[w.dtype], (schedule, picked, ey, ef)
 
 
+
+def test_segmented_ragged_sampled():
+    """The segmented one-pass schedule on a sequence the segments do not divide
+    (30,000 tokens: 14 segments of 2048 and a ragged one of 1328, which also
+    ends inside a 128-token window), bf16 with an initial state, against the
+    oracle on sampled (batch, head) pairs."""
+    import mamba_ssd_forward_chunked_gb300 as ssd
+    w = ssd_synth.custom("g", dtype="bf16", batch=1, seqlen=30000, nheads=64, ngroups=8, dstate=128,
+                         chunk_size=256, init_state=True)
+    inp = ssd_synth.make_inputs(w)
+    pairs = sampled_pairs(w.batch, w.nheads, 6)
+    yr, fr, _ = oracle.recurrence(inp, pairs=pairs)
+    yrs = np.stack([yr[b, :, h] for b, h in pairs])
+    frs = np.stack([fr[b, h] for b, h in pairs])
+    d = to_device(inp, w.dtype)
+    shape = ssd.shape_of(d["x"], d["Bm"], w.chunk_size)
+    assert ssd.ssd_fwd_kernel_count(shape) == 5
+    y, f = run_gpu_schedule(d, w.chunk_size, "auto")
+    torch.cuda.synchronize()
+    ys, fs = pair_rows(y, f, pairs)
+    assert np.all(np.isfinite(ys))
+    ey, ef = rel_err(ys, yrs), rel_err(fs, frs)
+    assert ey <= TOL["bf16"] and ef <= TOL["bf16"], (ey, ef)
+
 SMALL = [
     dict(seqlen=1),
     dict(seqlen=37),
