@@ -82,9 +82,12 @@ ssd_status layout_of(const ssd_shape* shape, ssd_workspace_layout* out) {
   if (st != SSD_OK) return st;
   const ssd_shape& s = *shape;
   const int64_t nc = (s.seqlen + s.chunk_size - 1) / s.chunk_size;
-  // bf16: the cumsum rows also hold the segmented schedule's 2048-token segments
+  // bf16 beyond 2048 tokens: the cumsum rows also hold the segmented schedule's 2048-token
+  // segments (shorter sequences never take it)
   const size_t lp = std::max(static_cast<size_t>(nc) * s.chunk_size,
-                             s.dtype == SSD_BF16 ? (static_cast<size_t>(s.seqlen) + 2047) / 2048 * 2048 : 0);
+                             s.dtype == SSD_BF16 && s.seqlen > 2048
+                                 ? (static_cast<size_t>(s.seqlen) + 2047) / 2048 * 2048
+                                 : 0);
   const size_t heads = static_cast<size_t>(s.batch) * s.nheads;
   const size_t nstate = static_cast<size_t>(s.batch) * nc * s.nheads * s.headdim * s.dstate;
   ssd_workspace_layout L{};
@@ -240,7 +243,7 @@ bool use_fused(const ssd_shape& s) {
 // segment may be shorter).  Measured on GB300 with 64 sequences of 32768 tokens: segments of
 // 1024, 2048 and 4096 tokens ran 0.61-1.12, 0.62-1.12 and 0.68-1.18 ms.
 int segment_windows(const ssd_shape& s) {
-  if (s.dtype != SSD_BF16 || use_fused(s)) return 0;
+  if (s.dtype != SSD_BF16 || s.seqlen <= 2048 || use_fused(s)) return 0;
   const int sms = sm_count();
   if (sms <= 0) return 0;
   const int64_t pairs = static_cast<int64_t>(s.batch) * (s.nheads / 2);
