@@ -63,9 +63,9 @@ __global__ void __launch_bounds__(kThreads) chunk_cumsum_kernel(Dims d, const fl
   const float a_h = h < d.H ? A[h] : 0.f;
   const int per = P0 / 32;  // 2, 4 or 8 tokens per lane
   float carry = 0.f;        // sum of the chunk's earlier pieces
-  for (int t0 = c * Q; t0 < (c + 1) * Q; t0 += P0) {
-    // all of the block's loads first (P0 * 8 / 256 <= 8 per thread), then the stores to shared memory
-    float v[8];
+  // a piece's loads (P0 * 8 / 256 <= 8 per thread); the next piece's go out before this one is
+  // scanned
+  auto load_piece = [&](int t0, float (&v)[8]) {
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
       const int idx = threadIdx.x + k * kThreads;
@@ -73,6 +73,14 @@ __global__ void __launch_bounds__(kThreads) chunk_cumsum_kernel(Dims d, const fl
       const int tok = t0 + t;
       v[k] = (t < P0 && tok < d.L && h2 < d.H) ? dt[(static_cast<int64_t>(b) * d.L + tok) * d.H + h2] : 0.f;
     }
+  };
+  float vn[8];
+  load_piece(c * Q, vn);
+  for (int t0 = c * Q; t0 < (c + 1) * Q; t0 += P0) {
+    float v[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) v[k] = vn[k];
+    if (t0 + P0 < (c + 1) * Q) load_piece(t0 + P0, vn);
     __syncthreads();  // the previous piece's shared-memory reads are done
 #pragma unroll
     for (int k = 0; k < 8; ++k) {

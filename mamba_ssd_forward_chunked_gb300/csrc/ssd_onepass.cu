@@ -402,6 +402,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (w0 == 0 && fl == 0 && init)
           prefetch_l2_bulk(init + (static_cast<int64_t>(b) * d.H + 2 * pair) * d.P * d.N,
                            static_cast<uint32_t>(2 * d.P * d.N * sizeof(float)));
+        // a segment's entering state (both heads of the pair, bf16), likewise (not at dstate 256,
+        // where the schedule warp's registers would spill)
+        if (kPB && w0 > 0 && fl == 0 && seg_h)
+          prefetch_l2_bulk(seg_h + ((static_cast<int64_t>(b) * ((nw + R - 1) / R) + w0 / R) * d.H + 2 * pair) * d.P * d.N,
+                           static_cast<uint32_t>(2 * d.P * d.N * sizeof(__nv_bfloat16)));
         for (int w = w0; good && w < w1; ++w, ++n) {
           const int ts = n % kInfoRing;
           if (n >= kInfoRing && !mbar_wait_short(&tempty[ts], ((n / kInfoRing) - 1) & 1, spin_ns)) {
