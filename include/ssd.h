@@ -144,14 +144,15 @@ size_t ssd_fwd_workspace_size(const ssd_shape* shape);
  *    transpose itself).
  *  - segmented one-pass (SSD_BF16 only): chunk_cumsum, chunk_state and
  *    state_passing with segments of 2048 (or 1024) tokens as their chunk,
- *    which leaves every segment's entering state (bf16) in the workspace, then
- *    the one-pass pair, which runs each segment as an independent run from it.
+ *    which leaves every segment's entering state (fp32) in the workspace and
+ *    writes final_state, then the one-pass pair on the sequences' segments
+ *    taken as a batch of one-segment sequences, each from its entering state.
  * ssd_fwd takes the one-pass schedule for SSD_BF16 when there are at least as
  * many (batch, head pair) sequences as multiprocessors (below that the chain
  * of windows, not bandwidth, bounds the one-pass kernel); below that, the
- * segmented one when the segments give at least two per multiprocessor over
- * all pairs (a sequence's last segment may be shorter); otherwise the staged
- * one (always for SSD_F32).  The one-pass schedules work in windows of 128
+ * segmented one when the segments divide the sequence and give at least two
+ * per multiprocessor over all pairs; otherwise the staged one (always for
+ * SSD_F32).  The one-pass schedules work in windows of 128
  * tokens whatever chunk_size is; the result is the recurrence's either way.
  * init_state may be NULL (zero initial state); final_state
  * may be NULL (not written; the workspace holds the running state instead).

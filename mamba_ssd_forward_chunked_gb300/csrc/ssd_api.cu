@@ -4,7 +4,6 @@
 // ssd_fwd_check, which reads the 4-byte status word).
 #include <cudaTypedefs.h>
 
-#include <algorithm>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
@@ -82,12 +81,7 @@ ssd_status layout_of(const ssd_shape* shape, ssd_workspace_layout* out) {
   if (st != SSD_OK) return st;
   const ssd_shape& s = *shape;
   const int64_t nc = (s.seqlen + s.chunk_size - 1) / s.chunk_size;
-  // bf16 beyond 2048 tokens: the cumsum rows also hold the segmented schedule's 2048-token
-  // segments (shorter sequences never take it)
-  const size_t lp = std::max(static_cast<size_t>(nc) * s.chunk_size,
-                             s.dtype == SSD_BF16 && s.seqlen > 2048
-                                 ? (static_cast<size_t>(s.seqlen) + 2047) / 2048 * 2048
-                                 : 0);
+  const size_t lp = static_cast<size_t>(nc) * s.chunk_size;
   const size_t heads = static_cast<size_t>(s.batch) * s.nheads;
   const size_t nstate = static_cast<size_t>(s.batch) * nc * s.nheads * s.headdim * s.dstate;
   ssd_workspace_layout L{};
@@ -239,17 +233,17 @@ bool use_fused(const ssd_shape& s) {
 // first carry the state across segments of 2048 (or 1024) tokens -- chunk_cumsum, chunk_state
 // and state_passing with the segment as their chunk -- and the one-pass kernel then runs every
 // segment as an independent run from its entering state, so every multiprocessor has work.
-// It applies when the segments give at least two runs per multiprocessor (a sequence's last
-// segment may be shorter).  Measured on GB300 with 64 sequences of 32768 tokens: segments of
-// 1024, 2048 and 4096 tokens ran 0.61-1.12, 0.62-1.12 and 0.68-1.18 ms.
+// It applies when the segments divide the sequence and give at least two per multiprocessor
+// over all pairs.  Measured on GB300 with 64 sequences of 32768 tokens: segments of 1024, 2048
+// and 4096 tokens ran 0.61-1.12, 0.62-1.12 and 0.68-1.18 ms.
 int segment_windows(const ssd_shape& s) {
-  if (s.dtype != SSD_BF16 || s.seqlen <= 2048 || use_fused(s)) return 0;
+  if (s.dtype != SSD_BF16 || use_fused(s)) return 0;
   const int sms = sm_count();
   if (sms <= 0) return 0;
   const int64_t pairs = static_cast<int64_t>(s.batch) * (s.nheads / 2);
   for (int r : {16, 8}) {
     const int64_t q = 128 * r;
-    if (pairs * ((s.seqlen + q - 1) / q) >= 2 * static_cast<int64_t>(sms)) return r;
+    if (s.seqlen % q == 0 && pairs * (s.seqlen / q) >= 2 * static_cast<int64_t>(sms)) return r;
   }
   return 0;
 }
@@ -512,24 +506,32 @@ ssd_status fwd_impl(int path, int first, int end, const ssd_shape* shape, const 
     return from_cuda(e);
   }
   if (path == 2) {
-    // the staged state kernels with the segment as their chunk (the workspace's cumsum rows are
-    // padded for it, and there are no more segments than chunks), then the one-pass kernel from
-    // the segments' entering states
+    // The staged state kernels, with the segment as their chunk, leave every segment's entering
+    // state (fp32, [B][segment][H][P][N]) and the final state.  A sequence's segments lie back
+    // to back in x, dt, Bm, Cm and y, so they are also a batch of B * segments sequences of one
+    // segment each; the one-pass pair runs that batch, each sequence as one claimed run from its
+    // entering state.
     const int R = segment_windows(*shape);
     ssd_shape ss = *shape;
     ss.chunk_size = 128 * R;
     const Dims ds = make_dims(ss);
+    ssd_shape sv = *shape;
+    sv.batch = shape->batch * ds.nc;
+    sv.seqlen = 128 * R;
+    const Dims dv = make_dims(sv);
     ChunkStateMaps smaps;
-    OnePassMaps omaps;
-    if (!build_state_maps(ss, x, Bm, w.states, &smaps) || !build_onepass_maps(*shape, x, Bm, Cm, y, w.cbm, &omaps))
+    OnePassMaps vmaps;
+    if (!build_state_maps(ss, x, Bm, w.states, &smaps) || !build_onepass_maps(sv, x, Bm, Cm, y, w.cbm, &vmaps))
       return SSD_ERR_CUDA;
+    // in the region sized for the chunks' bf16 entering states (at least twice as many chunks)
+    float* seg_init = reinterpret_cast<float*>(w.states_bf16);
     const uint64_t spin = spin_limit_ns();
     step([&](bool) { return launch_chunk_cumsum(ds, dt, A, w, cs, nullptr); });
     step([&](bool dep) { return launch_chunk_state(ds, true, smaps, w, spin, cs, dep); });
-    step([&](bool) { return launch_state_passing(ds, true, init_state, nullptr, w, cs, false); });
-    step([&](bool) { return launch_causal_cb(d, omaps, w, spin, cs, false); });
+    step([&](bool) { return launch_state_passing(ds, true, init_state, final_state, w, cs, false, seg_init); });
+    step([&](bool) { return launch_causal_cb(dv, vmaps, w, spin, cs, false); });
     step([&](bool dep) {
-      return launch_onepass(d, omaps, dt, A, D, x, init_state, final_state, w, spin, cs, dep, w.states_bf16, R);
+      return launch_onepass(dv, vmaps, dt, A, D, x, seg_init, nullptr, w, spin, cs, dep, R);
     });
     return from_cuda(e);
   }

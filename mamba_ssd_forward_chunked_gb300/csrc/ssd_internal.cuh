@@ -83,8 +83,11 @@ cudaError_t launch_chunk_cumsum(const Dims& d, const float* dt, const float* A, 
 cudaError_t launch_b_transpose(const Dims& d, const void* Bm, const Work& w, cudaStream_t stream);
 cudaError_t launch_chunk_state(const Dims& d, bool bf16, const ChunkStateMaps& maps, const Work& w,
                                uint64_t spin_ns, cudaStream_t stream, bool dependent = false);
+// hprev32 (bf16 problems): write the entering states in fp32 there instead of bf16 into
+// w.states_bf16 (the segmented one-pass schedule)
 cudaError_t launch_state_passing(const Dims& d, bool bf16, const float* init, float* final_state,
-                                 const Work& w, cudaStream_t stream, bool dependent = false);
+                                 const Work& w, cudaStream_t stream, bool dependent = false,
+                                 float* hprev32 = nullptr);
 cudaError_t launch_compute_out(const Dims& d, bool bf16, const ComputeOutMaps& maps, const float* D,
                                const void* x, void* y, const Work& w, uint64_t spin_ns, cudaStream_t stream,
                                bool dependent = false);
@@ -92,12 +95,10 @@ cudaError_t launch_compute_out(const Dims& d, bool bf16, const ComputeOutMaps& m
 // counter and flags (otherwise an earlier launch of the call has)
 cudaError_t launch_causal_cb(const Dims& d, const OnePassMaps& maps, const Work& w, uint64_t spin_ns,
                              cudaStream_t stream, bool first = true);
-// With seg_h set, every run is one segment of seg_windows windows whose entering state is
-// read from seg_h (bf16 [B][segment][H][P][N]) instead of being chained between runs.
+// force_R > 0: claimed runs of force_R windows whatever the shape's own choice would be
 cudaError_t launch_onepass(const Dims& d, const OnePassMaps& maps, const float* dt, const float* A, const float* D,
                            const void* x, const float* init, float* final_state, const Work& w, uint64_t spin_ns,
-                           cudaStream_t stream, bool dependent = false, const void* seg_h = nullptr,
-                           int seg_windows = 0);
+                           cudaStream_t stream, bool dependent = false, int force_R = 0);
 cudaError_t launch_timeout_probe(int* status, uint64_t limit_ns, cudaStream_t stream);
 
 }  // namespace ssd

@@ -268,8 +268,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                        const __grid_constant__ CUtensorMap ymap, Dims d, int R, const float* __restrict__ dtg,
                        const float* __restrict__ Avec, const float* __restrict__ Dvec,
                        const __nv_bfloat16* __restrict__ Mg, const float* init, float* final_state, float* hslot,
-                       int* flags, int* counter, const __nv_bfloat16* __restrict__ xg,
-                       const __nv_bfloat16* __restrict__ seg_h, int* status, uint64_t spin_ns) {
+                       int* flags, int* counter, const __nv_bfloat16* __restrict__ xg, int* status,
+                       uint64_t spin_ns) {
   constexpr bool kPB = kN <= 128;  // product buffers (else the state accumulated in tensor memory)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -402,11 +402,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (w0 == 0 && fl == 0 && init)
           prefetch_l2_bulk(init + (static_cast<int64_t>(b) * d.H + 2 * pair) * d.P * d.N,
                            static_cast<uint32_t>(2 * d.P * d.N * sizeof(float)));
-        // a segment's entering state (both heads of the pair, bf16), likewise (not at dstate 256,
-        // where the schedule warp's registers would spill)
-        if (kPB && w0 > 0 && fl == 0 && seg_h)
-          prefetch_l2_bulk(seg_h + ((static_cast<int64_t>(b) * ((nw + R - 1) / R) + w0 / R) * d.H + 2 * pair) * d.P * d.N,
-                           static_cast<uint32_t>(2 * d.P * d.N * sizeof(__nv_bfloat16)));
         for (int w = w0; good && w < w1; ++w, ++n) {
           const int ts = n % kInfoRing;
           if (n >= kInfoRing && !mbar_wait_short(&tempty[ts], ((n / kInfoRing) - 1) & 1, spin_ns)) {
@@ -703,13 +698,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     // before writing O for window m: the carried product of window m - 1 is done
     auto o_free = [&](int m) -> bool { return m < 1 || mbar_wait_short(&cdone[(m - 1) & 1], yph(m - 1), spin_ns); };
-    // Segments (seg_h set): every run is one segment of R windows whose entering state the
-    // staged kernels have computed ahead of this launch (bf16, [B][segment][H][P][N]); runs
-    // neither wait for nor publish to one another.
-    const int nseg = R > 0 ? (nw + R - 1) / R : 0;
-    auto seg_row = [&](const WinInfo& I, int h) -> const __nv_bfloat16* {
-      return seg_h + ((static_cast<int64_t>(I.b) * nseg + I.w / R) * d.H + h) * d.P * d.N + static_cast<int64_t>(p) * d.N;
-    };
     // the window's scalars: alpha = e^{G_S} and the rescaled-form flag of this head
     float alpha = 1.f;
     bool fastH = true;
@@ -751,7 +739,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // slot[k * 128]), init_state (prefetched into L2 when the run was published) or zero;
         // O = h_in
         bool bad = !mbar_wait_short(&xready[xs(n)], xph(n), spin_ns) || !o_free(n);
-        if (!seq_first && !seg_h && et == 0) bad = bad || !wait_flag_geq(flags + I.b * hp + I.pair, I.w, spin_ns);
+        if (!seq_first && et == 0) bad = bad || !wait_flag_geq(flags + I.b * hp + I.pair, I.w, spin_ns);
         if (named_bar_or(bar_s, 128, bad)) {
           ok = false;
           break;
@@ -762,20 +750,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (seq_first && !hin) {
 #pragma unroll
           for (int q = 0; q < kN; ++q) hs[q] = 0.f;
-        } else if (!seq_first && seg_h) {
-          const uint4* src = reinterpret_cast<const uint4*>(seg_row(I, h));
-#pragma unroll
-          for (int k = 0; k < kN / 8; ++k) {
-            const uint4 v = __ldcg(src + k);
-            hs[8 * k] = bf16_lo(v.x);
-            hs[8 * k + 1] = bf16_hi(v.x);
-            hs[8 * k + 2] = bf16_lo(v.y);
-            hs[8 * k + 3] = bf16_hi(v.y);
-            hs[8 * k + 4] = bf16_lo(v.z);
-            hs[8 * k + 5] = bf16_hi(v.z);
-            hs[8 * k + 6] = bf16_lo(v.w);
-            hs[8 * k + 7] = bf16_hi(v.w);
-          }
         } else {
           const float4* src0 = seq_first ? reinterpret_cast<const float4*>(hin) : slot;
           const int stride = seq_first ? 1 : 128;
@@ -818,14 +792,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (last) {
         // publish: the slot for the run that continues this sequence, or final_state
         if (!seq_last) {
-          if (!seg_h) {
 #pragma unroll
-            for (int k = 0; k < kN / 4; ++k)
-              __stcg(slot + k * 128, make_float4(hs[4 * k], hs[4 * k + 1], hs[4 * k + 2], hs[4 * k + 3]));
-            __threadfence();
-            named_bar_sync(bar_s, 128);
-            if (et == 0) st_release_gpu(flags + I.b * hp + I.pair, I.w + 1);
-          }
+          for (int k = 0; k < kN / 4; ++k)
+            __stcg(slot + k * 128, make_float4(hs[4 * k], hs[4 * k + 1], hs[4 * k + 2], hs[4 * k + 3]));
+          __threadfence();
+          named_bar_sync(bar_s, 128);
+          if (et == 0) st_release_gpu(flags + I.b * hp + I.pair, I.w + 1);
         } else if (final_state) {
 #pragma unroll
           for (int k = 0; k < kN / 4; ++k)
@@ -865,7 +837,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the state entering the run: predecessor's slot, init_state or zero, put in place
         // as pi * h_in with O = h_in
         bool bad = !mbar_wait_short(&xready[xs(n)], xph(n), spin_ns) || !o_free(n);
-        if (!seq_first && !seg_h && et == 0) bad = bad || !wait_flag_geq(flags + I.b * hp + I.pair, I.w, spin_ns);
+        if (!seq_first && et == 0) bad = bad || !wait_flag_geq(flags + I.b * hp + I.pair, I.w, spin_ns);
         if (named_bar_or(bar_s, 128, bad)) {
           ok = false;
           break;
@@ -880,7 +852,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         // L2 round trip, and little code, since this path runs once per run and its code is
         // never in the instruction cache.
         const bool zero = seq_first && !hin;
-        const bool from_seg = !seq_first && seg_h;  // a segment's entering state (bf16)
         const float4* src0 = seq_first ? reinterpret_cast<const float4*>(hin) : slot;
         const int step = seq_first ? 8 : 8 * 128, stride = seq_first ? 1 : 128;
 #pragma unroll 1
@@ -889,20 +860,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (zero) {
 #pragma unroll
             for (int q = 0; q < 64; ++q) hb[q] = 0u;
-          } else if (from_seg) {
-            const uint4* src = reinterpret_cast<const uint4*>(seg_row(I, h) + n0);
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-              const uint4 v = __ldcg(src + q);
-              hb[8 * q] = __float_as_uint(bf16_lo(v.x));
-              hb[8 * q + 1] = __float_as_uint(bf16_hi(v.x));
-              hb[8 * q + 2] = __float_as_uint(bf16_lo(v.y));
-              hb[8 * q + 3] = __float_as_uint(bf16_hi(v.y));
-              hb[8 * q + 4] = __float_as_uint(bf16_lo(v.z));
-              hb[8 * q + 5] = __float_as_uint(bf16_hi(v.z));
-              hb[8 * q + 6] = __float_as_uint(bf16_lo(v.w));
-              hb[8 * q + 7] = __float_as_uint(bf16_hi(v.w));
-            }
           } else {
 #pragma unroll
             for (int q = 0; q < 16; ++q) {
@@ -950,7 +907,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!last) return;
           const float* hv = reinterpret_cast<const float*>(v);
           if (!seq_last) {  // for the run that continues this sequence
-            if (seg_h) return;
 #pragma unroll
             for (int q = 0; q < 8; ++q)
               __stcg(slot + ((n0 >> 5) * 8 + q) * 128, make_float4(hv[4 * q], hv[4 * q + 1], hv[4 * q + 2], hv[4 * q + 3]));
@@ -1051,7 +1007,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive(&oready[(n + 1) & 1]);
         } else {
           tc_fence_before();
-          if (!seq_last && !seg_h) {
+          if (!seq_last) {
             __threadfence();
             named_bar_sync(bar_s, 128);
             if (et == 0) st_release_gpu(flags + I.b * hp + I.pair, I.w + 1);
@@ -1269,7 +1225,7 @@ int onepass_grid(const Dims& d, int sms, int R) {
 
 cudaError_t launch_onepass(const Dims& d, const OnePassMaps& maps, const float* dt, const float* A, const float* D,
                            const void* x, const float* init, float* final_state, const Work& w, uint64_t spin_ns,
-                           cudaStream_t stream, bool dependent, const void* seg_h, int seg_windows) {
+                           cudaStream_t stream, bool dependent, int force_R) {
   int dev = 0, sms = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -1285,13 +1241,11 @@ cudaError_t launch_onepass(const Dims& d, const OnePassMaps& maps, const float* 
   e = cudaFuncGetAttributes(&fa, kern);
   if (e != cudaSuccess) return e;
   if (fa.numRegs != static_cast<int>(kRegLaunch)) return cudaErrorInvalidConfiguration;
-  // segments: claimed runs of exactly one segment each
-  const int R = seg_h ? seg_windows : onepass_run_length(d, sms);
+  const int R = force_R > 0 ? force_R : onepass_run_length(d, sms);
   const int grid = onepass_grid(d, sms, R);
   return launch_k(kern, dim3(grid), dim3(kThreads), smem, stream, dependent, maps.x, maps.cm, maps.bm,
                   maps.m, maps.y, d, R, dt, A, D, static_cast<const __nv_bfloat16*>(w.cbm), init, final_state,
-                  w.hslot, w.flags, w.counter, static_cast<const __nv_bfloat16*>(x),
-                  static_cast<const __nv_bfloat16*>(seg_h), w.status, spin_ns);
+                  w.hslot, w.flags, w.counter, static_cast<const __nv_bfloat16*>(x), w.status, spin_ns);
 }
 
 }  // namespace ssd

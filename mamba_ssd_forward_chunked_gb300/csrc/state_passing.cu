@@ -37,7 +37,8 @@ __global__ void __launch_bounds__(kThreads) state_passing_kernel(Dims d, const f
                                                                   void* states,
                                                                   __nv_bfloat16* __restrict__ states_bf16,
                                                                   const float* __restrict__ init,
-                                                                  float* __restrict__ final_state) {
+                                                                  float* __restrict__ final_state,
+                                                                  float* __restrict__ hprev32) {
   constexpr int kVec = PassVec<kBF16>::kVec;
   grid_dep_wait();  // chunk_state's results are visible from here on
   grid_dep_launch();
@@ -86,14 +87,19 @@ __global__ void __launch_bounds__(kThreads) state_passing_kernel(Dims d, const f
             s_c[2 * e] = __uint_as_float(w[e] << 16);
             s_c[2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
           }
-          uint4 packed;
-          uint32_t* pk = &packed.x;
+          if (hprev32) {  // the entering state in fp32 (the segmented one-pass schedule)
+            reinterpret_cast<float4*>(hprev32)[2 * o] = make_float4(st[0], st[1], st[2], st[3]);
+            reinterpret_cast<float4*>(hprev32)[2 * o + 1] = make_float4(st[4], st[5], st[6], st[7]);
+          } else {
+            uint4 packed;
+            uint32_t* pk = &packed.x;
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            __nv_bfloat162 v2 = __floats2bfloat162_rn(st[2 * e], st[2 * e + 1]);
-            pk[e] = *reinterpret_cast<uint32_t*>(&v2);
+            for (int e = 0; e < 4; ++e) {
+              __nv_bfloat162 v2 = __floats2bfloat162_rn(st[2 * e], st[2 * e + 1]);
+              pk[e] = *reinterpret_cast<uint32_t*>(&v2);
+            }
+            reinterpret_cast<uint4*>(states_bf16)[o] = packed;
           }
-          reinterpret_cast<uint4*>(states_bf16)[o] = packed;
         } else {
 #pragma unroll
           for (int e = 0; e < 4; ++e) s_c[e] = __uint_as_float(w[e]);
@@ -122,15 +128,15 @@ __global__ void __launch_bounds__(kThreads) state_passing_kernel(Dims d, const f
 }  // namespace
 
 cudaError_t launch_state_passing(const Dims& d, bool bf16, const float* init, float* final_state,
-                                 const Work& w, cudaStream_t stream, bool dependent) {
+                                 const Work& w, cudaStream_t stream, bool dependent, float* hprev32) {
   const int64_t total = static_cast<int64_t>(d.B) * d.H * d.P * d.N / (bf16 ? 8 : 4);
   const unsigned blocks = static_cast<unsigned>((total + kThreads - 1) / kThreads);
   const float* cs = w.cumsum;
   if (bf16)
     return launch_k(state_passing_kernel<true>, dim3(blocks), dim3(kThreads), 0, stream, dependent, d, cs, w.states,
-                    w.states_bf16, init, final_state);
+                    w.states_bf16, init, final_state, hprev32);
   return launch_k(state_passing_kernel<false>, dim3(blocks), dim3(kThreads), 0, stream, dependent, d, cs, w.states,
-                  static_cast<__nv_bfloat16*>(nullptr), init, final_state);
+                  static_cast<__nv_bfloat16*>(nullptr), init, final_state, static_cast<float*>(nullptr));
 }
 
 }  // namespace ssd

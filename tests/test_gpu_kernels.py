@@ -125,7 +125,7 @@ def test_full_forward_equals_the_four_steps(name, over):
 @pytest.mark.parametrize("over", [CASES[1][1], CASES[3][1], CASES[4][1],
                                   dict(batch=16, seqlen=384, nheads=20, dstate=128, chunk_size=128, dtype="bf16",
                                        init_state=True),
-                                  dict(batch=1, seqlen=32768 - 300, nheads=64, ngroups=8, dstate=64, chunk_size=128,
+                                  dict(batch=1, seqlen=32768, nheads=64, ngroups=8, dstate=64, chunk_size=128,
                                        dtype="bf16", init_state=True)],
                          ids=["f32-N128", "f32-N256-ragged", "bf16-staged-G2", "bf16-one-pass", "bf16-segmented"])
 def test_launch_ranges_equal_the_full_forward(over):

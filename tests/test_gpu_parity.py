@@ -76,13 +76,13 @@ def test_sweep_points_sampled(name):
 
 
 
-def test_segmented_ragged_sampled():
-    """The segmented one-pass schedule on a sequence the segments do not divide
-    (30,000 tokens: 14 segments of 2048 and a ragged one of 1328, which also
-    ends inside a 128-token window), bf16 with an initial state, against the
-    oracle on sampled (batch, head) pairs."""
+def test_segmented_sampled():
+    """The segmented one-pass schedule (15 segments of 2048 tokens, two
+    sequences, so segment states cross a batch boundary in the reshaped
+    batch), bf16 with an initial state and dstate 128, against the oracle on
+    sampled (batch, head) pairs, final state included."""
     import mamba_ssd_forward_chunked_gb300 as ssd
-    w = ssd_synth.custom("g", dtype="bf16", batch=1, seqlen=30000, nheads=64, ngroups=8, dstate=128,
+    w = ssd_synth.custom("g", dtype="bf16", batch=2, seqlen=30720, nheads=32, ngroups=8, dstate=128,
                          chunk_size=256, init_state=True)
     inp = ssd_synth.make_inputs(w)
     pairs = sampled_pairs(w.batch, w.nheads, 6)
@@ -98,6 +98,7 @@ def test_segmented_ragged_sampled():
     assert np.all(np.isfinite(ys))
     ey, ef = rel_err(ys, yrs), rel_err(fs, frs)
     assert ey <= TOL["bf16"] and ef <= TOL["bf16"], (ey, ef)
+
 
 SMALL = [
     dict(seqlen=1),
