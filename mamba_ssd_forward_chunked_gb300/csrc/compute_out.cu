@@ -48,10 +48,10 @@
 // log2(e), and keeps the last X block of its head until the epilogue: it reads
 // x_i (for D*x) from it, overwrites it with y in the same swizzled layout and
 // writes y out with TMA tensor stores, so no global load or scattered store
-// sits on its critical path.  TF32 operands must be K-major in shared memory (an MN-major
-// TF32 operand read back as zeros in a layout probe on this part), so in the
-// fp32 path each warpgroup first transposes its X block (eight 32 x 32 boxes)
-// in place; bf16 reads X MN-major.  Every wait is bounded; on expiry the CTA
+// sits on its critical path.  X is the intra product's MN-major B operand in both
+// precisions: bf16 as one 64-p box in the 128-byte swizzle, fp32 as two 32-p boxes in
+// the 128-byte swizzle of 32-byte atoms (the layout the tensor core reads an MN-major
+// TF32 operand in; TMA writes it).  Every wait is bounded; on expiry the CTA
 // records SSD_ERR_DEVICE_TIMEOUT, stops, frees its tensor memory and exits.
 #include "ptx.cuh"
 #include "ssd_internal.cuh"
@@ -189,17 +189,25 @@ __device__ __forceinline__ void causal_strip(uint32_t (&v)[32], int j0, int i, u
   }
 }
 
+// 16-byte piece k (values 4k .. 4k + 3) of row r of a 32-p fp32 box: in the
+// 32-byte-atom swizzle, 32-byte chunk k / 2 of the row sits at (k / 2) ^ (r % 4).
+__device__ __forceinline__ int a32_piece(int k, int r) { return (((k >> 1) ^ (r & 3)) << 1) | (k & 1); }
+
 // Copies token r's raw x row (64 values, or zeros) over its rescaled copy in
-// the X block, in the layout the epilogue reads: TF32 boxes (r / 32, half)
-// after the transpose, bf16 row r (128-byte swizzle).  Only thread r touches
-// these bytes.
+// the X block, in the layout the epilogue reads: TF32 row r of the two 32-p
+// boxes (32-byte-atom swizzle), bf16 row r (128-byte swizzle).  Only thread r
+// touches these bytes.
 template <bool kTF32, typename T>
 __device__ __noinline__ void restore_x_row(uint8_t* xy, int r, const T* src) {
   if constexpr (kTF32) {
     for (int half = 0; half < 2; ++half) {
-      uint8_t* bx = xy + (r >> 5) * 8192 + half * 4096;
-      for (int q = 0; q < 32; ++q)
-        *reinterpret_cast<float*>(bx + box_t_offset(r & 31, q)) = src ? static_cast<float>(src[32 * half + q]) : 0.f;
+      float4* row = reinterpret_cast<float4*>(xy + half * 16384 + r * 128);
+      for (int k = 0; k < 8; ++k) {
+        const int q = 32 * half + 4 * k;
+        row[a32_piece(k, r)] = src ? make_float4(static_cast<float>(src[q]), static_cast<float>(src[q + 1]),
+                                                 static_cast<float>(src[q + 2]), static_cast<float>(src[q + 3]))
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
     }
   } else {
     for (int k = 0; k < 8; ++k)
@@ -307,12 +315,9 @@ __global__ void __launch_bounds__(OutCfg<T>::kThreads, 1)
               const int h = id.h0 + (nb - NB);
               mbar_arrive_expect_tx(&xfullb[s], static_cast<uint32_t>(C::kXBytes));
               if constexpr (C::kTF32) {
-                // 32 x 32 boxes at s * 8 KB + half * 4 KB: once transposed, each
-                // 32-token K block is one 64-row K-major tile
-                for (int sb = 0; sb < 4; ++sb)
-                  for (int hf = 0; hf < 2; ++hf)
-                    tma_load_3d(st + sb * 8192 + hf * 4096, &xmap, &xfullb[s], h * d.P + hf * 32,
-                                id.c * Q + jb * 128 + sb * 32, id.b);
+                // two 128-token boxes of 32 p, 16 KB apart (the operand's column blocks)
+                for (int hf = 0; hf < 2; ++hf)
+                  tma_load_3d(st + hf * 16384, &xmap, &xfullb[s], h * d.P + hf * 32, id.c * Q + jb * 128, id.b);
               } else {
                 tma_load_3d(st, &xmap, &xfullb[s], h * d.P, id.c * Q + jb * 128, id.b);
               }
@@ -327,7 +332,7 @@ __global__ void __launch_bounds__(OutCfg<T>::kThreads, 1)
       const uint32_t fmt = C::kTF32 ? 2u : 1u;
       const uint32_t id_yoff = idesc_f32acc(fmt, 128, 64, 0, 0);
       const uint32_t id_cb = idesc_f32acc(fmt, 128, 128, 0, 0);
-      const uint32_t id_yint = idesc_f32acc(fmt, 128, 64, 0, C::kTF32 ? 0u : 1u);
+      const uint32_t id_yint = idesc_f32acc(fmt, 128, 64, 0, 1u);
       int it = 0, xit = 0, ntd = 0, nm = 0;
       for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x, ++ntd) {
         const TileId id = decode_tile(tile, d, ntile);
@@ -374,7 +379,9 @@ __global__ void __launch_bounds__(OutCfg<T>::kThreads, 1)
             for (int k = 0; k < 128 / C::kKStepX; ++k) {
               uint64_t xd;
               if constexpr (C::kTF32) {
-                xd = sdesc_sw128(xb + (k >> 2) * 8192 + (k & 3) * 32, 16, 1024);  // X^T, K-major
+                // X, MN-major: a K step is 8 token rows of 128 B; LBO = the second 32-p box,
+                // SBO = 4-row groups
+                xd = sdesc_sw128_a32(xb + k * 1024, 16384, 512);
               } else {
                 xd = sdesc_sw128(xb + k * C::kKStepX * 128, 16384, 1024);  // X, MN-major (one 64-p atom)
               }
@@ -504,42 +511,30 @@ __global__ void __launch_bounds__(OutCfg<T>::kThreads, 1)
           ok = false;
           break;
         }
-        // X block landed (TF32 transposes it before its first use)
-        if (C::kTF32 && !mbar_wait(&xfullb[xs % C::kXStages], (xs / C::kXStages) & 1, spin_ns)) {
-          ok = false;
-          break;
-        }
-        if constexpr (C::kTF32) {
-          // flip this head's X block to K-major (eight boxes, two per round)
-          const int m = et & 63;
-#pragma unroll 1
-          for (int box0 = 0; box0 < 8; box0 += 2) {
-            const int bi = box0 + (et >> 6);
-            uint8_t* bp = xb + bi * 4096;
-            float4 v[4];
-            box_read_4x4(bp, m, v);
-            if (fast) {  // rescaled form: X^ = 2^(G_m - G_j) dt_j x_j (tokens 4a..4a+3 of the box)
-              const float* w = vref + jb * 128 + (bi >> 1) * 32 + 4 * (m >> 3);
+        if (fast) {  // rescaled form: X^ = 2^(G_m - G_j) dt_j x_j, rows scaled in place (row et = token et)
+          if (!mbar_wait(&xfullb[xs % C::kXStages], (xs / C::kXStages) & 1, spin_ns)) {
+            ok = false;
+            break;
+          }
+          const float wj = vref[jb * 128 + et];
+          if constexpr (C::kTF32) {
+            // 128 bytes of the row in each of the two 32-p boxes; the chunk order is rotated per
+            // row so that a warp's accesses spread over all banks (the scale is the same for all)
 #pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                v[q].x = clamp_finite(v[q].x * w[q]);
-                v[q].y = clamp_finite(v[q].y * w[q]);
-                v[q].z = clamp_finite(v[q].z * w[q]);
-                v[q].w = clamp_finite(v[q].w * w[q]);
+            for (int hf = 0; hf < 2; ++hf) {
+              float4* row = reinterpret_cast<float4*>(xb + hf * 16384 + et * 128);
+#pragma unroll
+              for (int k = 0; k < 8; ++k) {
+                float4* cp = row + (k ^ (et & 7));
+                float4 v = *cp;
+                v.x = clamp_finite(v.x * wj);
+                v.y = clamp_finite(v.y * wj);
+                v.z = clamp_finite(v.z * wj);
+                v.w = clamp_finite(v.w * wj);
+                *cp = v;
               }
             }
-            named_bar_sync(bar_id, 128);
-            box_write_4x4_transposed(bp, m, v);
-          }
-          fence_proxy_async_smem();
-        }
-        if constexpr (!C::kTF32) {
-          if (fast) {  // rescaled form: X^ rows scaled in place (row et = token et of the block)
-            if (!mbar_wait(&xfullb[xs % C::kXStages], (xs / C::kXStages) & 1, spin_ns)) {
-              ok = false;
-              break;
-            }
-            const float wj = vref[jb * 128 + et];
+          } else {
             uint4* row = reinterpret_cast<uint4*>(xb + et * 128);
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
@@ -551,8 +546,8 @@ __global__ void __launch_bounds__(OutCfg<T>::kThreads, 1)
               v.w = scale_bf16x2_clamped(v.w, wj);
               *cp = v;
             }
-            fence_proxy_async_smem();
           }
+          fence_proxy_async_smem();
         }
         // masked matrix, four 32-column strips; two TMEM loads in flight so the
         // next strip's load overlaps this strip's arithmetic
@@ -588,7 +583,7 @@ __global__ void __launch_bounds__(OutCfg<T>::kThreads, 1)
         mbar_arrive(&mready[hh]);
         ++nm;
         // this warpgroup's share of releasing the X block; the last one is kept for D*x
-        if (!C::kTF32 && !mbar_wait(&xfullb[xs % C::kXStages], (xs / C::kXStages) & 1, spin_ns)) {
+        if (!mbar_wait(&xfullb[xs % C::kXStages], (xs / C::kXStages) & 1, spin_ns)) {
           ok = false;
           break;
         }
@@ -637,20 +632,17 @@ __global__ void __launch_bounds__(OutCfg<T>::kThreads, 1)
       for (int half = 0; half < 2; ++half) {
         const uint32_t (&yv)[32] = yall[half];
         if constexpr (C::kTF32) {
-          // box (r / 32, half) holds x transposed (row = p); y goes back untransposed
-          // (row = token).  The box belongs to this warp alone, so a warp sync
-          // separates its reads from its writes.
-          uint8_t* bx = xy + (r >> 5) * 8192 + half * 4096;
-          float out[32];
+          // row r of box `half` holds x_r's 32 values (32-byte-atom swizzle); y_r goes in place
+          float4* row = reinterpret_cast<float4*>(xy + half * 16384 + r * 128);
 #pragma unroll
-          for (int q = 0; q < 32; ++q)
-            out[q] = ry * fmaf(kx, *reinterpret_cast<const float*>(bx + box_t_offset(r & 31, q)), __uint_as_float(yv[q]));
-          __syncwarp();
-          const int rr = r & 31;
-#pragma unroll
-          for (int k = 0; k < 8; ++k)
-            *reinterpret_cast<float4*>(bx + rr * 128 + ((k ^ (rr & 7)) << 4)) =
-                make_float4(out[4 * k], out[4 * k + 1], out[4 * k + 2], out[4 * k + 3]);
+          for (int k = 0; k < 8; ++k) {
+            float4* px = row + a32_piece(k, r);
+            const float4 xv = *px;
+            const int q = 4 * k;
+            *px = make_float4(ry * fmaf(kx, xv.x, __uint_as_float(yv[q])), ry * fmaf(kx, xv.y, __uint_as_float(yv[q + 1])),
+                              ry * fmaf(kx, xv.z, __uint_as_float(yv[q + 2])),
+                              ry * fmaf(kx, xv.w, __uint_as_float(yv[q + 3])));
+          }
         } else {
           // MN-major rows: token r is row r, p in 16-B chunks of 8 (in place)
 #pragma unroll
@@ -676,8 +668,8 @@ __global__ void __launch_bounds__(OutCfg<T>::kThreads, 1)
         const int tok0 = id.c * Q + id.t * 128;
         for (int sb = 0; sb < nbox; ++sb) {
           if constexpr (C::kTF32) {
-            tma_store_3d(&ymap, xy + sb * 8192, h * d.P, tok0 + 32 * sb, id.b);
-            tma_store_3d(&ymap, xy + sb * 8192 + 4096, h * d.P + 32, tok0 + 32 * sb, id.b);
+            tma_store_3d(&ymap, xy + sb * 4096, h * d.P, tok0 + 32 * sb, id.b);
+            tma_store_3d(&ymap, xy + 16384 + sb * 4096, h * d.P + 32, tok0 + 32 * sb, id.b);
           } else {
             tma_store_3d(&ymap, xy + sb * 4096, h * d.P, tok0 + 32 * sb, id.b);
           }

@@ -187,10 +187,26 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
   return d;
 }
 
+// The same descriptor for the 128-byte swizzle in 32-byte atoms (layout type 1): within each
+// 128-byte row, 32-byte chunk c sits at c ^ (row % 4), the pattern TMA writes with
+// CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B.  It is the layout an MN-major TF32 operand takes (the
+// 16-byte-chunk swizzle above does not serve TF32 MN-major: the product read zeros).  For an
+// MN-major operand, `lbo` is the stride between 128-byte column blocks along M/N and `sbo` the
+// stride between 4-row groups along K (512 bytes when the rows are dense).
+__device__ __forceinline__ uint64_t sdesc_sw128_a32(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(1) << 61;  // SWIZZLE_128B_BASE32B
+  return d;
+}
+
 // Instruction descriptor for kind::f16 / kind::tf32 with an fp32 accumulator.
 // fmt: 0 = f16, 1 = bf16, 2 = tf32 (same for A and B).  *_mn = 1 selects the
-// MN-major (transposed) shared-memory layout for that operand (used for bf16
-// only: TF32 operands are kept K-major).
+// MN-major (transposed) shared-memory layout for that operand (TF32 MN-major
+// operands use the 32-byte-atom swizzle of sdesc_sw128_a32).
 __host__ __device__ constexpr uint32_t idesc_f32acc(uint32_t fmt, uint32_t M, uint32_t N, uint32_t a_mn,
                                                     uint32_t b_mn) {
   return (1u << 4) | (fmt << 7) | (fmt << 10) | (a_mn << 15) | (b_mn << 16) | ((N >> 3) << 17) |

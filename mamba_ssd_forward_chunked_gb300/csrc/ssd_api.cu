@@ -44,15 +44,17 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// Tiled map with a 128-byte swizzle, zero fill outside the tensor.
+// Tiled map with a 128-byte swizzle (16-byte chunks, or 32-byte chunks for the MN-major TF32
+// operands), zero fill outside the tensor.
 bool encode(CUtensorMap* m, bool bf16, int rank, const void* base, const uint64_t* dims,
-            const uint64_t* strides_bytes, const uint32_t* box) {
+            const uint64_t* strides_bytes, const uint32_t* box,
+            CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   auto fn = encode_fn();
   if (!fn) return false;
   const uint32_t estr[5] = {1, 1, 1, 1, 1};
   CUresult r = fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
                   static_cast<cuuint32_t>(rank), const_cast<void*>(base), dims, strides_bytes, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -194,11 +196,13 @@ bool build_out_maps(const ssd_shape& s, const void* x, const void* Bm, const voi
     const uint64_t hp = static_cast<uint64_t>(s.nheads) * s.headdim;
     const uint64_t dims[3] = {hp, static_cast<uint64_t>(s.seqlen), static_cast<uint64_t>(s.batch)};
     const uint64_t str[2] = {hp * es, hp * es * s.seqlen};
-    // bf16: one 128-token x 64-p box per block; fp32: 32 x 32 boxes (transposed in shared memory)
-    const uint32_t box[3] = {atom, bf16 ? 128u : 32u, 1};
-    if (!encode(&m->x, bf16, 3, x, dims, str, box)) return false;
+    // one 128-token box per 128-byte column of the block (bf16: 64 p, fp32: 32 p); fp32 tiles
+    // take the 32-byte-atom swizzle, the layout of an MN-major TF32 operand
+    const CUtensorMapSwizzle sw = bf16 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B;
+    const uint32_t box[3] = {atom, 128u, 1};
+    if (!encode(&m->x, bf16, 3, x, dims, str, box, sw)) return false;
     const uint32_t ybox[3] = {atom, 32u, 1};
-    if (!encode(&m->y, bf16, 3, y, dims, str, ybox)) return false;
+    if (!encode(&m->y, bf16, 3, y, dims, str, ybox, sw)) return false;
   }
   return true;
 }
