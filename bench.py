@@ -222,7 +222,7 @@ def whole_job_tokens_per_s(tokens_per_rank: int, world: int, ms: float) -> float
 
 # ------------------------------------------------------------------ GPU arm
 
-SHARED_HEADERS = ("ptx.cuh", "ssd_internal.cuh", "tile_transpose.cuh")
+SHARED_HEADERS = ("ptx.cuh", "ssd_internal.cuh")
 
 
 def kernel_source_digest(kernel: str, root: str = None) -> str:

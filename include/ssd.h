@@ -96,12 +96,6 @@ typedef struct {
  *               for every 128-token window and group the causal select of
  *               C B^T, M[i][j] = c_i . b_j for j <= i and 0 above the
  *               diagonal (one-pass schedule, written by its first step)
- *   bT          (SSD_F32 only) fp32, B*G*Lp*N values: Bm in 4 KB boxes of 32
- *               tokens x 32 dstate, transposed (a row is one dstate index),
- *               rounded to TF32 and 128-byte swizzled -- the K-major operand
- *               layout chunk_state's tensor cores read -- as
- *               [B][G][Lp/32][N/32][box]; written once per call and shared by
- *               every head of the group
  * nc = ceil(seqlen / chunk_size), Lp = nc * chunk_size. */
 typedef struct {
   size_t status;
@@ -111,7 +105,6 @@ typedef struct {
   size_t states_bf16;
   size_t chain;
   size_t hslot;
-  size_t bT;
   size_t cbm;
   size_t total;
 } ssd_workspace_layout;
@@ -138,10 +131,7 @@ size_t ssd_fwd_workspace_size(const ssd_shape* shape);
  *    and intra-window products and y; the state moves between windows in
  *    tensor memory and between runs of windows through the workspace (or
  *    final_state).  x is read once and the states never reach HBM.
- *  - staged: chunk_cumsum, chunk_state, state_passing and compute_out
- *    (SSD_F32: the chunk_cumsum launch also transposes Bm into the workspace,
- *    once for every head of a group; ssd_chunk_state called alone does that
- *    transpose itself).
+ *  - staged: chunk_cumsum, chunk_state, state_passing and compute_out.
  *  - segmented one-pass (SSD_BF16 only): chunk_cumsum, chunk_state and
  *    state_passing with segments of 2048 (or 1024) tokens as their chunk,
  *    which leaves every segment's entering state (fp32) in the workspace and

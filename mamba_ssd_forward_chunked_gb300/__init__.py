@@ -46,7 +46,7 @@ class ssd_shape(ctypes.Structure):
 class ssd_workspace_layout(ctypes.Structure):
     _fields_ = [("status", ctypes.c_size_t), ("cumsum", ctypes.c_size_t), ("dt_t", ctypes.c_size_t),
                 ("states", ctypes.c_size_t), ("states_bf16", ctypes.c_size_t), ("chain", ctypes.c_size_t),
-                ("hslot", ctypes.c_size_t), ("bT", ctypes.c_size_t), ("cbm", ctypes.c_size_t),
+                ("hslot", ctypes.c_size_t), ("cbm", ctypes.c_size_t),
                 ("total", ctypes.c_size_t)]
 
 
@@ -191,9 +191,7 @@ def workspace_views(shape: ssd_shape, ws: torch.Tensor) -> Dict[str, torch.Tenso
     out["chain"] = view(L["chain"], 1 + B * (H // 2), torch.int32, (1 + B * (H // 2),))
     out["hslot"] = view(L["hslot"], B * H * P * N, torch.float32, (B * H * P * N,))
     G = shape.ngroups
-    if shape.dtype != SSD_BF16:  # Bm in 4 KB TF32 boxes, [B][G][Lp/32][N/32][box]
-        out["bT"] = view(L["bT"], B * G * Lp * N, torch.float32, (B * G * Lp * N,))
-    else:  # causal C B^T per (batch, 128-token window, group)
+    if shape.dtype == SSD_BF16:  # causal C B^T per (batch, 128-token window, group)
         nw = -(-shape.seqlen // 128)
         out["cbm"] = view(L["cbm"], B * nw * G * 128 * 128, torch.bfloat16, (B, nw, G, 128, 128))
     return out

@@ -14,13 +14,8 @@
 // head's Q values with one warp (serial runs per lane + a warp-shuffle scan of
 // the run totals) and writes cumsum and dt as contiguous [B][H][Lp] rows.
 // Tokens past L read as dt = 0, so the cumsum stays flat in a ragged last chunk.
-//
-// fp32 problems append to the same grid the blocks that put Bm in chunk_state's
-// K-major TF32 layout (one per 32-token stage and (batch, group)): the two jobs
-// are independent, and one launch keeps a kernel boundary off the path.
 #include "ptx.cuh"
 #include "ssd_internal.cuh"
-#include "tile_transpose.cuh"
 
 namespace ssd {
 namespace {
@@ -32,18 +27,11 @@ __global__ void __launch_bounds__(kThreads) chunk_cumsum_kernel(Dims d, const fl
                                                                  const float* __restrict__ A,
                                                                  float* __restrict__ cumsum,
                                                                  float* __restrict__ dt_t, int* status,
-                                                                 int* chain, int nchain, int ncum,
-                                                                 const float* __restrict__ Bm,
-                                                                 float* __restrict__ bT) {
+                                                                 int* chain, int nchain) {
   __shared__ float s_dt[kHeadsPerBlock * 257];
   __shared__ float s_g[kHeadsPerBlock * 257];
   grid_dep_launch();  // the next kernel may start its prologue while this one runs
   const int blk = blockIdx.x;
-  if (blk >= ncum) {  // Bm transpose block
-    const int j = blk - ncum, stages = d.Lp / 32;
-    b_transpose_stage(Bm, bT, d.L, d.G, d.N, d.Lp, j % stages, j / stages, threadIdx.x);
-    return;
-  }
   const int Q = d.Q;
   // a chunk longer than 256 tokens (the one-pass schedule's segments) goes in pieces of 256,
   // the running sum carried from piece to piece
@@ -129,13 +117,11 @@ __global__ void __launch_bounds__(kThreads) chunk_cumsum_kernel(Dims d, const fl
 }  // namespace
 
 cudaError_t launch_chunk_cumsum(const Dims& d, const float* dt, const float* A, const Work& w,
-                                cudaStream_t stream, const void* Bm) {
+                                cudaStream_t stream) {
   const int64_t ncum = static_cast<int64_t>(d.nc) * ((d.H + kHeadsPerBlock - 1) / kHeadsPerBlock) * d.B;
-  const int64_t ntr = Bm ? static_cast<int64_t>(d.Lp / 32) * d.B * d.G : 0;
-  if (ncum + ntr > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
-  chunk_cumsum_kernel<<<static_cast<unsigned>(ncum + ntr), kThreads, 0, stream>>>(
-      d, dt, A, w.cumsum, w.dt_t, w.status, w.counter, 1 + d.B * (d.H / 2), static_cast<int>(ncum),
-      static_cast<const float*>(Bm), w.bT);
+  if (ncum > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
+  chunk_cumsum_kernel<<<static_cast<unsigned>(ncum), kThreads, 0, stream>>>(
+      d, dt, A, w.cumsum, w.dt_t, w.status, w.counter, 1 + d.B * (d.H / 2));
   return cudaGetLastError();
 }
 

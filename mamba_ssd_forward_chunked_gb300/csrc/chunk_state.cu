@@ -23,17 +23,16 @@
 // the swizzle never moves data across rows.  The fp32 accumulator lives in
 // tensor memory (dstate columns) and is drained by tcgen05.ld.
 //
-// fp32 inputs run the MMA as TF32, whose shared-memory operands must be
-// K-major.  B arrives K-major (transposed once per group by the Bm transpose
-// blocks).  For x there are two forms.  While dstate plus one 32-column slot
-// per ring stage fits in 256 tensor-memory columns (dstate <= 128; two CTAs per
-// SM still fit), each thread reads its (head, p) row's 32 tokens from the
-// landed box, scales and rounds them and stores them to tensor memory, where
-// the MMA takes them as its A operand: shared memory then carries the TMA
-// writes, one read of x and the MMA's B reads, about two thirds of the traffic
-// of the in-place form.  At dstate 256 each 32-token x 32-element box is
-// transposed in place in shared memory instead (scaled and rounded on the
-// way).  bf16 keeps the MN-major tiles and only scales.
+// fp32 inputs run the MMA as TF32.  An MN-major TF32 operand is read in the
+// 128-byte swizzle of 32-byte atoms, so the fp32 tensor maps write that layout
+// and both operands stay MN-major, as in bf16.  For x there are two forms.
+// While dstate plus one 32-column slot per ring stage fits in 256 tensor-memory
+// columns (dstate <= 128; two CTAs per SM still fit), each thread reads its
+// (head, p) row's 32 tokens from the landed box, scales and rounds them and
+// stores them to tensor memory, where the MMA takes them as its A operand:
+// shared memory then carries the TMA writes, one read of x and the MMA's B
+// reads, about two thirds of the traffic of the in-place form.  At dstate 256
+// the x boxes are scaled (and rounded to TF32) in place, as bf16 does.
 //
 // Warp roles (192 threads): warp 0 issues TMA, warp 1 owns TMEM and issues
 // the MMAs (one thread), warps 2-5 compute the weights, transform each stage
@@ -42,7 +41,6 @@
 // (device-timeout status, no hang).
 #include "ptx.cuh"
 #include "ssd_internal.cuh"
-#include "tile_transpose.cuh"
 
 namespace ssd {
 namespace {
@@ -65,19 +63,6 @@ __host__ __device__ inline uint32_t state_stage_bytes(int N, int atom, int box, 
   return static_cast<uint32_t>(abytes + (N / atom) * box);
 }
 
-// fp32 problems: Bm in the K-major TF32 box layout, once per (batch, group).
-// Every head of a group multiplies by the same B, so its transpose (and TF32
-// rounding) is done once here instead of in each head pair's CTA.  The full
-// forward runs the same stages inside the chunk_cumsum launch; this kernel
-// serves the standalone chunk_state step.  One CTA per (32-token stage,
-// batch * group).
-constexpr int kBtThreads = 256;
-
-__global__ void __launch_bounds__(kBtThreads) b_transpose_kernel(Dims d, const float* __restrict__ Bm,
-                                                                  float* __restrict__ bT) {
-  b_transpose_stage(Bm, bT, d.L, d.G, d.N, d.Lp, blockIdx.x, blockIdx.y, threadIdx.x);
-}
-
 // Stages that fit the ring budget (2..4).
 __host__ __device__ inline int state_stages(uint32_t stage_bytes, int ring_bytes, int max_stages) {
   const int n = ring_bytes / static_cast<int>(stage_bytes);
@@ -88,8 +73,7 @@ template <typename T>
 __global__ void __launch_bounds__(StateCfg<T>::kThreads, 2)
     chunk_state_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap bmap,
                        const __grid_constant__ CUtensorMap smap, Dims d, const float* __restrict__ cumsum,
-                       const float* __restrict__ dt_t, const float* __restrict__ bT, int* status,
-                       uint64_t spin_ns) {
+                       const float* __restrict__ dt_t, int* status, uint64_t spin_ns) {
   using C = StateCfg<T>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -163,21 +147,14 @@ __global__ void __launch_bounds__(StateCfg<T>::kThreads, 2)
         const int tok = c * Q + it * C::kTokens;
         for (int k = 0; k < C::kABoxes; ++k)
           tma_load_3d(sa + k * C::kBox, &xmap, &full[s], h0 * d.P + k * C::kAtom, tok, b);
-        if constexpr (C::kTF32) {  // B already transposed: the stage's boxes are contiguous
-          const uint8_t* src = reinterpret_cast<const uint8_t*>(bT) +
-                               ((static_cast<int64_t>(b) * d.G + g) * (d.Lp / 32) + tok / 32) * bBoxes * C::kBox;
-          bulk_g2s(sb, src, static_cast<uint32_t>(bBoxes * C::kBox), &full[s]);
-        } else {
-          for (int k = 0; k < bBoxes; ++k)
-            tma_load_4d(sb + k * C::kBox, &bmap, &full[s], k * C::kAtom, g, tok, b);
-        }
+        for (int k = 0; k < bBoxes; ++k)
+          tma_load_4d(sb + k * C::kBox, &bmap, &full[s], k * C::kAtom, g, tok, b);
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      // bf16: both operands MN-major; TF32: both K-major after the transpose
-      const uint32_t mn = C::kTF32 ? 0u : 1u;
-      const uint32_t idesc = idesc_f32acc(C::kTF32 ? 2u : 1u, 128u, static_cast<uint32_t>(N), mn, mn);
+      // both operands MN-major (A from tensor memory in the TF32 form that puts it there)
+      const uint32_t idesc = idesc_f32acc(C::kTF32 ? 2u : 1u, 128u, static_cast<uint32_t>(N), ts ? 0u : 1u, 1u);
       for (int it = 0; it < nstages; ++it) {
         const int s = it % NS, r = it / NS;
         if (!mbar_wait(&scaled[s], r & 1, spin_ns)) {
@@ -191,15 +168,15 @@ __global__ void __launch_bounds__(StateCfg<T>::kThreads, 2)
         for (int k = 0; k < C::kTokens / C::kKStep; ++k) {
           uint64_t ad, bd;
           if constexpr (C::kTF32) {
-            // K-major, 128-B swizzle: rows of 32 tokens; a K step of 8 tokens
-            // is 32 B along the row; SBO = 1024 B between 8-row groups.
-            bd = sdesc_sw128(sb + k * 32, 16, 1024);
+            // MN-major, 128-B swizzle of 32-B atoms: a K step is 8 token rows (1 KB);
+            // LBO = stride between 32-element column blocks (one TMA box), SBO = 4-row groups.
+            bd = sdesc_sw128_a32(sb + k * 1024, C::kBox, 512);
             if (ts) {  // A: the stage's tensor-memory slot, one column per token
               mma_ts<true>(tmem, tmem + a_col + static_cast<uint32_t>(s * C::kTokens + k * C::kKStep), bd, idesc,
                            (it | k) != 0 ? 1u : 0u);
               continue;
             }
-            ad = sdesc_sw128(sa + k * 32, 16, 1024);
+            ad = sdesc_sw128_a32(sa + k * 1024, C::kBox, 512);
           } else {
             // MN-major, 128-B swizzle: LBO = stride between 128-B atom columns
             // (one TMA box), SBO = stride between 8-row groups along K.
@@ -223,45 +200,37 @@ __global__ void __launch_bounds__(StateCfg<T>::kThreads, 2)
       uint8_t* sa = smem + s * stage_bytes;
       if (ts) {
         // thread = row quad * 32 + lane of M = (head in pair, p): box `quad` holds its 32
-        // tokens as one 4-byte column (conflict-free: a warp reads one 128-B row at a time)
+        // tokens as one 4-byte column (conflict-free: a warp reads one 128-B row at a time;
+        // value `lane` of row j sits in 32-byte chunk (lane / 8) ^ (j % 4))
         const int quad = warp & 3;
         const uint8_t* bp = sa + quad * C::kBox;
         const float* w = w_s + (quad >> 1) * Q + it * C::kTokens;
         uint32_t v[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
-          const float xv = *reinterpret_cast<const float*>(bp + j * 128 + ((((lane >> 2) ^ (j & 7)) << 4) |
-                                                                                ((lane & 3) << 2)));
+          const float xv = *reinterpret_cast<const float*>(bp + j * 128 + ((((lane >> 3) ^ (j & 3)) << 5) |
+                                                                                ((lane & 7) << 2)));
           v[j] = __float_as_uint(round_tf32(xv * w[j]));
         }
         tmem_st32(tmem + (static_cast<uint32_t>(quad * 32) << 16) + a_col + static_cast<uint32_t>(s * C::kTokens), v);
         tmem_st_wait();
         tc_fence_before();
       } else if constexpr (C::kTF32) {
-        // two boxes per round: the A boxes (x, scaled by w); B arrives transposed
-        const int nboxes = C::kABoxes;
-        const int m = et & 63;
-        for (int box0 = 0; box0 < nboxes; box0 += 2) {
-          const int box = box0 + (et >> 6);
-          uint8_t* bp = sa + box * C::kBox;
-          float4 v[4];
-          box_read_4x4(bp, m, v);
-          if (box < C::kABoxes) {
-            const float* w = w_s + (box >> 1) * Q + it * C::kTokens + 4 * (m >> 3);
+        // x scaled in place: thread = token row (et % 32) of A box et / 32 (32 p of one head);
+        // the row's 16-byte chunks go in a per-row rotated order so that a warp's accesses
+        // spread over all banks (one scale for the whole row)
+        const int box = et >> 5, row = et & 31;
+        const float w = w_s[(box >> 1) * Q + it * C::kTokens + row];
+        float4* rp = reinterpret_cast<float4*>(sa + box * C::kBox + row * 128);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              v[q].x = round_tf32(v[q].x * w[q]); v[q].y = round_tf32(v[q].y * w[q]);
-              v[q].z = round_tf32(v[q].z * w[q]); v[q].w = round_tf32(v[q].w * w[q]);
-            }
-          } else {
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              v[q].x = round_tf32(v[q].x); v[q].y = round_tf32(v[q].y);
-              v[q].z = round_tf32(v[q].z); v[q].w = round_tf32(v[q].w);
-            }
-          }
-          named_bar_sync(1, 128);  // the round's boxes are fully read before any write
-          box_write_4x4_transposed(bp, m, v);
+        for (int k = 0; k < 8; ++k) {
+          float4* cp = rp + (k ^ (row & 7));
+          float4 v = *cp;
+          v.x = round_tf32(v.x * w);
+          v.y = round_tf32(v.y * w);
+          v.z = round_tf32(v.z * w);
+          v.w = round_tf32(v.w * w);
+          *cp = v;
         }
       } else {
         constexpr int kChunks = C::kABytes / 16;
@@ -366,16 +335,10 @@ cudaError_t launch_impl(const Dims& d, const ChunkStateMaps& maps, const Work& w
   }
   const dim3 grid(d.H / 2, d.nc, d.B);
   return launch_k(chunk_state_kernel<T>, grid, dim3(C::kThreads), smem, stream, dependent, maps.x, maps.bm, maps.s, d,
-                  static_cast<const float*>(w.cumsum), static_cast<const float*>(w.dt_t),
-                  static_cast<const float*>(w.bT), w.status, spin_ns);
+                  static_cast<const float*>(w.cumsum), static_cast<const float*>(w.dt_t), w.status, spin_ns);
 }
 
 }  // namespace
-
-cudaError_t launch_b_transpose(const Dims& d, const void* Bm, const Work& w, cudaStream_t stream) {
-  b_transpose_kernel<<<dim3(d.Lp / 32, d.B * d.G), kBtThreads, 0, stream>>>(d, static_cast<const float*>(Bm), w.bT);
-  return cudaGetLastError();
-}
 
 cudaError_t launch_chunk_state(const Dims& d, bool bf16, const ChunkStateMaps& maps, const Work& w,
                                uint64_t spin_ns, cudaStream_t stream, bool dependent) {

@@ -55,7 +55,6 @@
 // records SSD_ERR_DEVICE_TIMEOUT, stops, frees its tensor memory and exits.
 #include "ptx.cuh"
 #include "ssd_internal.cuh"
-#include "tile_transpose.cuh"
 
 namespace ssd {
 namespace {

@@ -312,6 +312,14 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // ------------------------------------------------------------------ misc
+// fp32 rounded to the nearest TF32 value (ties away from zero), the operand
+// precision of the kind::tf32 MMA.
+__device__ __forceinline__ float round_tf32(float f) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(f));
+  return __uint_as_float(r);
+}
+
 // 2^x with the hardware approximation (PTX ex2.approx.ftz.f32: relative error
 // about 2^-22).  Callers keep the exponent below 128 so the result is finite.
 __device__ __forceinline__ float fast_exp2(float x) {

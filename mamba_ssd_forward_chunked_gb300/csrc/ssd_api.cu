@@ -102,8 +102,6 @@ ssd_status layout_of(const ssd_shape* shape, ssd_workspace_layout* out) {
   off = align_up(off + (1 + heads / 2) * sizeof(int));
   L.hslot = off;
   off = align_up(off + heads * s.headdim * s.dstate * sizeof(float));
-  L.bT = off;
-  if (s.dtype == SSD_F32) off = align_up(off + static_cast<size_t>(s.batch) * s.ngroups * lp * s.dstate * sizeof(float));
   L.cbm = off;
   if (s.dtype == SSD_BF16) {
     const size_t nwin = static_cast<size_t>((s.seqlen + 127) / 128);
@@ -126,7 +124,6 @@ Work carve(void* ws, const ssd_workspace_layout& L, bool bf16) {
   w.flags = w.counter + 1;
   w.hslot = reinterpret_cast<float*>(p + L.hslot);
   w.cbm = bf16 ? static_cast<void*>(p + L.cbm) : nullptr;
-  w.bT = bf16 ? nullptr : reinterpret_cast<float*>(p + L.bT);
   return w;
 }
 
@@ -147,11 +144,13 @@ bool build_state_maps(const ssd_shape& s, const void* x, const void* Bm, const v
   const uint64_t es = esize(s);
   const uint32_t atom = static_cast<uint32_t>(128 / es);
   const uint64_t hp = static_cast<uint64_t>(s.nheads) * s.headdim;
+  // the MMA operands (x, Bm) are MN-major: fp32 tiles in the 32-byte-atom swizzle TF32 needs
+  const CUtensorMapSwizzle sw = bf16 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B;
   {
     const uint64_t dims[3] = {hp, static_cast<uint64_t>(s.seqlen), static_cast<uint64_t>(s.batch)};
     const uint64_t str[2] = {hp * es, hp * es * s.seqlen};
     const uint32_t box[3] = {atom, 32, 1};
-    if (!encode(&m->x, bf16, 3, x, dims, str, box)) return false;
+    if (!encode(&m->x, bf16, 3, x, dims, str, box, sw)) return false;
   }
   {
     const uint64_t gn = static_cast<uint64_t>(s.ngroups) * s.dstate;
@@ -159,7 +158,7 @@ bool build_state_maps(const ssd_shape& s, const void* x, const void* Bm, const v
                               static_cast<uint64_t>(s.seqlen), static_cast<uint64_t>(s.batch)};
     const uint64_t str[3] = {s.dstate * es, gn * es, gn * es * s.seqlen};
     const uint32_t box[4] = {atom, 1, 32, 1};
-    if (!encode(&m->bm, bf16, 4, Bm, dims, str, box)) return false;
+    if (!encode(&m->bm, bf16, 4, Bm, dims, str, box, sw)) return false;
   }
   {
     const int64_t nc = (s.seqlen + s.chunk_size - 1) / s.chunk_size;
@@ -359,8 +358,7 @@ ssd_status ssd_chunk_state(const ssd_shape* shape, const void* x, const void* Bm
   if (!build_state_maps(*shape, x, Bm, w.states, &maps)) return SSD_ERR_CUDA;
   const Dims d = make_dims(*shape);
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = bf16 ? cudaSuccess : launch_b_transpose(d, Bm, w, cs);
-  if (e == cudaSuccess) e = launch_chunk_state(d, bf16, maps, w, spin_limit_ns(), cs);
+  cudaError_t e = launch_chunk_state(d, bf16, maps, w, spin_limit_ns(), cs);
   return from_cuda(e);
 }
 
@@ -530,7 +528,7 @@ ssd_status fwd_impl(int path, int first, int end, const ssd_shape* shape, const 
     // in the region sized for the chunks' bf16 entering states (at least twice as many chunks)
     float* seg_init = reinterpret_cast<float*>(w.states_bf16);
     const uint64_t spin = spin_limit_ns();
-    step([&](bool) { return launch_chunk_cumsum(ds, dt, A, w, cs, nullptr); });
+    step([&](bool) { return launch_chunk_cumsum(ds, dt, A, w, cs); });
     step([&](bool dep) { return launch_chunk_state(ds, true, smaps, w, spin, cs, dep); });
     step([&](bool) { return launch_state_passing(ds, true, init_state, final_state, w, cs, false, seg_init); });
     step([&](bool) { return launch_causal_cb(dv, vmaps, w, spin, cs, false); });
@@ -546,7 +544,7 @@ ssd_status fwd_impl(int path, int first, int end, const ssd_shape* shape, const 
     return SSD_ERR_CUDA;
   const uint64_t spin = spin_limit_ns();
   // fp32: the chunk_cumsum launch also transposes Bm once for every head of its group
-  step([&](bool) { return launch_chunk_cumsum(d, dt, A, w, cs, bf16 ? nullptr : Bm); });
+  step([&](bool) { return launch_chunk_cumsum(d, dt, A, w, cs); });
   // chunk_state and compute_out are programmatic dependents of the kernel before them (their
   // launch and prologue overlap its tail).  state_passing is one only while chunk_state runs
   // in a single wave (two CTAs per SM): launched early beside a later wave, its blocks slowed

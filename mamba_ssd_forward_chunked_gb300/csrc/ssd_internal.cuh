@@ -29,7 +29,6 @@ struct Work {
   int* counter;                // one-pass kernel: tile counter
   int* flags;                  // one-pass kernel: [B][H/2] windows published
   float* hslot;                // one-pass kernel: states at run boundaries (its own layout)
-  float* bT;                   // fp32 problems: Bm as K-major TF32 boxes for chunk_state, or null
   void* cbm;                   // bf16 problems: causal C B^T per (batch, 128-token window, group), or null
 };
 
@@ -75,12 +74,8 @@ cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t sme
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
-// With Bm non-null (fp32 problems) the same launch also writes Bm into the workspace's
-// K-major TF32 box layout (w.bT) that chunk_state reads.
 cudaError_t launch_chunk_cumsum(const Dims& d, const float* dt, const float* A, const Work& w,
-                                cudaStream_t stream, const void* Bm = nullptr);
-// fp32 problems: the same Bm layout alone, for the standalone chunk_state step.
-cudaError_t launch_b_transpose(const Dims& d, const void* Bm, const Work& w, cudaStream_t stream);
+                                cudaStream_t stream);
 cudaError_t launch_chunk_state(const Dims& d, bool bf16, const ChunkStateMaps& maps, const Work& w,
                                uint64_t spin_ns, cudaStream_t stream, bool dependent = false);
 // hprev32 (bf16 problems): write the entering states in fp32 there instead of bf16 into

@@ -76,9 +76,7 @@ def test_workspace_layout(ext):
             assert lay["states_bf16"] - lay["states"] >= 2 * nc * 32 * 64 * 128 * es
             extra = 2 * nc * 32 * 64 * 128 * 2 if dt == ext.SSD_BF16 else 0
             assert lay["total"] >= lay["states_bf16"] + extra
-            # fp32: room for Bm as transposed TF32 boxes (B * G * Lp * N floats), bf16: none
-            bT = 2 * 1 * Lp * 128 * 4 if dt == ext.SSD_F32 else 0
-            assert lay["cbm"] - lay["bT"] >= bT and lay["bT"] >= lay["hslot"] + 2 * 32 * 64 * 128 * 4
+            assert lay["cbm"] >= lay["hslot"] + 2 * 32 * 64 * 128 * 4
             # bf16: the causal C B^T block of every (batch, 128-token window, group)
             cbm = 2 * (-(-L // 128)) * 1 * 128 * 128 * 2 if dt == ext.SSD_BF16 else 0
             assert lay["total"] - lay["cbm"] >= cbm
@@ -124,7 +122,7 @@ def test_empty_batch_needs_no_device(ext):
     n = ext.ssd_fwd_workspace_size(s)
     assert ext.lib.ssd_fwd(ctypes.byref(s), None, None, None, None, None, None, None, None, None, ws, n, None) == 0
     assert ext.ssd_fwd_kernel_count(s) == 0
-    assert ext.ssd_fwd_kernel_count(shape(ext)) == 4  # fp32 staged: the Bm transpose rides in chunk_cumsum
+    assert ext.ssd_fwd_kernel_count(shape(ext)) == 4  # fp32 staged
     assert ext.ssd_fwd_kernel_count(shape(ext, dtype=ext.SSD_BF16, dstate=256)) == 4  # bf16 staged
 
 
@@ -146,7 +144,6 @@ def test_workspace_views_are_disjoint_and_inside(ext):
             spans.sort()
             for (a0, a1, na), (b0, b1, nb) in zip(spans, spans[1:]):
                 assert a1 <= b0, (na, nb)
-            assert ("bT" in dict((n, 1) for _, _, n in spans)) == (dt == ext.SSD_F32)
             assert ("cbm" in dict((n, 1) for _, _, n in spans)) == (dt == ext.SSD_BF16)
 
 

@@ -99,9 +99,9 @@ def test_compute_out_causal_upper_triangle_is_exactly_zero():
 @pytest.mark.parametrize("name,over", [CASES[1], CASES[3], CASES[5]], ids=[CASES[1][0], CASES[3][0], CASES[5][0]])
 def test_full_forward_equals_the_four_steps(name, over):
     """ssd_fwd on the staged schedule (fp32 inputs; bf16 at dstate 256) gives
-    bit for bit what the four step calls give in order: the full forward folds
-    the fp32 Bm transpose into the chunk_cumsum launch and chains the kernels
-    with programmatic dependent launch, and neither may change a result."""
+    bit for bit what the four step calls give in order: the full forward chains
+    the kernels with programmatic dependent launch, which may not change a
+    result."""
     ssd, w, inp, d, shape, ws = _setup(over)
     assert ssd.ssd_fwd_kernel_count(shape) == 4
     B, L, H = inp["dt"].shape
@@ -118,8 +118,6 @@ def test_full_forward_equals_the_four_steps(name, over):
     torch.cuda.synchronize()
     assert torch.equal(y1, y2)
     assert torch.equal(f1, f2)
-    if w.dtype == "f32":
-        assert torch.equal(ssd.workspace_views(shape, ws)["bT"], ssd.workspace_views(shape, ws2)["bT"])
 
 
 @pytest.mark.parametrize("over", [CASES[1][1], CASES[3][1], CASES[4][1],
