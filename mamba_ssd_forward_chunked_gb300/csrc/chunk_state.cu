@@ -25,14 +25,8 @@
 //
 // fp32 inputs run the MMA as TF32.  An MN-major TF32 operand is read in the
 // 128-byte swizzle of 32-byte atoms, so the fp32 tensor maps write that layout
-// and both operands stay MN-major, as in bf16.  For x there are two forms.
-// While dstate plus one 32-column slot per ring stage fits in 256 tensor-memory
-// columns (dstate <= 128; two CTAs per SM still fit), each thread reads its
-// (head, p) row's 32 tokens from the landed box, scales and rounds them and
-// stores them to tensor memory, where the MMA takes them as its A operand:
-// shared memory then carries the TMA writes, one read of x and the MMA's B
-// reads, about two thirds of the traffic of the in-place form.  At dstate 256
-// the x boxes are scaled (and rounded to TF32) in place, as bf16 does.
+// and both operands stay MN-major, as in bf16; the x boxes are scaled (and
+// rounded to TF32) in place.
 //
 // Warp roles (192 threads): warp 0 issues TMA, warp 1 owns TMEM and issues
 // the MMAs (one thread), warps 2-5 compute the weights, transform each stage
@@ -93,11 +87,7 @@ __global__ void __launch_bounds__(StateCfg<T>::kThreads, 2)
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(accum + 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nstages = Q / C::kTokens;
-  // TF32 with the x operand in tensor memory: the accumulator's N columns, then one
-  // 32-column slot per ring stage
-  const bool ts = C::kTF32 && N + NS * C::kTokens <= 256;
-  const uint32_t a_col = static_cast<uint32_t>(N);
-  const uint32_t tmem_cols = ts ? 256u : static_cast<uint32_t>(N);
+  const uint32_t tmem_cols = static_cast<uint32_t>(N);  // the accumulator
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
@@ -153,8 +143,8 @@ __global__ void __launch_bounds__(StateCfg<T>::kThreads, 2)
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      // both operands MN-major (A from tensor memory in the TF32 form that puts it there)
-      const uint32_t idesc = idesc_f32acc(C::kTF32 ? 2u : 1u, 128u, static_cast<uint32_t>(N), ts ? 0u : 1u, 1u);
+      // both operands MN-major
+      const uint32_t idesc = idesc_f32acc(C::kTF32 ? 2u : 1u, 128u, static_cast<uint32_t>(N), 1u, 1u);
       for (int it = 0; it < nstages; ++it) {
         const int s = it % NS, r = it / NS;
         if (!mbar_wait(&scaled[s], r & 1, spin_ns)) {
@@ -170,13 +160,8 @@ __global__ void __launch_bounds__(StateCfg<T>::kThreads, 2)
           if constexpr (C::kTF32) {
             // MN-major, 128-B swizzle of 32-B atoms: a K step is 8 token rows (1 KB);
             // LBO = stride between 32-element column blocks (one TMA box), SBO = 4-row groups.
-            bd = sdesc_sw128_a32(sb + k * 1024, C::kBox, 512);
-            if (ts) {  // A: the stage's tensor-memory slot, one column per token
-              mma_ts<true>(tmem, tmem + a_col + static_cast<uint32_t>(s * C::kTokens + k * C::kKStep), bd, idesc,
-                           (it | k) != 0 ? 1u : 0u);
-              continue;
-            }
             ad = sdesc_sw128_a32(sa + k * 1024, C::kBox, 512);
+            bd = sdesc_sw128_a32(sb + k * 1024, C::kBox, 512);
           } else {
             // MN-major, 128-B swizzle: LBO = stride between 128-B atom columns
             // (one TMA box), SBO = stride between 8-row groups along K.
@@ -198,24 +183,7 @@ __global__ void __launch_bounds__(StateCfg<T>::kThreads, 2)
         break;
       }
       uint8_t* sa = smem + s * stage_bytes;
-      if (ts) {
-        // thread = row quad * 32 + lane of M = (head in pair, p): box `quad` holds its 32
-        // tokens as one 4-byte column (conflict-free: a warp reads one 128-B row at a time;
-        // value `lane` of row j sits in 32-byte chunk (lane / 8) ^ (j % 4))
-        const int quad = warp & 3;
-        const uint8_t* bp = sa + quad * C::kBox;
-        const float* w = w_s + (quad >> 1) * Q + it * C::kTokens;
-        uint32_t v[32];
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const float xv = *reinterpret_cast<const float*>(bp + j * 128 + ((((lane >> 3) ^ (j & 3)) << 5) |
-                                                                                ((lane & 7) << 2)));
-          v[j] = __float_as_uint(round_tf32(xv * w[j]));
-        }
-        tmem_st32(tmem + (static_cast<uint32_t>(quad * 32) << 16) + a_col + static_cast<uint32_t>(s * C::kTokens), v);
-        tmem_st_wait();
-        tc_fence_before();
-      } else if constexpr (C::kTF32) {
+      if constexpr (C::kTF32) {
         // x scaled in place: thread = token row (et % 32) of A box et / 32 (32 p of one head);
         // the row's 16-byte chunks go in a per-row rotated order so that a warp's accesses
         // spread over all banks (one scale for the whole row)
