@@ -74,6 +74,9 @@ struct OutCfg {
   static constexpr int kWgFloats = 3 * 256;  // per warpgroup: cumsum, dt, strip factors for 256 columns
 };
 
+static_assert(OutCfg<float>::kOffH1 == OutCfg<float>::kOffH0 + 64 * 128,
+              "the pair's entering-state slices must be adjacent (one N = 128 carried-state product)");
+
 constexpr float kSpan = 100.f;  // rescaled form: log2 bound on the diagonal block's decay
 
 // Register split (setmaxnreg): 384 threads launch with kRegLaunch each (12 warps, three per
@@ -329,7 +332,9 @@ __global__ void __launch_bounds__(OutCfg<T>::kThreads, 1)
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       const uint32_t fmt = C::kTF32 ? 2u : 1u;
-      const uint32_t id_yoff = idesc_f32acc(fmt, 128, 64, 0, 0);
+      // the carried-state term of both heads in one product: the pair's entering states sit
+      // back to back in the stage (rows = (head, p)), and so do Y_h0 and Y_h1 in tensor memory
+      const uint32_t id_yoff = idesc_f32acc(fmt, 128, 128, 0, 0);
       const uint32_t id_cb = idesc_f32acc(fmt, 128, 128, 0, 0);
       const uint32_t id_yint = idesc_f32acc(fmt, 128, 64, 0, 1u);
       int it = 0, xit = 0, ntd = 0, nm = 0;
@@ -355,11 +360,8 @@ __global__ void __launch_bounds__(OutCfg<T>::kThreads, 1)
               // K-major, 128-B swizzle: a K step is 32 B along the row; SBO = 1024 B
               const uint64_t ad = sdesc_sw128(st + C::kOffC + k * 32, 16, 1024);
               const uint32_t acc = (nb | k) != 0 ? 1u : 0u;
-              if (jb == 0) {
+              if (jb == 0)
                 mma_ss<C::kTF32>(tmem + C::kColY0, ad, sdesc_sw128(st + C::kOffH0 + k * 32, 16, 1024), id_yoff, acc);
-                mma_ss<C::kTF32>(tmem + C::kColY0 + 64, ad, sdesc_sw128(st + C::kOffH1 + k * 32, 16, 1024), id_yoff,
-                                 acc);
-              }
               mma_ss<C::kTF32>(tmem + C::kColCB, ad, sdesc_sw128(st + C::kOffB + k * 32, 16, 1024), id_cb, acc);
             }
             mma_commit(&empty[s]);
