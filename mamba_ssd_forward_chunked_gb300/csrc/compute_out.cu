@@ -22,9 +22,12 @@
 //     Y_h  += M_h X_h,jb                                     (A = M_h from TMEM)
 //     y_i   = Y_h[i] + D_h x_i
 //
-// Tensor memory (512 columns): [0,128) CB (fp32), [128,256) M_h0, [256,384)
-// M_h1 (TF32: 128 columns; bf16: packed pairs in the first 64), [384,448)
-// Y_h0, [448,512) Y_h1.  The exponentials are factored so that every factor
+// Tensor memory (512 columns): [0,128) CB (fp32), [128,192) Y_h0, [192,256)
+// Y_h1, [256,384) M_h0, [384,512) M_h1 (TF32: 128 columns; bf16: packed pairs
+// in the first 64).  In the first column block CB and both carried-state terms
+// are one N = 256 product per K step: the stage holds B_jb's rows and then the
+// pair's entering-state rows back to back, and CB, Y_h0, Y_h1 are adjacent
+// columns.  The exponentials are factored so that every factor
 // is <= 1: for a 32-column strip entirely left of row i,
 // exp(G_i - G_j) = exp(G_i - G_e) exp(G_e - G_j) with e the strip's last
 // column; only the 32 x 32 blocks on the diagonal take one exp per element,
@@ -70,12 +73,14 @@ struct OutCfg {
   static constexpr int kXStages = kTF32 ? 2 : 4;                                   // X ring
   static constexpr int kKStepX = kTF32 ? 8 : 16;                                   // tokens per intra MMA
   static constexpr int kThreads = 384;
-  static constexpr uint32_t kColCB = 0, kColM0 = 128, kColY0 = 384, kTmemCols = 512;
+  static constexpr uint32_t kColCB = 0, kColY0 = 128, kColM0 = 256, kTmemCols = 512;
   static constexpr int kWgFloats = 3 * 256;  // per warpgroup: cumsum, dt, strip factors for 256 columns
 };
 
-static_assert(OutCfg<float>::kOffH1 == OutCfg<float>::kOffH0 + 64 * 128,
-              "the pair's entering-state slices must be adjacent (one N = 128 carried-state product)");
+static_assert(OutCfg<float>::kOffH0 == OutCfg<float>::kOffB + 128 * 128 &&
+                  OutCfg<float>::kOffH1 == OutCfg<float>::kOffH0 + 64 * 128 &&
+                  OutCfg<float>::kColY0 == OutCfg<float>::kColCB + 128,
+              "B_jb's and the entering states' slices, and CB and Y, must be adjacent (one N = 256 product)");
 
 constexpr float kSpan = 100.f;  // rescaled form: log2 bound on the diagonal block's decay
 
@@ -332,9 +337,8 @@ __global__ void __launch_bounds__(OutCfg<T>::kThreads, 1)
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       const uint32_t fmt = C::kTF32 ? 2u : 1u;
-      // the carried-state term of both heads in one product: the pair's entering states sit
-      // back to back in the stage (rows = (head, p)), and so do Y_h0 and Y_h1 in tensor memory
-      const uint32_t id_yoff = idesc_f32acc(fmt, 128, 128, 0, 0);
+      // first column block: C [B_jb; h_h0; h_h1]^T -> [CB | Y_h0 | Y_h1] in one product
+      const uint32_t id_cby = idesc_f32acc(fmt, 128, 256, 0, 0);
       const uint32_t id_cb = idesc_f32acc(fmt, 128, 128, 0, 0);
       const uint32_t id_yint = idesc_f32acc(fmt, 128, 64, 0, 1u);
       int it = 0, xit = 0, ntd = 0, nm = 0;
@@ -360,9 +364,8 @@ __global__ void __launch_bounds__(OutCfg<T>::kThreads, 1)
               // K-major, 128-B swizzle: a K step is 32 B along the row; SBO = 1024 B
               const uint64_t ad = sdesc_sw128(st + C::kOffC + k * 32, 16, 1024);
               const uint32_t acc = (nb | k) != 0 ? 1u : 0u;
-              if (jb == 0)
-                mma_ss<C::kTF32>(tmem + C::kColY0, ad, sdesc_sw128(st + C::kOffH0 + k * 32, 16, 1024), id_yoff, acc);
-              mma_ss<C::kTF32>(tmem + C::kColCB, ad, sdesc_sw128(st + C::kOffB + k * 32, 16, 1024), id_cb, acc);
+              mma_ss<C::kTF32>(tmem + C::kColCB, ad, sdesc_sw128(st + C::kOffB + k * 32, 16, 1024),
+                               jb == 0 ? id_cby : id_cb, acc);
             }
             mma_commit(&empty[s]);
           }
