@@ -1,9 +1,10 @@
 #!/usr/bin/env python3
 """Throughput of the Mamba-2 chunked SSD forward pass on GB300.
 
-One step = one ssd_fwd call (the schedule it picks for the shape: chunk_cumsum
-then the one-pass kernel, or chunk_cumsum -> chunk_state -> state_passing ->
-compute_out) over one batch of seeded synthetic inputs already resident in HBM.
+One step = one ssd_fwd call (the schedule it picks for the shape: causal_cb then
+the one-pass kernel; chunk_state -> state_passing -> compute_out; or the staged
+state kernels over long segments, then the one-pass pair) over one batch of
+seeded synthetic inputs already resident in HBM.
 Prints ONE JSON line (rank 0).  The default workload is the 2.7B-layer shape
 (bf16, batch 4 x 4096 tokens, 80 heads, dstate 128).
 
@@ -46,7 +47,7 @@ PRE_STEP_SLEEP_CYCLES = 200_000
 # GB300's nominal dense tensor-core rates: TF32 1.1 PFLOP/s against bf16 2.25 PFLOP/s.  Used only
 # when the live measurement below cannot run.
 NOMINAL_TF32_OVER_BF16 = 1.1 / 2.25
-KERNELS = ("chunk_cumsum", "chunk_state", "state_passing", "compute_out")  # staged schedule
+KERNELS = ("chunk_state", "state_passing", "compute_out")  # staged schedule (chunk_state forms the cumsum)
 FUSED_KERNELS = ("causal_cb", "ssd_onepass")                                 # one-pass schedule
 # segmented one-pass schedule: the staged state kernels over segments, then the one-pass pair
 SEGMENTED_KERNELS = ("chunk_cumsum", "chunk_state", "state_passing", "causal_cb", "ssd_onepass")
@@ -83,8 +84,9 @@ def kernel_model(w: ssd_synth.Workload):
     f_state = B * nc * H * 2 * Q * N * P
     f_cb = B * nc * G * N * Q * (Q + 1)
     return {
+        # segmented schedule only; on the staged one chunk_state reads dt and A itself
         "chunk_cumsum": {"bytes": by["dt"] + by["AD"] // 2, "flops": 0},
-        "chunk_state": {"bytes": by["x"] + by["BmCm"] // 2, "flops": f_state},
+        "chunk_state": {"bytes": by["x"] + by["BmCm"] // 2 + by["dt"] + by["AD"] // 2, "flops": f_state},
         "state_passing": {"bytes": by["final"] + by["init"], "flops": 0},
         "compute_out": {"bytes": by["x"] + by["y"] + by["BmCm"] + by["AD"] // 2, "flops": flops - f_state},
         # one-pass schedule: the causal C B^T blocks (Bm, Cm read), then everything of the step

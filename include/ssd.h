@@ -87,7 +87,7 @@ typedef struct {
  *               chunk, rounded to bf16 for the output kernel's tensor cores
  *   chain       int32 [1 + B*H/2]  one-pass kernel: tile counter, then per
  *               (batch, head pair) the number of windows whose state is
- *               published (cleared by chunk_cumsum)
+ *               published (cleared by the call's first kernel)
  *   hslot       fp32, B*H*P*N values  one-pass kernel: the state handed from
  *               one run of windows to the next, per head pair in a layout of
  *               its own ([N/32][8][2*P rows][4]: a warp's 16-byte accesses are
@@ -131,7 +131,9 @@ size_t ssd_fwd_workspace_size(const ssd_shape* shape);
  *    and intra-window products and y; the state moves between windows in
  *    tensor memory and between runs of windows through the workspace (or
  *    final_state).  x is read once and the states never reach HBM.
- *  - staged: chunk_cumsum, chunk_state, state_passing and compute_out.
+ *  - staged: chunk_state (which forms each chunk's cumsum itself, exactly as
+ *    chunk_cumsum does, and writes the cumsum and dt_t rows), state_passing and
+ *    compute_out.
  *  - segmented one-pass (SSD_BF16 only): chunk_cumsum, chunk_state and
  *    state_passing with segments of 2048 (or 1024) tokens as their chunk,
  *    which leaves every segment's entering state (fp32) in the workspace and
@@ -197,7 +199,8 @@ ssd_status ssd_fwd_range(const ssd_shape* shape, const void* x, const float* dt,
 ssd_status ssd_fwd_check(const void* workspace);
 
 /* --- The four steps, callable one by one (for SSD_F32, ssd_fwd computes
- * exactly what these four calls in order compute; for SSD_BF16 the four calls in order give the
+ * exactly what these four calls in order compute -- its chunk_state launch
+ * forms the step-1 rows itself; for SSD_BF16 the four calls in order give the
  * same result as ssd_fwd through the staged path).  Each reads and writes the
  * workspace regions named. ---- */
 
@@ -237,7 +240,7 @@ ssd_status ssd_compute_out(const ssd_shape* shape, const void* x, const void* Bm
 ssd_status ssd_debug_timeout_probe(void* workspace, uint32_t limit_us, ssd_stream_t stream);
 
 /* Number of kernels ssd_fwd enqueues for `shape` (0 for an empty input): 2
- * on the one-pass schedule, 5 on the segmented one and 4 on the staged one. */
+ * on the one-pass schedule, 5 on the segmented one and 3 on the staged one. */
 int ssd_fwd_kernel_count(const ssd_shape* shape);
 
 /* Bytes of the device array that ssd_fwd_static_scratch uses as its workspace. */

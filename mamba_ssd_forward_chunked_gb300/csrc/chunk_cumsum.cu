@@ -14,6 +14,9 @@
 // head's Q values with one warp (serial runs per lane + a warp-shuffle scan of
 // the run totals) and writes cumsum and dt as contiguous [B][H][Lp] rows.
 // Tokens past L read as dt = 0, so the cumsum stays flat in a ragged last chunk.
+// The staged schedule's chunk_state forms the same rows itself (chunk_scan.cuh);
+// this kernel serves the segmented schedule's segments and the step-by-step API.
+#include "chunk_scan.cuh"
 #include "ptx.cuh"
 #include "ssd_internal.cuh"
 
@@ -78,29 +81,13 @@ __global__ void __launch_bounds__(kThreads) chunk_cumsum_kernel(Dims d, const fl
     }
     __syncthreads();
 
-    float run[8];
-    float acc = 0.f;
+    float dv[8], g[8];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      if (k < per) {
-        acc += s_dt[hh * ld + lane * per + k] * a_h;
-        run[k] = acc;
-      }
-    }
-    float incl = acc;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const float u = __shfl_up_sync(0xffffffffu, incl, off);
-      if (lane >= off) incl += u;
-    }
-    // exclusive prefix = the previous lane's inclusive one (not incl - acc): each G_t is then
-    // computed from tokens <= t only, so later tokens cannot change it even by rounding
-    float excl = __shfl_up_sync(0xffffffffu, incl, 1);
-    if (lane == 0) excl = 0.f;
+    for (int k = 0; k < 8; ++k) dv[k] = k < per ? s_dt[hh * ld + lane * per + k] : 0.f;
+    cumsum_piece(dv, per, a_h, carry, g);
 #pragma unroll
     for (int k = 0; k < 8; ++k)
-      if (k < per) s_g[hh * ld + lane * per + k] = run[k] + excl + carry;
-    carry += __shfl_sync(0xffffffffu, incl, 31);
+      if (k < per) s_g[hh * ld + lane * per + k] = g[k];
     __syncthreads();
 
     for (int idx = threadIdx.x; idx < kHeadsPerBlock * P0; idx += kThreads) {

@@ -33,6 +33,7 @@
 // and write S_c.  A ring of 2-4 stages (as many as fit 96 KB; mbarriers full ->
 // scaled -> empty) pipelines the 32-token stages.  All waits are bounded
 // (device-timeout status, no hang).
+#include "chunk_scan.cuh"
 #include "ptx.cuh"
 #include "ssd_internal.cuh"
 
@@ -66,8 +67,9 @@ __host__ __device__ inline int state_stages(uint32_t stage_bytes, int ring_bytes
 template <typename T>
 __global__ void __launch_bounds__(StateCfg<T>::kThreads, 2)
     chunk_state_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap bmap,
-                       const __grid_constant__ CUtensorMap smap, Dims d, const float* __restrict__ cumsum,
-                       const float* __restrict__ dt_t, int* status, uint64_t spin_ns) {
+                       const __grid_constant__ CUtensorMap smap, Dims d, float* __restrict__ cumsum,
+                       float* __restrict__ dt_t, const float* __restrict__ dt, const float* __restrict__ A,
+                       int* chain, int nchain, int* status, uint64_t spin_ns) {
   using C = StateCfg<T>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -107,10 +109,44 @@ __global__ void __launch_bounds__(StateCfg<T>::kThreads, 2)
     tmem_alloc(tmem_holder, tmem_cols);
     tmem_relinquish();
   }
-  grid_dep_wait();  // chunk_cumsum's results are visible from here on
+  grid_dep_wait();  // the kernel before (chunk_cumsum, when it ran) is complete from here on
   grid_dep_launch();
-  if (warp >= 2) {
-    // token weights w_j = exp(G_last - G_j) * dt_j for both heads (exponent <= 0)
+  // token weights w_j = exp(G_last - G_j) * dt_j for both heads (exponent <= 0)
+  if (dt) {
+    // The chunk's cumsum formed here (dt non-null; one piece, Q <= 256): one warp per head of
+    // the pair, the rows written for state_passing and compute_out exactly as chunk_cumsum
+    // writes them.  As the call's first kernel, CTA (0, 0, 0) clears the status word and the
+    // first `nchain` one-pass counters.
+    if (nchain >= 0 && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0) {
+      if (threadIdx.x == 0) *status = 0;
+      for (int k = threadIdx.x; k < nchain; k += C::kThreads) chain[k] = 0;
+    }
+    if (warp == 2 || warp == 3) {
+      const int hl = warp - 2, h = h0 + hl;
+      const int per = Q / 32;  // 2, 4 or 8 tokens per lane
+      const int64_t row = (static_cast<int64_t>(b) * d.H + h) * d.Lp + static_cast<int64_t>(c) * Q;
+      float v[8], gv[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int tok = c * Q + lane * per + k;
+        v[k] = (k < per && tok < d.L) ? dt[(static_cast<int64_t>(b) * d.L + tok) * d.H + h] : 0.f;
+      }
+      float carry = 0.f;
+      cumsum_piece(v, per, A[h], carry, gv);
+      // the chunk's last value (per is 2, 4 or 8; constant indices keep gv in registers)
+      const float gl = per == 2 ? gv[1] : per == 4 ? gv[3] : gv[7];
+      const float glast = __shfl_sync(0xffffffffu, gl, 31);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        if (k < per) {
+          const int j = lane * per + k;
+          cumsum[row + j] = gv[k];
+          dt_t[row + j] = v[k];
+          w_s[hl * Q + j] = expf(glast - gv[k]) * v[k];
+        }
+      }
+    }
+  } else if (warp >= 2) {
     for (int idx = threadIdx.x - 64; idx < 2 * Q; idx += 128) {
       const int hl = idx / Q, j = idx % Q;
       const int64_t row = (static_cast<int64_t>(b) * d.H + h0 + hl) * d.Lp + static_cast<int64_t>(c) * Q;
@@ -289,7 +325,7 @@ __global__ void __launch_bounds__(StateCfg<T>::kThreads, 2)
 
 template <typename T>
 cudaError_t launch_impl(const Dims& d, const ChunkStateMaps& maps, const Work& w, uint64_t spin_ns,
-                        cudaStream_t stream, bool dependent) {
+                        cudaStream_t stream, bool dependent, const float* dt, const float* A, int nchain) {
   using C = StateCfg<T>;
   const uint32_t stage_bytes = state_stage_bytes(d.N, C::kAtom, C::kBox, C::kABytes);
   const int ns = state_stages(stage_bytes, C::kRingBytes, C::kMaxStages);
@@ -302,16 +338,18 @@ cudaError_t launch_impl(const Dims& d, const ChunkStateMaps& maps, const Work& w
     configured = smem;
   }
   const dim3 grid(d.H / 2, d.nc, d.B);
+  if (dt && d.Q > 256) return cudaErrorInvalidValue;  // the in-kernel cumsum takes one piece
   return launch_k(chunk_state_kernel<T>, grid, dim3(C::kThreads), smem, stream, dependent, maps.x, maps.bm, maps.s, d,
-                  static_cast<const float*>(w.cumsum), static_cast<const float*>(w.dt_t), w.status, spin_ns);
+                  w.cumsum, w.dt_t, dt, A, w.counter, nchain, w.status, spin_ns);
 }
 
 }  // namespace
 
 cudaError_t launch_chunk_state(const Dims& d, bool bf16, const ChunkStateMaps& maps, const Work& w,
-                               uint64_t spin_ns, cudaStream_t stream, bool dependent) {
-  return bf16 ? launch_impl<__nv_bfloat16>(d, maps, w, spin_ns, stream, dependent)
-              : launch_impl<float>(d, maps, w, spin_ns, stream, dependent);
+                               uint64_t spin_ns, cudaStream_t stream, bool dependent, const float* dt,
+                               const float* A, int nchain) {
+  return bf16 ? launch_impl<__nv_bfloat16>(d, maps, w, spin_ns, stream, dependent, dt, A, nchain)
+              : launch_impl<float>(d, maps, w, spin_ns, stream, dependent, dt, A, nchain);
 }
 
 }  // namespace ssd

@@ -331,7 +331,7 @@ size_t ssd_fwd_workspace_size(const ssd_shape* shape) {
 int ssd_fwd_kernel_count(const ssd_shape* shape) {
   if (ssd_validate_shape(shape) != SSD_OK || empty_problem(*shape)) return 0;
   const int sched = schedule_of(*shape);
-  return sched == 1 ? 2 : sched == 2 ? 5 : 4;
+  return sched == 1 ? 2 : sched == 2 ? 5 : 3;
 }
 
 ssd_status ssd_chunk_cumsum(const ssd_shape* shape, const float* dt, const float* A, void* workspace,
@@ -543,15 +543,15 @@ ssd_status fwd_impl(int path, int first, int end, const ssd_shape* shape, const 
   if (!build_state_maps(*shape, x, Bm, w.states, &smaps) || !build_out_maps(*shape, x, Bm, Cm, hp, y, &omaps))
     return SSD_ERR_CUDA;
   const uint64_t spin = spin_limit_ns();
-  // fp32: the chunk_cumsum launch also transposes Bm once for every head of its group
-  step([&](bool) { return launch_chunk_cumsum(d, dt, A, w, cs); });
-  // chunk_state and compute_out are programmatic dependents of the kernel before them (their
-  // launch and prologue overlap its tail).  state_passing is one only while chunk_state runs
-  // in a single wave (two CTAs per SM): launched early beside a later wave, its blocks slowed
-  // long sequences (16k tokens x dstate 256: 0.397 against 0.381 ms), while on a one-wave
-  // problem the early launch saves about 1 us (370M layer: 0.0897 against 0.0908 ms).
+  // chunk_state forms each chunk's cumsum itself (no chunk_cumsum launch) and, as the first
+  // kernel, clears the status word and the one-pass counters.  compute_out is a programmatic dependent of the kernel
+  // before it (its launch and prologue overlap that kernel's tail).  state_passing is one only
+  // while chunk_state runs in a single wave (two CTAs per SM): launched early beside a later
+  // wave, its blocks slowed long sequences (16k tokens x dstate 256: 0.397 against 0.381 ms),
+  // while on a one-wave problem the early launch saves about 1 us (370M layer: 0.0897 against
+  // 0.0908 ms).
   const bool one_wave = static_cast<int64_t>(d.B) * d.nc * (d.H / 2) <= 2 * static_cast<int64_t>(sm_count());
-  step([&](bool dep) { return launch_chunk_state(d, bf16, smaps, w, spin, cs, dep); });
+  step([&](bool dep) { return launch_chunk_state(d, bf16, smaps, w, spin, cs, dep, dt, A, 1 + d.B * (d.H / 2)); });
   step([&](bool dep) { return launch_state_passing(d, bf16, init_state, final_state, w, cs, one_wave && dep); });
   step([&](bool dep) { return launch_compute_out(d, bf16, omaps, D, x, y, w, spin, cs, dep); });
   return from_cuda(e);

@@ -76,8 +76,12 @@ cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t sme
 
 cudaError_t launch_chunk_cumsum(const Dims& d, const float* dt, const float* A, const Work& w,
                                 cudaStream_t stream);
+// dt non-null (Q <= 256): chunk_state forms the chunk cumsum itself and writes the cumsum and
+// dt_t rows (chunk_cumsum need not run); nchain >= 0 makes it the call's first kernel, which
+// clears the status word and that many one-pass counters.  dt null: it reads chunk_cumsum's rows.
 cudaError_t launch_chunk_state(const Dims& d, bool bf16, const ChunkStateMaps& maps, const Work& w,
-                               uint64_t spin_ns, cudaStream_t stream, bool dependent = false);
+                               uint64_t spin_ns, cudaStream_t stream, bool dependent = false,
+                               const float* dt = nullptr, const float* A = nullptr, int nchain = -1);
 // hprev32 (bf16 problems): write the entering states in fp32 there instead of bf16 into
 // w.states_bf16 (the segmented one-pass schedule)
 cudaError_t launch_state_passing(const Dims& d, bool bf16, const float* init, float* final_state,

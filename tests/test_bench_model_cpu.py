@@ -11,7 +11,7 @@ import pytest
 import bench
 import ssd_synth
 
-STAGED = ("chunk_cumsum", "chunk_state", "state_passing", "compute_out")
+STAGED = ("chunk_state", "state_passing", "compute_out")
 
 
 @pytest.mark.parametrize("name", ["tiny", "mamba2-370m", "mamba2-2.7b", "long-16k-n256", "sweep-L2048-N256-Q128"])

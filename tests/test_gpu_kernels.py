@@ -99,11 +99,12 @@ def test_compute_out_causal_upper_triangle_is_exactly_zero():
 @pytest.mark.parametrize("name,over", [CASES[1], CASES[3], CASES[5]], ids=[CASES[1][0], CASES[3][0], CASES[5][0]])
 def test_full_forward_equals_the_four_steps(name, over):
     """ssd_fwd on the staged schedule (fp32 inputs; bf16 at dstate 256) gives
-    bit for bit what the four step calls give in order: the full forward chains
-    the kernels with programmatic dependent launch, which may not change a
-    result."""
+    bit for bit what the four step calls give in order: the full forward forms
+    the chunk cumsum inside chunk_state (three launches, the same scan as the
+    chunk_cumsum kernel) and chains the kernels with programmatic dependent
+    launch, and neither may change a result."""
     ssd, w, inp, d, shape, ws = _setup(over)
-    assert ssd.ssd_fwd_kernel_count(shape) == 4
+    assert ssd.ssd_fwd_kernel_count(shape) == 3
     B, L, H = inp["dt"].shape
     y1, f1 = ssd.ssd_fwd(d["x"], d["dt"], d["A"], d["Bm"], d["Cm"], d["D"], w.chunk_size,
                          init_state=d.get("init"), workspace=ws)
@@ -118,6 +119,8 @@ def test_full_forward_equals_the_four_steps(name, over):
     torch.cuda.synchronize()
     assert torch.equal(y1, y2)
     assert torch.equal(f1, f2)
+    v1, v2 = ssd.workspace_views(shape, ws), ssd.workspace_views(shape, ws2)
+    assert torch.equal(v1["cumsum"], v2["cumsum"]) and torch.equal(v1["dt_t"], v2["dt_t"])
 
 
 @pytest.mark.parametrize("over", [CASES[1][1], CASES[3][1], CASES[4][1],
