@@ -30,7 +30,10 @@
 //
 // Warp roles (192 threads): warp 0 issues TMA, warp 1 owns TMEM and issues
 // the MMAs (one thread), warps 2-5 compute the weights, transform each stage
-// and write S_c.  A ring of 2-4 stages (as many as fit 96 KB; mbarriers full ->
+// and write S_c.  On the staged schedule the weights start from the chunk's
+// cumsum of dt*A, which warps 2 and 3 form here (one head each, the scan of
+// chunk_scan.cuh) and write to the workspace for the kernels after this one,
+// so that schedule has no chunk_cumsum launch.  A ring of 2-4 stages (as many as fit 96 KB; mbarriers full ->
 // scaled -> empty) pipelines the 32-token stages.  All waits are bounded
 // (device-timeout status, no hang).
 #include "chunk_scan.cuh"
