@@ -20,6 +20,11 @@ CASES = [
     ("f32-N256-Q128-ragged", dict(seqlen=300, nheads=4, dstate=256, chunk_size=128, init_state=True)),
     ("bf16-N64-Q64-G2", dict(batch=2, seqlen=200, nheads=8, ngroups=2, dstate=64, chunk_size=64, dtype="bf16")),
     ("bf16-N256-Q256-G2", dict(seqlen=700, nheads=4, ngroups=2, dstate=256, chunk_size=256, dtype="bf16")),
+    # dstate 256 with four heads per group, two groups
+    ("bf16-N256-Q128-G2-quad", dict(batch=2, seqlen=400, nheads=8, ngroups=2, dstate=256, chunk_size=128,
+                                     dtype="bf16", init_state=True)),
+    ("f32-N256-Q64-G2-quad", dict(batch=2, seqlen=200, nheads=8, ngroups=2, dstate=256, chunk_size=64,
+                                   init_state=True)),
 ]
 
 
@@ -96,7 +101,8 @@ def test_compute_out_causal_upper_triangle_is_exactly_zero():
     assert torch.isfinite(y1).all()
 
 
-@pytest.mark.parametrize("name,over", [CASES[1], CASES[3], CASES[5]], ids=[CASES[1][0], CASES[3][0], CASES[5][0]])
+@pytest.mark.parametrize("name,over", [CASES[1], CASES[3], CASES[5], CASES[7]],
+                         ids=[CASES[1][0], CASES[3][0], CASES[5][0], CASES[7][0]])
 def test_full_forward_equals_the_four_steps(name, over):
     """ssd_fwd on the staged schedule (fp32 inputs; bf16 at dstate 256) gives
     bit for bit what the four step calls give in order: the full forward forms
