@@ -351,6 +351,10 @@ cudaError_t launch_impl(const Dims& d, const ChunkStateMaps& maps, const Work& w
 cudaError_t launch_chunk_state(const Dims& d, bool bf16, const ChunkStateMaps& maps, const Work& w,
                                uint64_t spin_ns, cudaStream_t stream, bool dependent, const float* dt,
                                const float* A, int nchain) {
+  // fp32 at dstate 256 with the cumsum formed in-kernel: one persistent CTA per SM walking its
+  // units with two accumulators (chunk_state_persistent.cu)
+  if (!bf16 && d.N == 256 && dt && d.Q <= 256)
+    return launch_chunk_state_persistent(d, maps, w, spin_ns, stream, dependent, dt, A, nchain);
   return bf16 ? launch_impl<__nv_bfloat16>(d, maps, w, spin_ns, stream, dependent, dt, A, nchain)
               : launch_impl<float>(d, maps, w, spin_ns, stream, dependent, dt, A, nchain);
 }

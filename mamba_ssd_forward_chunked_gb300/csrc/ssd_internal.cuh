@@ -82,6 +82,10 @@ cudaError_t launch_chunk_cumsum(const Dims& d, const float* dt, const float* A, 
 cudaError_t launch_chunk_state(const Dims& d, bool bf16, const ChunkStateMaps& maps, const Work& w,
                                uint64_t spin_ns, cudaStream_t stream, bool dependent = false,
                                const float* dt = nullptr, const float* A = nullptr, int nchain = -1);
+// The persistent form launch_chunk_state takes for fp32 at dstate 256 with dt non-null (Q <= 256).
+cudaError_t launch_chunk_state_persistent(const Dims& d, const ChunkStateMaps& maps, const Work& w, uint64_t spin_ns,
+                                          cudaStream_t stream, bool dependent, const float* dt, const float* A,
+                                          int nchain);
 // hprev32 (bf16 problems): write the entering states in fp32 there instead of bf16 into
 // w.states_bf16 (the segmented one-pass schedule)
 cudaError_t launch_state_passing(const Dims& d, bool bf16, const float* init, float* final_state,
