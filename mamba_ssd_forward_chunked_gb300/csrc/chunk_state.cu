@@ -150,10 +150,12 @@ __global__ void __launch_bounds__(StateCfg<T>::kThreads, 2)
       }
     }
   } else if (warp >= 2) {
+    // chunk_cumsum's rows, read-only here (non-coherent loads, several in flight)
+#pragma unroll 4
     for (int idx = threadIdx.x - 64; idx < 2 * Q; idx += 128) {
       const int hl = idx / Q, j = idx % Q;
       const int64_t row = (static_cast<int64_t>(b) * d.H + h0 + hl) * d.Lp + static_cast<int64_t>(c) * Q;
-      w_s[idx] = expf(cumsum[row + Q - 1] - cumsum[row + j]) * dt_t[row + j];
+      w_s[idx] = expf(__ldg(cumsum + row + Q - 1) - __ldg(cumsum + row + j)) * __ldg(dt_t + row + j);
     }
   }
   tc_fence_before();
