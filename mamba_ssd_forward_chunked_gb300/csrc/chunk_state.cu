@@ -114,49 +114,11 @@ __global__ void __launch_bounds__(StateCfg<T>::kThreads, 2)
   }
   grid_dep_wait();  // the kernel before (chunk_cumsum, when it ran) is complete from here on
   grid_dep_launch();
-  // token weights w_j = exp(G_last - G_j) * dt_j for both heads (exponent <= 0)
-  if (dt) {
-    // The chunk's cumsum formed here (dt non-null; one piece, Q <= 256): one warp per head of
-    // the pair, the rows written for state_passing and compute_out exactly as chunk_cumsum
-    // writes them.  As the call's first kernel, CTA (0, 0, 0) clears the status word and the
-    // first `nchain` one-pass counters.
-    if (nchain >= 0 && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0) {
-      if (threadIdx.x == 0) *status = 0;
-      for (int k = threadIdx.x; k < nchain; k += C::kThreads) chain[k] = 0;
-    }
-    if (warp == 2 || warp == 3) {
-      const int hl = warp - 2, h = h0 + hl;
-      const int per = Q / 32;  // 2, 4 or 8 tokens per lane
-      const int64_t row = (static_cast<int64_t>(b) * d.H + h) * d.Lp + static_cast<int64_t>(c) * Q;
-      float v[8], gv[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const int tok = c * Q + lane * per + k;
-        v[k] = (k < per && tok < d.L) ? dt[(static_cast<int64_t>(b) * d.L + tok) * d.H + h] : 0.f;
-      }
-      float carry = 0.f;
-      cumsum_piece(v, per, A[h], carry, gv);
-      // the chunk's last value (per is 2, 4 or 8; constant indices keep gv in registers)
-      const float gl = per == 2 ? gv[1] : per == 4 ? gv[3] : gv[7];
-      const float glast = __shfl_sync(0xffffffffu, gl, 31);
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        if (k < per) {
-          const int j = lane * per + k;
-          cumsum[row + j] = gv[k];
-          dt_t[row + j] = v[k];
-          w_s[hl * Q + j] = expf(glast - gv[k]) * v[k];
-        }
-      }
-    }
-  } else if (warp >= 2) {
-    // chunk_cumsum's rows, read-only here (non-coherent loads, several in flight)
-#pragma unroll 4
-    for (int idx = threadIdx.x - 64; idx < 2 * Q; idx += 128) {
-      const int hl = idx / Q, j = idx % Q;
-      const int64_t row = (static_cast<int64_t>(b) * d.H + h0 + hl) * d.Lp + static_cast<int64_t>(c) * Q;
-      w_s[idx] = expf(__ldg(cumsum + row + Q - 1) - __ldg(cumsum + row + j)) * __ldg(dt_t + row + j);
-    }
+  // As the call's first kernel (dt non-null, nchain >= 0), CTA (0, 0, 0) clears the status
+  // word and the first `nchain` one-pass counters.
+  if (dt && nchain >= 0 && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0) {
+    if (threadIdx.x == 0) *status = 0;
+    for (int k = threadIdx.x; k < nchain; k += C::kThreads) chain[k] = 0;
   }
   tc_fence_before();
   __syncthreads();
@@ -216,6 +178,47 @@ __global__ void __launch_bounds__(StateCfg<T>::kThreads, 2)
       mma_commit(accum);
     }
   } else {
+    // token weights w_j = exp(G_last - G_j) * dt_j for both heads (exponent <= 0), while the
+    // producer's first loads are in flight
+    if (dt) {
+      // The chunk's cumsum formed here (dt non-null; one piece, Q <= 256): one warp per head of
+      // the pair, the rows written for state_passing and compute_out exactly as chunk_cumsum
+      // writes them.
+      if (warp == 2 || warp == 3) {
+        const int hl = warp - 2, h = h0 + hl;
+        const int per = Q / 32;  // 2, 4 or 8 tokens per lane
+        const int64_t row = (static_cast<int64_t>(b) * d.H + h) * d.Lp + static_cast<int64_t>(c) * Q;
+        float v[8], gv[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int tok = c * Q + lane * per + k;
+          v[k] = (k < per && tok < d.L) ? dt[(static_cast<int64_t>(b) * d.L + tok) * d.H + h] : 0.f;
+        }
+        float carry = 0.f;
+        cumsum_piece(v, per, A[h], carry, gv);
+        // the chunk's last value (per is 2, 4 or 8; constant indices keep gv in registers)
+        const float gl = per == 2 ? gv[1] : per == 4 ? gv[3] : gv[7];
+        const float glast = __shfl_sync(0xffffffffu, gl, 31);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          if (k < per) {
+            const int j = lane * per + k;
+            cumsum[row + j] = gv[k];
+            dt_t[row + j] = v[k];
+            w_s[hl * Q + j] = expf(glast - gv[k]) * v[k];
+          }
+        }
+      }
+    } else {
+      // chunk_cumsum's rows, read-only here (non-coherent loads, several in flight)
+#pragma unroll 4
+      for (int idx = threadIdx.x - 64; idx < 2 * Q; idx += 128) {
+        const int hl = idx / Q, j = idx % Q;
+        const int64_t row = (static_cast<int64_t>(b) * d.H + h0 + hl) * d.Lp + static_cast<int64_t>(c) * Q;
+        w_s[idx] = expf(__ldg(cumsum + row + Q - 1) - __ldg(cumsum + row + j)) * __ldg(dt_t + row + j);
+      }
+    }
+    named_bar_sync(1, 128);  // w_s complete for the four scaling warps
     const int et = threadIdx.x - 64;
     for (int it = 0; it < nstages; ++it) {
       const int s = it % NS, r = it / NS;
